@@ -1,0 +1,165 @@
+/*
+ * bakron.h - C ABI of the BaKron solver library (libbakron.so), GB300 / sm_103a.
+ *
+ * BaKron ("BaKron: Efficient Quantization with Kronecker-Factored Hessians",
+ * Birnick & Saab) returns the matrix V that GPTQ produces on vec(W) when the
+ * Hessian is the Kronecker product A (x) B.  W is m x n; A (n x n) is the
+ * input-side factor (columns of W), B (m x m) the output-side factor (rows
+ * of W); vec is column-major, so entry (i, j) is vec index i + m j.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Matrices are dense, row-major, contiguous, fp32 (codes: int8).
+ * - Pointers named "host" are host memory; every other pointer is DEVICE
+ *   memory on the current CUDA device, owned by the caller.  The library
+ *   never allocates, frees or retains device memory: the caller passes a
+ *   workspace of at least the size the matching *_workspace_size call
+ *   reports.  Inputs are read-only; outputs must not alias inputs, each
+ *   other or the workspace.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *   enqueued on it; every compute call then synchronises the stream and reads
+ *   back a device status word, so the returned status is final.  Outputs are
+ *   unspecified when the status is not BAKRON_OK.
+ * - Argument validation happens before anything is enqueued and returns
+ *   BAKRON_ERR_INVALID_ARG with no side effects (no CUDA call is made).
+ */
+#ifndef BAKRON_H
+#define BAKRON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BAKRON_OK = 0,
+  BAKRON_ERR_INVALID_ARG = 1,  /* bad pointer, size, grid or workspace size */
+  BAKRON_ERR_NOT_PD = 2,       /* prepare: a factor is not positive definite */
+  BAKRON_ERR_NONFINITE = 3,    /* a NaN/Inf input or intermediate value */
+  BAKRON_ERR_CODE_RANGE = 4,   /* a code falls outside int8 (unclamped grids) */
+  BAKRON_ERR_TIMEOUT = 5,      /* a bounded device wait ran out */
+  BAKRON_ERR_UNSUPPORTED = 6,  /* device or launch configuration not supported */
+  BAKRON_ERR_CUDA = 7          /* a CUDA runtime/driver call failed */
+} bakron_status;
+
+/* Per-phase device times of one bakron_quantize call, filled when
+ * bakron_opts.times is non-NULL (CUDA events around each launch, on the
+ * call's stream).  Flop counts are 2 per multiply-add of the propagation
+ * products as executed (dense T x T tile products), before any precision
+ * split. */
+typedef struct {
+  double leaf_ms;         /* leaf sweeps (anti-diagonal steps inside tiles) */
+  double prop1_ms;        /* propagation stage 1: Y^T = U_A^T E_P^T */
+  double prop2_ms;        /* propagation stage 2: W~_Q -= U_B^T Y */
+  double other_ms;        /* padding, factor transposition/split */
+  double prop_flops;      /* executed propagation flops (both stages) */
+  int64_t leaf_launches;
+  int64_t prop_launches;  /* launches of the propagation product kernel */
+  int64_t other_launches;
+} bakron_phase_times;
+
+typedef struct {
+  int tile;                 /* tile edge T; only 128 is supported (0 = 128) */
+  int leaf_width;           /* tile anti-diagonals per leaf; only 1 (0 = 1) */
+  int use_3xtf32;           /* propagation products: 1 = tcgen05 tensor cores
+                               with a 3xTF32 split, 0 = fp32 FMA; the default
+                               is 1 where the tensor-core kernel is built */
+  long long spin_budget_cycles; /* bound of every device spin-wait, in SM
+                               clock cycles (0 = 4e9) */
+  int fault_inject;         /* test hook, bakron_quantize_antidiag only: one
+                               CTA skips its first grid-barrier arrival, so
+                               the others time out (BAKRON_ERR_TIMEOUT) */
+  bakron_phase_times* times; /* host; NULL = no per-phase timing */
+} bakron_opts;
+
+/* Fill `opts` with the defaults above. */
+void bakron_default_opts(bakron_opts* opts);
+
+/* Static message for a status code (never NULL). */
+const char* bakron_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int bakron_version(void);
+
+/* Workspace bytes bakron_quantize / bakron_quantize_antidiag need for an
+ * m x n problem (written to *bytes, host).  Pure host arithmetic. */
+bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts,
+                                    size_t* bytes);
+
+/* Workspace bytes bakron_prepare needs for factors of order n and m
+ * (either may be 0 when that factor is not prepared).  Pure host arithmetic. */
+bakron_status bakron_prepare_workspace_size(int64_t n, int64_t m, size_t* bytes);
+
+/* Row grid of the per-row symmetric quantizer (the base quantizer Q, which
+ * the abstract calls modular): scale[i] = max_j |W[i,j]| / qmax in fp32,
+ * and 1 for an all-zero row.  W: m x n (device); scale: m (device).
+ * qmax >= 1. */
+bakron_status bakron_rowscale(const float* W, int64_t m, int64_t n, int qmax,
+                              float* scale, void* stream);
+
+/* Factor preparation (Corollary 3.4 on the summary page "FastKron: Efficient
+ * Quantization with Kronecker-Factored Hessians" names L(A) = RevCholesky(A)).
+ * For each factor X of order k (A with n, B with m):
+ *   X_d = X + damp * mean(diag X) * I,
+ *   L   = RevCholesky(X_d): lower triangular with X_d = L^T L,
+ *   U   = L^{-T}: upper triangular with U^T U = X_d^{-1} (the GPTQ update
+ *         factor; its diagonal is 1/diag(L)).
+ * Outputs are full k x k row-major matrices with zeros in the other
+ * triangle.  B may be NULL (m = 0) to prepare A only.  UA/UB required;
+ * LA/LB nullable.  info (host, nullable, 2 entries): failing pivot index
+ * of A and of B in the original index order, -1 when that factor is
+ * positive definite; a failure returns BAKRON_ERR_NOT_PD.  ws: device
+ * workspace of bakron_prepare_workspace_size(n, m) bytes. */
+bakron_status bakron_prepare(const float* A, int64_t n, float damp_A,
+                             const float* B, int64_t m, float damp_B,
+                             float* UA, float* UB, float* LA, float* LB,
+                             int64_t* info, void* ws, size_t ws_bytes, void* stream);
+
+/* The BaKron solver (section 3 of the summary page): anti-diagonal
+ * parallelism plus divide and conquer over the anti-diagonal dimension.
+ *   W      m x n     weights
+ *   UA     n x n     U_A = L(A)^{-T} as written by bakron_prepare (upper;
+ *                    the strictly lower triangle is ignored)
+ *   UB     m x m     U_B = L(B)^{-T} (upper; likewise)
+ *   scale  m         per-row grid step s_i > 0
+ *   qmin, qmax       code clamp; INT32_MIN / INT32_MAX = no clamp
+ *   V      m x n     out: V = s_i * code
+ *   codes  m x n     out: int8 codes (BAKRON_ERR_CODE_RANGE if one does
+ *                    not fit)
+ *   preround m x n   out, nullable: each entry's value when it was rounded
+ * Every entry is rounded as c = clamp(rint(w~ / s_i)) (fp32 quotient, round
+ * half to even); its scaled error E = (w~ - s_i c) l^B_i l^A_j with
+ * l = 1/diag(U) updates w~[i',j'] -= U_B[i,i'] E U_A[j,j'] for all i' >= i,
+ * j' >= j.  opts: nullable (defaults).  ws: bakron_workspace_size bytes. */
+bakron_status bakron_quantize(const float* W, int64_t m, int64_t n,
+                              const float* UA, const float* UB,
+                              const float* scale, int qmin, int qmax,
+                              float* V, int8_t* codes, float* preround,
+                              const bakron_opts* opts, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* BaKron-antidiagonal (section 3 of the summary page; equivalent to YAQA):
+ * one persistent grid-synchronised kernel, m + n - 1 steps, each rounding
+ * one anti-diagonal and applying U_B^T E_d U_A to the entries on later
+ * anti-diagonals.  Same arguments and result as bakron_quantize (a
+ * cross-check variant, O(m^2 n^2) work).  guide_codes (nullable, m x n
+ * int8): where this kernel's own pre-rounding value lies within guide_tol
+ * grid units of a rounding boundary it takes the guide's code instead of
+ * its own decision; *overrides (host, nullable) receives how many such
+ * entries differed from its own decision. */
+bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n,
+                                       const float* UA, const float* UB,
+                                       const float* scale, int qmin, int qmax,
+                                       float* V, int8_t* codes, float* preround,
+                                       const int8_t* guide_codes, float guide_tol,
+                                       int64_t* overrides,
+                                       const bakron_opts* opts, void* ws, size_t ws_bytes,
+                                       void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BAKRON_H */

@@ -1,0 +1,280 @@
+"""Thin ctypes binding over libbakron.so (argument marshalling only).
+
+Every function here checks tensor devices/dtypes/shapes, allocates outputs
+and workspaces with PyTorch (device memory and streams are all PyTorch is used
+for), and calls the C entry point of the same name; every step of the solver
+runs in the library's CUDA kernels.  There is no CPU path: if the library has
+not been built, or no CUDA device is present, the first call raises.
+"""
+
+import ctypes
+import os
+
+_LIB = None
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbakron.so")
+
+OK = 0
+STATUS = {0: "BAKRON_OK", 1: "BAKRON_ERR_INVALID_ARG", 2: "BAKRON_ERR_NOT_PD",
+          3: "BAKRON_ERR_NONFINITE", 4: "BAKRON_ERR_CODE_RANGE", 5: "BAKRON_ERR_TIMEOUT",
+          6: "BAKRON_ERR_UNSUPPORTED", 7: "BAKRON_ERR_CUDA"}
+INT32_MIN = -(1 << 31)
+INT32_MAX = (1 << 31) - 1
+
+EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version",
+           "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
+           "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag"]
+
+
+class PhaseTimes(ctypes.Structure):
+    _fields_ = [("leaf_ms", ctypes.c_double), ("prop1_ms", ctypes.c_double),
+                ("prop2_ms", ctypes.c_double), ("other_ms", ctypes.c_double),
+                ("prop_flops", ctypes.c_double), ("leaf_launches", ctypes.c_int64),
+                ("prop_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int), ("leaf_width", ctypes.c_int), ("use_3xtf32", ctypes.c_int),
+                ("spin_budget_cycles", ctypes.c_longlong), ("fault_inject", ctypes.c_int),
+                ("times", ctypes.POINTER(PhaseTimes))]
+
+
+class BakronError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = lib().bakron_status_string(status).decode()
+        super().__init__("%s: %s (%s)" % (where, STATUS.get(status, status), msg))
+
+
+def lib():
+    """Load libbakron.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libbakron.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    L.bakron_default_opts.argtypes = [ctypes.POINTER(Opts)]
+    L.bakron_default_opts.restype = None
+    L.bakron_status_string.argtypes = [ctypes.c_int]
+    L.bakron_status_string.restype = ctypes.c_char_p
+    L.bakron_version.restype = ctypes.c_int
+    L.bakron_workspace_size.argtypes = [i64, i64, ctypes.POINTER(Opts), ctypes.POINTER(sz)]
+    L.bakron_prepare_workspace_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
+    L.bakron_rowscale.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp]
+    L.bakron_prepare.argtypes = [vp, i64, ctypes.c_float, vp, i64, ctypes.c_float,
+                                 vp, vp, vp, vp, ctypes.POINTER(i64), vp, sz, vp]
+    L.bakron_quantize.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                  vp, vp, vp, ctypes.POINTER(Opts), vp, sz, vp]
+    L.bakron_quantize_antidiag.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                           vp, vp, vp, vp, ctypes.c_float, ctypes.POINTER(i64),
+                                           ctypes.POINTER(Opts), vp, sz, vp]
+    for f in ("bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
+              "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag"):
+        getattr(L, f).restype = ctypes.c_int
+    _LIB = L
+    return L
+
+
+def default_opts(**kw):
+    o = Opts()
+    lib().bakron_default_opts(ctypes.byref(o))
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def _check(st, where):
+    if st != OK:
+        raise BakronError(st, where)
+
+
+def _torch():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the BaKron library runs on the GPU only")
+    return torch
+
+
+def _dev(t, dtype, shape, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_size(m, n, opts=None):
+    b = ctypes.c_size_t(0)
+    _check(lib().bakron_workspace_size(m, n, ctypes.byref(opts) if opts else None, ctypes.byref(b)),
+           "bakron_workspace_size")
+    return b.value
+
+
+def prepare_workspace_size(n, m):
+    b = ctypes.c_size_t(0)
+    _check(lib().bakron_prepare_workspace_size(n, m, ctypes.byref(b)), "bakron_prepare_workspace_size")
+    return b.value
+
+
+def _ws(nbytes, workspace):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small: need %d bytes" % nbytes)
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def bakron_rowscale(W, qmax, out=None, stream=None):
+    torch = _torch()
+    m, n = W.shape
+    if out is None:
+        out = torch.empty(m, dtype=torch.float32, device=W.device)
+    _check(lib().bakron_rowscale(_dev(W, torch.float32, (m, n), "W"), m, n, int(qmax),
+                                 _dev(out, torch.float32, (m,), "scale"), _stream(stream)),
+           "bakron_rowscale")
+    return out
+
+
+def bakron_prepare(A, damp_A, B=None, damp_B=0.0, want_L=False, workspace=None, stream=None,
+                   out=None):
+    """Returns (UA, UB, LA, LB, info); UB/LB are None when B is None."""
+    torch = _torch()
+    n = A.shape[0]
+    m = 0 if B is None else B.shape[0]
+    if out is not None:
+        UA, UB = out
+    else:
+        UA = torch.empty((n, n), dtype=torch.float32, device=A.device)
+        UB = None if B is None else torch.empty((m, m), dtype=torch.float32, device=A.device)
+    LA = torch.empty_like(UA) if want_L else None
+    LB = torch.empty_like(UB) if (want_L and B is not None) else None
+    nb = prepare_workspace_size(n, m)
+    ws = _ws(nb, workspace)
+    info = (ctypes.c_int64 * 2)(-1, -1)
+    st = lib().bakron_prepare(
+        _dev(A, torch.float32, (n, n), "A"), n, float(damp_A),
+        None if B is None else _dev(B, torch.float32, (m, m), "B"), m, float(damp_B),
+        _dev(UA, torch.float32, (n, n), "UA"),
+        None if UB is None else _dev(UB, torch.float32, (m, m), "UB"),
+        None if LA is None else _dev(LA, torch.float32, (n, n), "LA"),
+        None if LB is None else _dev(LB, torch.float32, (m, m), "LB"),
+        info, ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
+    if st != OK:
+        err = BakronError(st, "bakron_prepare")
+        err.info = (info[0], info[1])
+        raise err
+    return UA, UB, LA, LB, (info[0], info[1])
+
+
+def bakron_quantize(W, UA, UB, scale, qmin, qmax, want_preround=False, opts=None, workspace=None,
+                    stream=None, out=None):
+    """Returns (V, codes, preround-or-None)."""
+    torch = _torch()
+    m, n = W.shape
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        codes = torch.empty((m, n), dtype=torch.int8, device=W.device)
+    else:
+        V, codes = out
+    pre = torch.empty((m, n), dtype=torch.float32, device=W.device) if want_preround else None
+    nb = workspace_size(m, n, opts)
+    ws = _ws(nb, workspace)
+    st = lib().bakron_quantize(
+        _dev(W, torch.float32, (m, n), "W"), m, n,
+        _dev(UA, torch.float32, (n, n), "UA"), _dev(UB, torch.float32, (m, m), "UB"),
+        _dev(scale, torch.float32, (m,), "scale"), int(qmin), int(qmax),
+        _dev(V, torch.float32, (m, n), "V"), _dev(codes, torch.int8, (m, n), "codes"),
+        None if pre is None else _dev(pre, torch.float32, (m, n), "preround"),
+        ctypes.byref(opts) if opts is not None else None,
+        ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
+    _check(st, "bakron_quantize")
+    return V, codes, pre
+
+
+def bakron_quantize_antidiag(W, UA, UB, scale, qmin, qmax, guide_codes=None, guide_tol=1e-4,
+                             want_preround=False, opts=None, workspace=None, stream=None):
+    """Returns (V, codes, preround-or-None, overrides)."""
+    torch = _torch()
+    m, n = W.shape
+    V = torch.empty((m, n), dtype=torch.float32, device=W.device)
+    codes = torch.empty((m, n), dtype=torch.int8, device=W.device)
+    pre = torch.empty((m, n), dtype=torch.float32, device=W.device) if want_preround else None
+    nb = workspace_size(m, n, opts)
+    ws = _ws(nb, workspace)
+    over = ctypes.c_int64(0)
+    st = lib().bakron_quantize_antidiag(
+        _dev(W, torch.float32, (m, n), "W"), m, n,
+        _dev(UA, torch.float32, (n, n), "UA"), _dev(UB, torch.float32, (m, m), "UB"),
+        _dev(scale, torch.float32, (m,), "scale"), int(qmin), int(qmax),
+        _dev(V, torch.float32, (m, n), "V"), _dev(codes, torch.int8, (m, n), "codes"),
+        None if pre is None else _dev(pre, torch.float32, (m, n), "preround"),
+        None if guide_codes is None else _dev(guide_codes, torch.int8, (m, n), "guide_codes"),
+        float(guide_tol), ctypes.byref(over),
+        ctypes.byref(opts) if opts is not None else None,
+        ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
+    _check(st, "bakron_quantize_antidiag")
+    return V, codes, pre, over.value
+
+
+class Solver:
+    """The whole path on one GPU: row grid, factor preparation, solve.
+
+    Workspaces and outputs are allocated once per shape and reused, so
+    repeated solves of one shape allocate nothing.
+    """
+
+    def __init__(self, m, n, bits=None, qmin=None, qmax=None, opts=None, stream=None):
+        torch = _torch()
+        self.m, self.n = m, n
+        if bits is not None:
+            self.qmax = (1 << (bits - 1)) - 1
+            self.qmin = -(self.qmax + 1)
+        else:
+            self.qmin, self.qmax = qmin, qmax
+        self.opts = opts
+        self.stream = stream
+        dev = "cuda"
+        self.ws_q = torch.empty(workspace_size(m, n, opts), dtype=torch.uint8, device=dev)
+        self.ws_p = torch.empty(prepare_workspace_size(n, m), dtype=torch.uint8, device=dev)
+        self.scale = torch.empty(m, dtype=torch.float32, device=dev)
+        self.UA = torch.empty((n, n), dtype=torch.float32, device=dev)
+        self.UB = torch.empty((m, m), dtype=torch.float32, device=dev)
+        self.V = torch.empty((m, n), dtype=torch.float32, device=dev)
+        self.codes = torch.empty((m, n), dtype=torch.int8, device=dev)
+
+    def rowscale(self, W):
+        return bakron_rowscale(W, self.qmax, out=self.scale, stream=self.stream)
+
+    def prepare(self, A, damp_A, B, damp_B):
+        bakron_prepare(A, damp_A, B, damp_B, workspace=self.ws_p, stream=self.stream,
+                       out=(self.UA, self.UB))
+        return self.UA, self.UB
+
+    def quantize(self, W, UA=None, UB=None, scale=None, want_preround=False):
+        return bakron_quantize(W, self.UA if UA is None else UA, self.UB if UB is None else UB,
+                               self.scale if scale is None else scale, self.qmin, self.qmax,
+                               want_preround=want_preround, opts=self.opts, workspace=self.ws_q,
+                               stream=self.stream, out=(self.V, self.codes))
+
+    def solve(self, W, A, damp_A, B, damp_B):
+        """Row grid + factor preparation + BaKron solve; returns (V, codes)."""
+        self.rowscale(W)
+        self.prepare(A, damp_A, B, damp_B)
+        return self.quantize(W)[:2]

@@ -1,0 +1,113 @@
+// Internal declarations shared by the translation units of libbakron.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bakron.h"
+
+namespace bakron {
+
+constexpr int kTile = 128;          // tile edge T of the solver
+
+// Device-side status block, at the start of every workspace.
+struct DevStatus {
+  int status;          // bakron_status, first error wins (atomicCAS from 0)
+  int pad0;
+  long long info[2];   // prepare: failing pivot (flipped index) of A / B
+  unsigned long long barrier;   // grid-barrier arrival counter (antidiag)
+  unsigned long long overrides; // guided decisions that changed a code
+  int timeout_site;    // where a bounded wait gave up (diagnostic)
+  int pad1[9];
+};
+static_assert(sizeof(DevStatus) <= 256, "status block must fit in 256 bytes");
+
+__device__ __forceinline__ void set_status(DevStatus* st, int code) {
+  atomicCAS(&st->status, 0, code);
+}
+
+// Round an fp32 value to the nearest TF32 value (10 explicit mantissa bits),
+// ties away from zero on the magnitude; Inf/NaN pass through.  The 3xTF32
+// split keeps hi = tf32(x) and lo = x - hi (exact in fp32).
+__device__ __forceinline__ float tf32_round(float x) {
+  unsigned u = __float_as_uint(x);
+  if ((u & 0x7f800000u) != 0x7f800000u) u = (u + 0x1000u) & 0xffffe000u;
+  return __uint_as_float(u);
+}
+
+// One work item of the propagation products: output tile (row tile r,
+// column tile c) accumulates over K tiles [k0, k1).
+struct WorkItem {
+  int r, c, k0, k1;
+};
+
+struct PropArgs {
+  // C[r][c] = sum_k A[r][k] * B[c][k], A and B row-major with leading
+  // dimensions lda/ldb, each given as an (hi, lo) pair whose sum is exact.
+  const float* A_hi; const float* A_lo; int64_t lda;
+  const float* B_hi; const float* B_lo; int64_t ldb;
+  int64_t a_rows, b_rows;                      // rows of A and B (tensor maps)
+  float* out_hi; float* out_lo; int64_t ldo;   // stage 1: Y^T split
+  float* wt; int64_t ldw;                      // stage 2: W~ -= C
+  const WorkItem* items; int n_items;
+  int stage;  // 1 or 2
+  int max_k;  // longest K range of the items, in tiles
+};
+
+struct LeafArgs {
+  float* wt; int64_t ldw;            // padded working matrix W~ (Mp x Np)
+  const float* lat_hi; const float* lat_lo; int64_t lda;  // U_A^T split (Np x Np)
+  const float* lbt_hi; const float* lbt_lo; int64_t ldb;  // U_B^T split (Mp x Mp)
+  const float* scale;                // padded row scales (Mp)
+  float* e_hi; float* e_lo;          // scaled errors, split (Mp x Np, ld = ldw)
+  float* V; int8_t* codes; float* preround;  // outputs, m x n (preround nullable)
+  int64_t m, n;
+  int qmin, qmax;
+  int D, I0;                         // tile anti-diagonal; first row tile
+  DevStatus* st;
+};
+
+// Host launch wrappers (return cudaError_t of the launch).
+cudaError_t launch_rowscale(const float* W, int64_t m, int64_t n, int qmax, float* scale,
+                            cudaStream_t s);
+cudaError_t launch_pad_matrix(const float* src, int64_t rows, int64_t cols, float* dst,
+                              int64_t rows_p, int64_t cols_p, cudaStream_t s);
+cudaError_t launch_transpose_split(const float* U, int64_t k, float* hi, float* lo, int64_t kp,
+                                   cudaStream_t s);
+cudaError_t launch_pad_scale(const float* scale, int64_t m, float* sp, int64_t mp,
+                             cudaStream_t s);
+cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cudaStream_t s);
+cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s);
+cudaError_t launch_prop_simt(const PropArgs& p, cudaStream_t s);
+cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s);
+bool prop_tc_supported();
+
+// antidiag
+struct AntidiagArgs {
+  float* wt;                        // m x n working copy
+  const float* UA; const float* UB; const float* scale;
+  float* ebuf;                      // m: errors of the current diagonal (by row)
+  float* V; int8_t* codes; float* preround;
+  const int8_t* guide; float guide_tol;
+  int64_t m, n; int qmin, qmax;
+  long long budget; int fault_inject;
+  DevStatus* st;
+};
+cudaError_t launch_antidiag(const AntidiagArgs& a, int* unsupported, cudaStream_t s);
+
+// prepare
+struct PrepareFactorArgs {
+  const float* X; int64_t k; float damp;
+  float* U; float* L;            // outputs (L nullable)
+  float* C;                      // Kp x Kp scratch (flipped, then G)
+  float* Ginv;                   // Kp x Kp scratch (G^{-1})
+  float* T;                      // Kp x Kp scratch
+  float* scal;                   // device scalars (lambda)
+  int64_t kp;
+  int which;                     // 0 = A, 1 = B (info slot)
+  DevStatus* st;
+};
+cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s);
+int64_t prepare_pad(int64_t k);
+
+}  // namespace bakron

@@ -1,0 +1,137 @@
+// Small bandwidth-bound kernels: the row grid, padding, and the transposed
+// 3xTF32 split of the update factors.
+#include "internal.cuh"
+
+namespace bakron {
+
+namespace {
+unsigned grid_for(int64_t total, int threads) {
+  int64_t b = (total + threads - 1) / threads;
+  if (b > 152LL * 64) b = 152LL * 64;
+  if (b < 1) b = 1;
+  return (unsigned)b;
+}
+}  // namespace
+
+// ---------------------------------------------------------------- row grid
+// scale[i] = max_j |W[i,j]| / qmax (fp32, one IEEE division), 1 for a zero row.
+// One CTA per row; HBM-bound (reads W once).
+__global__ void __launch_bounds__(256) rowscale_kernel(const float* __restrict__ W, int64_t n,
+                                                       int qmax, float* __restrict__ scale) {
+  const int64_t i = blockIdx.x;
+  const float* row = W + i * n;
+  float amax = 0.f;
+  if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    const int64_t n4 = n >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    for (int64_t j = threadIdx.x; j < n4; j += blockDim.x) {
+      float4 v = __ldg(r4 + j);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    for (int64_t j = (n4 << 2) + threadIdx.x; j < n; j += blockDim.x) amax = fmaxf(amax, fabsf(row[j]));
+  } else {
+    for (int64_t j = threadIdx.x; j < n; j += blockDim.x) amax = fmaxf(amax, fabsf(row[j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
+    scale[i] = (a == 0.f) ? 1.f : a / (float)qmax;
+  }
+}
+
+cudaError_t launch_rowscale(const float* W, int64_t m, int64_t n, int qmax, float* scale,
+                            cudaStream_t s) {
+  if (m == 0) return cudaSuccess;
+  rowscale_kernel<<<(unsigned)m, 256, 0, s>>>(W, n, qmax, scale);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- padding
+// dst (rows_p x cols_p) = src (rows x cols) in the top-left corner, 0 elsewhere.
+__global__ void pad_matrix_kernel(const float* __restrict__ src, int64_t rows, int64_t cols,
+                                  float* __restrict__ dst, int64_t rows_p, int64_t cols_p) {
+  const int64_t total = rows_p * cols_p;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = t / cols_p, j = t - i * cols_p;
+    dst[t] = (i < rows && j < cols) ? src[i * cols + j] : 0.f;
+  }
+}
+
+cudaError_t launch_pad_matrix(const float* src, int64_t rows, int64_t cols, float* dst,
+                              int64_t rows_p, int64_t cols_p, cudaStream_t s) {
+  pad_matrix_kernel<<<grid_for(rows_p * cols_p, 256), 256, 0, s>>>(src, rows, cols, dst, rows_p,
+                                                                   cols_p);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------- transposed split of a factor
+// hi/lo (kp x kp): hi[a][b] + lo[a][b] = U[b][a] for b <= a < k (so the pair
+// holds U^T, lower triangular; the strictly lower triangle of U is ignored);
+// identity on the padding.  hi is U rounded to TF32, lo the exact fp32
+// remainder.  32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_split_kernel(const float* __restrict__ U,
+                                                              int64_t k, float* __restrict__ hi,
+                                                              float* __restrict__ lo, int64_t kp) {
+  __shared__ float t[32][33];
+  const int64_t a0 = (int64_t)blockIdx.y * 32, b0 = (int64_t)blockIdx.x * 32;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int64_t b = b0 + r, a = a0 + threadIdx.x;
+    float v;
+    if (b < k && a < k) v = (a >= b) ? U[b * k + a] : 0.f;
+    else v = (a == b) ? 1.f : 0.f;
+    t[r][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int64_t a = a0 + r, b = b0 + threadIdx.x;
+    const float v = t[threadIdx.x][r];
+    const float h = tf32_round(v);
+    hi[a * kp + b] = h;
+    lo[a * kp + b] = v - h;
+  }
+}
+
+cudaError_t launch_transpose_split(const float* U, int64_t k, float* hi, float* lo, int64_t kp,
+                                   cudaStream_t s) {
+  dim3 grid((unsigned)(kp / 32), (unsigned)(kp / 32));
+  transpose_split_kernel<<<grid, dim3(32, 8), 0, s>>>(U, k, hi, lo, kp);
+  return cudaGetLastError();
+}
+
+__global__ void pad_scale_kernel(const float* __restrict__ scale, int64_t m, float* __restrict__ sp,
+                                 int64_t mp) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < mp;
+       i += (int64_t)gridDim.x * blockDim.x)
+    sp[i] = (i < m) ? scale[i] : 1.f;
+}
+
+cudaError_t launch_pad_scale(const float* scale, int64_t m, float* sp, int64_t mp, cudaStream_t s) {
+  pad_scale_kernel<<<grid_for(mp, 256), 256, 0, s>>>(scale, m, sp, mp);
+  return cudaGetLastError();
+}
+
+// NONFINITE if any scale is NaN/Inf or not positive.
+__global__ void check_positive_finite_kernel(const float* __restrict__ x, int64_t count,
+                                             DevStatus* st) {
+  bool bad = false;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    bad |= !(v > 0.f) || !isfinite(v);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(st, BAKRON_ERR_NONFINITE);
+}
+
+cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cudaStream_t s) {
+  if (count == 0) return cudaSuccess;
+  check_positive_finite_kernel<<<grid_for(count, 256), 256, 0, s>>>(x, count, st);
+  return cudaGetLastError();
+}
+
+}  // namespace bakron
