@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-only entry points (sizes, defaults, status strings, argument
+validation that returns before any CUDA call) work without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bakron.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    if not os.path.exists(kb.LIB_PATH):
+        from kronecker_factored_gptq_gb300 import build
+        build.build()
+    return kb.lib()
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(bakron_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
+                 "bakron_rowscale", "bakron_workspace_size", "bakron_status_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), "libbakron.so does not export %s" % name
+
+
+def test_binding_lists_every_export():
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    assert set(declared_functions()) == set(kb.EXPORTS)
+
+
+def test_status_strings_and_version(L):
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    for code in range(8):
+        assert L.bakron_status_string(code)
+    assert L.bakron_status_string(99) == b"unknown status"
+    assert L.bakron_version() >= 10000
+    o = kb.default_opts()
+    assert o.tile == 128 and o.leaf_width == 1 and o.spin_budget_cycles > 0
+
+
+def test_workspace_sizes(L):
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    s1 = kb.workspace_size(64, 64)
+    s2 = kb.workspace_size(8192, 8192)
+    assert 0 < s1 < s2
+    # W~, E (hi, lo), Y (hi, lo) and four factor halves, fp32, padded to 128
+    assert s2 >= 4 * 8192 * 8192 * 9
+    assert kb.prepare_workspace_size(8192, 8192) >= 3 * 4 * 8192 * 8192
+    b = ctypes.c_size_t(0)
+    assert L.bakron_workspace_size(0, 5, None, ctypes.byref(b)) == 1
+    assert L.bakron_workspace_size(5, 5, None, None) == 1
+    assert L.bakron_prepare_workspace_size(0, 0, ctypes.byref(b)) == 1
+
+
+def test_invalid_arguments_return_before_any_cuda_call(L):
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    vp = ctypes.c_void_p
+    fake = vp(0x1000)
+    o = kb.default_opts()
+    # null pointers
+    assert L.bakron_quantize(None, 4, 4, fake, fake, fake, -8, 7, fake, fake, None, None,
+                             fake, 1 << 20, None) == 1
+    # qmin > qmax
+    assert L.bakron_quantize(fake, 4, 4, fake, fake, fake, 7, -8, fake, fake, None, None,
+                             fake, 1 << 20, None) == 1
+    # workspace too small
+    assert L.bakron_quantize(fake, 4, 4, fake, fake, fake, -8, 7, fake, fake, None, None,
+                             fake, 16, None) == 1
+    # bad options
+    bad = kb.default_opts(tile=64)
+    assert L.bakron_quantize(fake, 4, 4, fake, fake, fake, -8, 7, fake, fake, None,
+                             ctypes.byref(bad), fake, 1 << 20, None) == 1
+    assert L.bakron_quantize_antidiag(fake, 0, 4, fake, fake, fake, -8, 7, fake, fake, None, None,
+                                      0.0, None, ctypes.byref(o), fake, 1 << 20, None) == 1
+    assert L.bakron_prepare(None, 4, 0.0, None, 0, 0.0, fake, None, None, None, None, fake,
+                            1 << 20, None) == 1
+    assert L.bakron_prepare(fake, 4, -1.0, None, 0, 0.0, fake, None, None, None, None, fake,
+                            1 << 20, None) == 1
+    assert L.bakron_rowscale(fake, 4, 4, 0, fake, None) == 1
