@@ -83,6 +83,11 @@ const char* bakron_status_string(int status);
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int bakron_version(void);
 
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all entry points, all devices).  A diagnostic counter: the difference
+ * across a region counts the library's kernels in it. */
+int64_t bakron_kernel_launches(void);
+
 /* Workspace bytes bakron_quantize / bakron_quantize_antidiag need for an
  * m x n problem (written to *bytes, host).  Pure host arithmetic. */
 bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts,

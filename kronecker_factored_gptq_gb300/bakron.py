@@ -21,7 +21,7 @@ STATUS = {0: "BAKRON_OK", 1: "BAKRON_ERR_INVALID_ARG", 2: "BAKRON_ERR_NOT_PD",
 INT32_MIN = -(1 << 31)
 INT32_MAX = (1 << 31) - 1
 
-EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version",
+EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bakron_kernel_launches",
            "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
            "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag"]
 
@@ -63,6 +63,7 @@ def lib():
     L.bakron_status_string.argtypes = [ctypes.c_int]
     L.bakron_status_string.restype = ctypes.c_char_p
     L.bakron_version.restype = ctypes.c_int
+    L.bakron_kernel_launches.restype = ctypes.c_int64
     L.bakron_workspace_size.argtypes = [i64, i64, ctypes.POINTER(Opts), ctypes.POINTER(sz)]
     L.bakron_prepare_workspace_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
     L.bakron_rowscale.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp]
@@ -78,6 +79,11 @@ def lib():
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
+
+
+def kernel_launches():
+    """Kernels the library has launched in this process so far."""
+    return int(lib().bakron_kernel_launches())
 
 
 def default_opts(**kw):

@@ -128,6 +128,7 @@ cudaError_t launch_antidiag(const AntidiagArgs& a, int* unsupported, cudaStream_
   if (per_sm > 2) per_sm = 2;
   AntidiagArgs args = a;
   void* params[] = {&args};
+  count_launch();
   e = cudaLaunchCooperativeKernel((const void*)antidiag_kernel, dim3(nsm * per_sm), dim3(256),
                                   params, 0, s);
   if (e == cudaErrorCooperativeLaunchTooLarge) {

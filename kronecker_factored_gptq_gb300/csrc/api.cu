@@ -288,6 +288,8 @@ const char* bakron_status_string(int st) {
 
 int bakron_version(void) { return 10000; }
 
+int64_t bakron_kernel_launches(void) { return (int64_t)bakron::launches_so_far(); }
+
 bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts, size_t* bytes) {
   if (!bytes || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
   if (opts && !valid_opts(*opts)) return BAKRON_ERR_INVALID_ARG;

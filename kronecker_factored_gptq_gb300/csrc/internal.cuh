@@ -67,6 +67,10 @@ struct LeafArgs {
   DevStatus* st;
 };
 
+// Process-wide count of kernel launches made by the library.
+void count_launch(int k = 1);
+long long launches_so_far();
+
 // Host launch wrappers (return cudaError_t of the launch).
 cudaError_t launch_rowscale(const float* W, int64_t m, int64_t n, int qmax, float* scale,
                             cudaStream_t s);

@@ -147,6 +147,7 @@ cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  count_launch();
   leaf_kernel<<<n_tiles, NTHR, kLeafSmem, s>>>(a);
   return cudaGetLastError();
 }

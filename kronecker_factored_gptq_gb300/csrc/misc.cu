@@ -1,10 +1,13 @@
 // Small bandwidth-bound kernels: the row grid, padding, and the transposed
 // 3xTF32 split of the update factors.
+#include <atomic>
+
 #include "internal.cuh"
 
 namespace bakron {
 
 namespace {
+std::atomic<long long> g_launches{0};
 unsigned grid_for(int64_t total, int threads) {
   int64_t b = (total + threads - 1) / threads;
   if (b > 152LL * 64) b = 152LL * 64;
@@ -12,6 +15,9 @@ unsigned grid_for(int64_t total, int threads) {
   return (unsigned)b;
 }
 }  // namespace
+
+void count_launch(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------- row grid
 // scale[i] = max_j |W[i,j]| / qmax (fp32, one IEEE division), 1 for a zero row.
@@ -47,6 +53,7 @@ __global__ void __launch_bounds__(256) rowscale_kernel(const float* __restrict__
 cudaError_t launch_rowscale(const float* W, int64_t m, int64_t n, int qmax, float* scale,
                             cudaStream_t s) {
   if (m == 0) return cudaSuccess;
+  count_launch();
   rowscale_kernel<<<(unsigned)m, 256, 0, s>>>(W, n, qmax, scale);
   return cudaGetLastError();
 }
@@ -65,6 +72,7 @@ __global__ void pad_matrix_kernel(const float* __restrict__ src, int64_t rows, i
 
 cudaError_t launch_pad_matrix(const float* src, int64_t rows, int64_t cols, float* dst,
                               int64_t rows_p, int64_t cols_p, cudaStream_t s) {
+  count_launch();
   pad_matrix_kernel<<<grid_for(rows_p * cols_p, 256), 256, 0, s>>>(src, rows, cols, dst, rows_p,
                                                                    cols_p);
   return cudaGetLastError();
@@ -100,6 +108,7 @@ __global__ void __launch_bounds__(256) transpose_split_kernel(const float* __res
 cudaError_t launch_transpose_split(const float* U, int64_t k, float* hi, float* lo, int64_t kp,
                                    cudaStream_t s) {
   dim3 grid((unsigned)(kp / 32), (unsigned)(kp / 32));
+  count_launch();
   transpose_split_kernel<<<grid, dim3(32, 8), 0, s>>>(U, k, hi, lo, kp);
   return cudaGetLastError();
 }
@@ -112,6 +121,7 @@ __global__ void pad_scale_kernel(const float* __restrict__ scale, int64_t m, flo
 }
 
 cudaError_t launch_pad_scale(const float* scale, int64_t m, float* sp, int64_t mp, cudaStream_t s) {
+  count_launch();
   pad_scale_kernel<<<grid_for(mp, 256), 256, 0, s>>>(scale, m, sp, mp);
   return cudaGetLastError();
 }
@@ -130,6 +140,7 @@ __global__ void check_positive_finite_kernel(const float* __restrict__ x, int64_
 
 cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cudaStream_t s) {
   if (count == 0) return cudaSuccess;
+  count_launch();
   check_positive_finite_kernel<<<grid_for(count, 256), 256, 0, s>>>(x, count, st);
   return cudaGetLastError();
 }

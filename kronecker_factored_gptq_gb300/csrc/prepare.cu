@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 cudaError_t gemm(const GemmArgs& g, int64_t batch, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || batch <= 0) return cudaSuccess;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)batch);
+  count_launch();
   gemm_simt_kernel<<<grid, 256, 0, s>>>(g);
   return cudaGetLastError();
 }
@@ -259,12 +260,15 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     attr_set = true;
   }
   BK_TRY(cudaMemsetAsync(a.Ginv, 0, sizeof(float) * kp * kp, s));
+  count_launch();
   diag_mean_kernel<<<1, 256, 0, s>>>(a.X, k, a.damp, a.scal);
   BK_TRY(cudaGetLastError());
+  count_launch();
   flip_damp_kernel<<<grid_for(kp * kp), 256, 0, s>>>(a.X, k, a.scal, a.C, kp);
   BK_TRY(cudaGetLastError());
   for (int64_t kb = 0; kb < nblk; ++kb) {
-    potrf_block_kernel<<<1, 512, kPotrfSmem, s>>>(a.C, a.Ginv, kp, kb, k, a.st, a.which);
+    count_launch();
+  potrf_block_kernel<<<1, 512, kPotrfSmem, s>>>(a.C, a.Ginv, kp, kb, k, a.st, a.which);
     BK_TRY(cudaGetLastError());
     const int64_t rest = kp - (kb + 1) * NB;
     if (rest <= 0) break;
@@ -276,7 +280,8 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     g.C = a.T; g.ldc = NB;
     g.M = rest; g.N = NB; g.K = NB; g.alpha = 1.f; g.beta = 0.f;
     BK_TRY(gemm(g, 1, s));
-    copy_block_kernel<<<grid_for(rest * NB), 256, 0, s>>>(a.T, NB, panel, kp, rest, NB);
+    count_launch();
+  copy_block_kernel<<<grid_for(rest * NB), 256, 0, s>>>(a.T, NB, panel, kp, rest, NB);
     BK_TRY(cudaGetLastError());
     // trailing: C22 -= T T^T (lower tiles)
     GemmArgs h{};
@@ -320,6 +325,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
       BK_TRY(gemm(hl, 1, s));
     }
   }
+  count_launch();
   finalize_kernel<<<grid_for(k * k), 256, 0, s>>>(a.C, a.Ginv, kp, k, a.U, a.L);
   return cudaGetLastError();
 }

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(256) prop_simt_kernel(PropArgs p) {
 
 cudaError_t launch_prop_simt(const PropArgs& p, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
+  count_launch();
   prop_simt_kernel<<<p.n_items, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
