@@ -163,6 +163,23 @@ bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n,
                                        const bakron_opts* opts, void* ws, size_t ws_bytes,
                                        void* stream);
 
+/* bakron_quantize for callers that cannot allocate device memory, such as
+ * code embedded in a host application that owns all device memory through
+ * its own pool and forbids cudaMalloc/cudaFree (they synchronise the device
+ * and fragment the pool), or code that cannot keep a workspace between
+ * calls.  The paper has no counterpart; this is a deployment convenience.
+ * Same arguments and result as bakron_quantize with default options and no
+ * preround output, but no workspace: the library uses a fixed 12 MiB scratch
+ * array of its own on each GPU (held until the process exits), so m and n
+ * must be at most 512 (larger sizes return BAKRON_ERR_INVALID_ARG).  The
+ * first call on a device resolves that array's address (make it before any
+ * stream capture).  All calls on a device share the array: calls that
+ * overlap on the GPU race; serialise them. */
+bakron_status bakron_quantize_noalloc(const float* W, int64_t m, int64_t n,
+                                      const float* UA, const float* UB,
+                                      const float* scale, int qmin, int qmax,
+                                      float* V, int8_t* codes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

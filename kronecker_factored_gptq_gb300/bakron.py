@@ -23,7 +23,8 @@ INT32_MAX = (1 << 31) - 1
 
 EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bakron_kernel_launches",
            "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
-           "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag"]
+           "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
+           "bakron_quantize_noalloc"]
 
 
 class PhaseTimes(ctypes.Structure):
@@ -74,8 +75,11 @@ def lib():
     L.bakron_quantize_antidiag.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                            vp, vp, vp, vp, ctypes.c_float, ctypes.POINTER(i64),
                                            ctypes.POINTER(Opts), vp, sz, vp]
+    L.bakron_quantize_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                          vp, vp, vp]
     for f in ("bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
-              "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag"):
+              "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
+              "bakron_quantize_noalloc"):
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
@@ -237,6 +241,31 @@ def bakron_quantize_antidiag(W, UA, UB, scale, qmin, qmax, guide_codes=None, gui
         ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
     _check(st, "bakron_quantize_antidiag")
     return V, codes, pre, over.value
+
+
+NOALLOC_MAX_DIM = 512
+
+
+def bakron_quantize_noalloc(W, UA, UB, scale, qmin, qmax, out=None, stream=None):
+    """bakron_quantize without a workspace (the library's fixed scratch array;
+    m, n <= 512).  For callers that cannot allocate device memory, pass
+    pre-allocated ``out=(V, codes)``; this wrapper then allocates nothing
+    either.  Returns (V, codes)."""
+    torch = _torch()
+    m, n = W.shape
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        codes = torch.empty((m, n), dtype=torch.int8, device=W.device)
+    else:
+        V, codes = out
+    st = lib().bakron_quantize_noalloc(
+        _dev(W, torch.float32, (m, n), "W"), m, n,
+        _dev(UA, torch.float32, (n, n), "UA"), _dev(UB, torch.float32, (m, m), "UB"),
+        _dev(scale, torch.float32, (m,), "scale"), int(qmin), int(qmax),
+        _dev(V, torch.float32, (m, n), "V"), _dev(codes, torch.int8, (m, n), "codes"),
+        _stream(stream))
+    _check(st, "bakron_quantize_noalloc")
+    return V, codes
 
 
 class Solver:

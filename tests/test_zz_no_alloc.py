@@ -1,0 +1,68 @@
+"""bakron_quantize_noalloc: the solve for callers that cannot allocate device
+memory (for example a plugin inside a host application that owns all device
+memory through its own pool and forbids cudaMalloc/cudaFree).  It must give the
+same result as bakron_quantize, call after call, although every call reuses
+the library's one fixed scratch array and finds the previous call's data in it.
+
+This file is collected last on purpose, so a run that stops at the first
+failure has already run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle as O
+from kronecker_factored_gptq_gb300 import workloads as WL
+
+from _gpu_helpers import TOL, MAX_FRAC, shared_factors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_via_c_abi(kb, dW, dUA, dUB, ds, qmin, qmax, V, C):
+    import torch
+    m, n = dW.shape
+    st = kb.lib().bakron_quantize_noalloc(
+        ctypes.c_void_p(dW.data_ptr()), m, n, ctypes.c_void_p(dUA.data_ptr()),
+        ctypes.c_void_p(dUB.data_ptr()), ctypes.c_void_p(ds.data_ptr()), qmin, qmax,
+        ctypes.c_void_p(V.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+def test_noalloc_matches_quantize_on_consecutive_calls():
+    import torch
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    # a larger problem first, then a smaller one: the second call finds the
+    # first call's data in the shared scratch array
+    for m, n, bits, seed in ((512, 384, 4, 21), (200, 130, 3, 22)):
+        w = WL.random_problem(m, n, seed=seed, bits=bits)
+        UA32, UB32 = shared_factors(w.A, w.damp_A, w.B, w.damp_B)
+        s = O.row_scale(w.W, w.qmax)
+        dW, dUA, dUB, ds = to_dev(w.W, UA32, UB32, s)
+        V_ref, C_ref, pre_ref = kb.bakron_quantize(dW, dUA, dUB, ds, w.qmin, w.qmax,
+                                                   want_preround=True)
+        V = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+        C = torch.full((m, n), 99, dtype=torch.int8, device="cuda")
+        assert _noalloc_via_c_abi(kb, dW, dUA, dUB, ds, w.qmin, w.qmax, V, C) == kb.OK
+        c_ref = C_ref.cpu().numpy().astype(np.float64)
+        c_new = C.cpu().numpy().astype(np.float64)
+        # the comparison rule of the other parity tests (near ties only, <= 0.1%)
+        r = O.compare_codes(c_new, c_ref, pre_ref.cpu().numpy(), s, w.qmin, w.qmax, TOL, MAX_FRAC)
+        assert r["ok"], r
+        np.testing.assert_array_equal(V.cpu().numpy(), (s[:, None] * c_new.astype(np.float32)))
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    import torch
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    m, n = 513, 64
+    dW = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    dUA = torch.eye(n, dtype=torch.float32, device="cuda")
+    dUB = torch.eye(m, dtype=torch.float32, device="cuda")
+    ds = torch.ones(m, dtype=torch.float32, device="cuda")
+    V = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    C = torch.empty((m, n), dtype=torch.int8, device="cuda")
+    assert _noalloc_via_c_abi(kb, dW, dUA, dUB, ds, -8, 7, V, C) == 1
