@@ -64,8 +64,8 @@ typedef struct {
   int tile;                 /* tile edge T; only 128 is supported (0 = 128) */
   int leaf_width;           /* tile anti-diagonals per leaf; only 1 (0 = 1) */
   int use_3xtf32;           /* propagation products: 1 = tcgen05 tensor cores
-                               with a 3xTF32 split, 0 = fp32 FMA; the default
-                               is 1 where the tensor-core kernel is built */
+                               with a 3xTF32 split (default; needs sm_103,
+                               else BAKRON_ERR_UNSUPPORTED), 0 = fp32 FMA */
   long long spin_budget_cycles; /* bound of every device spin-wait, in SM
                                clock cycles (0 = 4e9) */
   int fault_inject;         /* test hook, bakron_quantize_antidiag only: one

@@ -266,7 +266,7 @@ void bakron_default_opts(bakron_opts* o) {
   std::memset(o, 0, sizeof(*o));
   o->tile = T;
   o->leaf_width = 1;
-  o->use_3xtf32 = prop_tc_supported() ? 1 : 0;
+  o->use_3xtf32 = 1;
   o->spin_budget_cycles = 4000000000LL;
   o->fault_inject = 0;
   o->times = nullptr;
@@ -417,11 +417,13 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   p1.B_hi = ehi; p1.B_lo = elo; p1.ldb = L.Np; p1.b_rows = L.Mp;
   p1.out_hi = yhi; p1.out_lo = ylo; p1.ldo = L.Mp;
   p1.stage = 1;
+  p1.st = st;
   PropArgs p2{};
   p2.A_hi = lbthi; p2.A_lo = lbtlo; p2.lda = L.Mp; p2.a_rows = L.Mp;
   p2.B_hi = yhi; p2.B_lo = ylo; p2.ldb = L.Mp; p2.b_rows = L.Np;
   p2.wt = wt; p2.ldw = L.Np;
   p2.stage = 2;
+  p2.st = st;
   for (const Op& op : sch.ops) {
     if (op.kind == 0) {
       la.D = op.D;

@@ -52,6 +52,7 @@ struct PropArgs {
   const WorkItem* items; int n_items;
   int stage;  // 1 or 2
   int max_k;  // longest K range of the items, in tiles
+  DevStatus* st;
 };
 
 struct LeafArgs {

@@ -1,13 +1,344 @@
 // Propagation products on the tcgen05 tensor cores with a 3xTF32 split.
+//
+// The two propagation stages of BaKron (summary page "FastKron: Efficient
+// Quantization with Kronecker-Factored Hessians", section 3: the error of the
+// first half of the anti-diagonals is pushed into the second half with dense
+// products) are both "C[r][c] = sum_k A[r][k] B[c][k]" over lists of
+// 128 x 128 output tiles with per-tile K ranges.  Each operand is stored
+// pre-split, x = hi + lo with hi = tf32(x); the tensor core accumulates
+//     C = A_hi B_hi + A_hi B_lo + A_lo B_hi
+// in fp32 (TMEM), dropping only A_lo B_lo (relative size 2^-22), which keeps
+// the products at fp32 accuracy.
+//
+// One CTA (4 warps) per work item:
+//   warp 0, one thread: TMA producer, 3-stage ring of 32-wide K slices, each
+//     stage holding A_hi, A_lo, B_hi, B_lo as 128 x 32 fp32 tiles with the
+//     128-byte swizzle (64 KiB per stage);
+//   warp 1, one thread: issues tcgen05.mma (M = N = 128, K = 8 per
+//     instruction, 3 per K step) and commits each stage back to the producer;
+//   warp 2: allocates / frees the 128 TMEM columns of the accumulator;
+//   all 4 warps: epilogue, TMEM -> registers (warp w owns lanes 32w..32w+31,
+//     i.e. output rows) -> global: stage 1 writes C split into (hi, lo),
+//     stage 2 subtracts C from W~.
+// Every mbarrier wait is bounded (clock64 budget); on expiry the CTA records
+// BAKRON_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs (with a
+// bound again), frees TMEM and returns.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace bakron {
 
-bool prop_tc_supported() { return false; }
+namespace {
+constexpr int BM = 128, BN = 128, BKF = 32;      // tile rows, cols, K slice (floats)
+constexpr int STAGES = 3;
+constexpr uint32_t TILE_BYTES = BM * BKF * 4;    // 16 KiB
+constexpr uint32_t STAGE_BYTES = 4 * TILE_BYTES; // A_hi, A_lo, B_hi, B_lo
+constexpr size_t kSmem = (size_t)STAGES * STAGE_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 128;
+constexpr long long kBudget = 400000000LL;       // ~0.2 s of SM clock per wait
+
+// instruction descriptor, kind::tf32: D fp32, A/B tf32, both K-major, M=N=128
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false on timeout or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kBudget) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), start address in 16-byte units.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+  d |= (uint64_t)1 << 46;             // descriptor version
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+}  // namespace
+
+__global__ void __launch_bounds__(128, 1)
+    prop_tc_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
+                   const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
+                   PropArgs p, DevStatus* st) {
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  __shared__ __align__(8) unsigned long long bar_full[STAGES], bar_empty[STAGES], bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[blockIdx.x];
+  const int nk = (it.k1 - it.k0) * (kTile / BKF);
+  // 1024-byte aligned stage ring
+  const uint32_t base_raw = smem_u32(dsm);
+  const uint32_t sbase = (base_raw + 1023u) & ~1023u;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_done), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abortp = &abort_flag;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    const int kx0 = it.k0 * kTile;
+    const int ya = it.r * BM, yb = it.c * BN;
+    int issued = 0;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % STAGES;
+      const uint32_t u = (uint32_t)(i / STAGES);
+      if (i >= STAGES && !mbar_wait(smem_u32(&bar_empty[s]), (u & 1u) ^ 1u, abortp)) {
+        set_status(st, BAKRON_ERR_TIMEOUT);
+        *abortp = 1;
+        break;
+      }
+      const uint32_t fb = smem_u32(&bar_full[s]);
+      mbar_expect_tx(fb, STAGE_BYTES);
+      const uint32_t sd = sbase + (uint32_t)s * STAGE_BYTES;
+      const int x = kx0 + i * BKF;
+      tma_load_2d(sd, &tm_ahi, fb, x, ya);
+      tma_load_2d(sd + TILE_BYTES, &tm_alo, fb, x, ya);
+      tma_load_2d(sd + 2 * TILE_BYTES, &tm_bhi, fb, x, yb);
+      tma_load_2d(sd + 3 * TILE_BYTES, &tm_blo, fb, x, yb);
+      ++issued;
+    }
+    // drain: every issued copy must have landed before the CTA may exit
+    for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i) {
+      const int s = i % STAGES;
+      const uint32_t u = (uint32_t)(i / STAGES);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_full[s]), u & 1u)) {
+        if (clock64() - t0 > kBudget) { set_status(st, BAKRON_ERR_TIMEOUT); break; }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % STAGES;
+      const uint32_t u = (uint32_t)(i / STAGES);
+      if (!mbar_wait(smem_u32(&bar_full[s]), u & 1u, abortp)) {
+        set_status(st, BAKRON_ERR_TIMEOUT);
+        *abortp = 1;
+        break;
+      }
+      fence_after_sync();
+      const uint32_t sd = sbase + (uint32_t)s * STAGE_BYTES;
+      const uint64_t ahi = desc_sw128(sd), alo = desc_sw128(sd + TILE_BYTES);
+      const uint64_t bhi = desc_sw128(sd + 2 * TILE_BYTES), blo = desc_sw128(sd + 3 * TILE_BYTES);
+#pragma unroll
+      for (int j = 0; j < BKF / 8; ++j) {
+        const uint64_t o = (uint64_t)(j * 32 >> 4);  // 8 tf32 = 32 bytes along K
+        mma_tf32(tmem, ahi + o, bhi + o, (i > 0 || j > 0) ? 1u : 0u);
+        mma_tf32(tmem, ahi + o, blo + o, 1u);
+        mma_tf32(tmem, alo + o, bhi + o, 1u);
+      }
+      mma_commit(smem_u32(&bar_empty[s]));
+    }
+    mma_commit(smem_u32(&bar_done));
+  }
+  __syncwarp();
+
+  // ---------------- epilogue (all 4 warps)
+  bool ok = true;
+  {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(smem_u32(&bar_done), 0u)) {
+      if (clock64() - t0 > kBudget) { ok = false; break; }
+    }
+  }
+  if (!ok) set_status(st, BAKRON_ERR_TIMEOUT);
+  fence_after_sync();
+  ok = ok && (*abortp == 0);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) {
+    const int row = warp * 32 + lane;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ch * 32), v);
+      if (p.stage == 1) {
+        float* oh = p.out_hi + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN + ch * 32;
+        float* ol = p.out_lo + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN + ch * 32;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 h, l;
+          h.x = tf32_round(v[4 * q + 0]); l.x = v[4 * q + 0] - h.x;
+          h.y = tf32_round(v[4 * q + 1]); l.y = v[4 * q + 1] - h.y;
+          h.z = tf32_round(v[4 * q + 2]); l.z = v[4 * q + 2] - h.z;
+          h.w = tf32_round(v[4 * q + 3]); l.w = v[4 * q + 3] - h.w;
+          reinterpret_cast<float4*>(oh)[q] = h;
+          reinterpret_cast<float4*>(ol)[q] = l;
+        }
+      } else {
+        float4* w = reinterpret_cast<float4*>(p.wt + ((int64_t)it.r * BM + row) * p.ldw +
+                                              (int64_t)it.c * BN + ch * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 x = w[q];
+          x.x -= v[4 * q + 0]; x.y -= v[4 * q + 1]; x.z -= v[4 * q + 2]; x.w -= v[4 * q + 3];
+          w[q] = x;
+        }
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    fence_after_sync();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// rows x cols fp32 row-major matrix with leading dimension ld (floats);
+// box = 32 columns (128 bytes) x 128 rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+  const cuuint32_t box[2] = {(cuuint32_t)BKF, (cuuint32_t)BM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool prop_tc_supported() {
+  static int cached = -1;
+  if (cached >= 0) return cached == 1;
+  int dev = 0, major = 0, minor = 0;
+  bool ok = cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+            major == 10 && minor == 3 && encode_fn() != nullptr;
+  if (!ok) (void)cudaGetLastError();
+  cached = ok ? 1 : 0;
+  return ok;
+}
 
 cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s) {
-  (void)p; (void)s;
-  return cudaErrorNotSupported;
+  if (p.n_items == 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(prop_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap ahi, alo, bhi, blo;
+  if (!make_map(&ahi, p.A_hi, p.a_rows, p.lda) || !make_map(&alo, p.A_lo, p.a_rows, p.lda) ||
+      !make_map(&bhi, p.B_hi, p.b_rows, p.ldb) || !make_map(&blo, p.B_lo, p.b_rows, p.ldb))
+    return cudaErrorInvalidValue;
+  count_launch();
+  prop_tc_kernel<<<p.n_items, 128, kSmem, s>>>(ahi, alo, bhi, blo, p, p.st);
+  return cudaGetLastError();
 }
 
 }  // namespace bakron
