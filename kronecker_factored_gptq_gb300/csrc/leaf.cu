@@ -14,10 +14,19 @@
 // in-tile entry to the top-left, because r(a', b) is complete (all b' <= b
 // rounded) one step before row a needs it.
 //
-// Threads: 4 per tile row (512).  Thread (a, q) keeps Ub(4t+q, a), t < 32, in
-// registers; r is kept transposed in shared memory (rT[b][a], pitch = 4 mod 32
-// so the column reads of one step are conflict-free), Ua row-major (pitch =
-// 3 mod 32).  One __syncthreads per anti-diagonal step.
+// Work split, TPR = 4 threads per tile row (512 threads):
+//  * column sum: thread (a, q) keeps Ub(TPR t + q, a) in registers and reads
+//    the completed r(a', b) from shared memory (rT[b][a'], pitch TPR mod 32);
+//  * row accumulator: the not-yet-complete r(a, b'') live in REGISTERS.
+//    Thread q of row a owns the columns b'' whose anti-diagonal a + b'' is
+//    q mod TPR; its register FR[j] holds the column with anti-diagonal
+//    TPR (kb + j) + q at step block kb.  The step loop is unrolled by TPR,
+//    so the entry completing at sub-step s is always FR[0] of thread s, and
+//    the array shifts by one register every TPR steps: every register index
+//    is static.  The one completed value per row and step is published to
+//    rT for the rows below;
+//  * one lane per row rounds the entry; the error is broadcast by shuffle.
+// Loops stop at the warp's largest trip count.  One __syncthreads per step.
 #include "internal.cuh"
 
 namespace bakron {
@@ -26,24 +35,30 @@ namespace {
 constexpr int T = kTile;
 constexpr int TPR = 4;
 constexpr int NTHR = T * TPR;
-constexpr int PR = T + 4;   // rT pitch
-constexpr int PU = T + 3;   // Ua pitch
-constexpr int PE = T;       // Es pitch
+constexpr int CH = T / TPR;         // column-sum registers per thread
+constexpr int NFR = T / TPR + 1;    // row-accumulator registers per thread
+constexpr int PR = T + TPR;         // rT pitch (TPR mod 32): conflict-free column reads
+constexpr int PU = T + TPR - 1;     // Ua pitch (TPR - 1 mod 32): conflict-free row reads
+constexpr int PE = T;               // Es pitch
+constexpr int NSTEP = 2 * T - 1;
 constexpr size_t kLeafSmem =
     sizeof(float) * ((size_t)T * PR + (size_t)T * PU + (size_t)T * PE + T) + (size_t)T * T;
+constexpr unsigned FULL = 0xffffffffu;
 }  // namespace
 
 __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   extern __shared__ __align__(16) float smem[];
-  float* rT = smem;                       // [T][PR]
+  float* rT = smem;                       // [T][PR] completed row accumulators, transposed
   float* Ua = rT + T * PR;                // [T][PU]
   float* Es = Ua + T * PU;                // [T][PE]: x0, then the scaled error
   float* lA = Es + T * PE;                // [T]: 1 / Ua(b, b)
   signed char* cs = reinterpret_cast<signed char*>(lA + T);  // [T][T] codes
 
   const int tid = threadIdx.x;
-  const int row = (tid >> 5) * 8 + ((tid & 31) >> 2);
-  const int q = tid & 3;
+  const int lane = tid & 31;
+  const int row = tid / TPR;
+  const int q = tid % TPR;
+  const int gbase = lane & ~(TPR - 1);
   const int I = a.I0 + blockIdx.x;
   const int J = a.D - I;
   const int64_t i0 = (int64_t)I * T, j0 = (int64_t)J * T;
@@ -60,12 +75,16 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   }
   for (int idx = tid; idx < T * PR; idx += NTHR) rT[idx] = 0.f;
 
-  float ub[32];
+  float ub[CH];
   {
     const int64_t g = (i0 + row) * a.ldb + i0;
 #pragma unroll
-    for (int t = 0; t < 32; ++t) ub[t] = a.lbt_hi[g + 4 * t + q] + a.lbt_lo[g + 4 * t + q];
+    for (int t = 0; t < CH; ++t) {
+      const int ap = TPR * t + q;
+      ub[t] = (ap < row) ? a.lbt_hi[g + ap] + a.lbt_lo[g + ap] : 0.f;
+    }
   }
+  const int cnt = row > q ? (row - q + TPR - 1) / TPR : 0;  // # of a' = TPR t + q < row
   const int64_t gd = (i0 + row) * a.ldb + i0 + row;
   const float ubaa = a.lbt_hi[gd] + a.lbt_lo[gd];
   const float lB = 1.f / ubaa;
@@ -78,45 +97,84 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
 
   const float fqmin = (float)a.qmin, fqmax = (float)a.qmax;
   bool nonfinite = false, out_of_range = false;
-  const int tmax = (row - q + 3) >> 2;  // # of t with 4t + q < row
-
-  for (int d = 0; d < 2 * T - 1; ++d) {
-    const int b = d - row;
-    const bool act = (b >= 0) && (b < T);
-    float p = 0.f;
-    if (act) {
-      const float* rc = rT + b * PR + q;
+  float FR[NFR];
 #pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (t < tmax) p = fmaf(ub[t], rc[4 * t], p);
-    }
-    p += __shfl_xor_sync(0xffffffffu, p, 1);
-    p += __shfl_xor_sync(0xffffffffu, p, 2);
-    float e = 0.f, c = 0.f;
-    if (act) {
-      const float rpart = rT[b * PR + row];
-      const float x = Es[row * PE + b] - p - ubaa * rpart;
-      nonfinite |= !isfinite(x);
-      c = rintf(x / s);
-      c = fminf(fmaxf(c, fqmin), fqmax);
-      out_of_range |= (c < -128.f) || (c > 127.f);
-      const float qv = s * c;
-      e = (x - qv) * lB * lA[b];
-      if (q == 1 && a.preround && row_real && j0 + b < a.n) a.preround[gi * a.n + j0 + b] = x;
-    }
-    __syncwarp();
-    if (act) {
-      if (q == 0) {
+  for (int j = 0; j < NFR; ++j) FR[j] = 0.f;
+
+  for (int kb = 0; kb * TPR < NSTEP; ++kb) {
+#pragma unroll
+    for (int sg = 0; sg < TPR; ++sg) {
+      const int d = kb * TPR + sg;
+      if (d >= NSTEP) break;
+      const int b = d - row;
+      const bool act = (b >= 0) && (b < T);
+      // ---- column sum over the rows above (completed accumulators)
+      float p = 0.f;
+      {
+        // loads in groups of 8 with no branch between them (the registers
+        // ub[t >= cnt] are 0 and rT is zero-initialised, so a group may run
+        // past cnt); two accumulators shorten the dependent chain
+        const int cm = __reduce_max_sync(FULL, act ? cnt : 0);
+        const float* rc = rT + b * PR + q;
+        float p1 = 0.f;
+#pragma unroll
+        for (int tb = 0; tb < CH; tb += 8) {
+          if (tb >= cm) break;
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = act ? rc[TPR * (tb + u)] : 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) {
+            p = fmaf(ub[tb + u], v[u], p);
+            p1 = fmaf(ub[tb + u + 1], v[u + 1], p1);
+          }
+        }
+        p += p1;
+      }
+#pragma unroll
+      for (int o = 1; o < TPR; o <<= 1) p += __shfl_xor_sync(FULL, p, o);
+      // ---- round (one lane per row)
+      float e = 0.f;
+      if (act && q == sg) {
+        const float x = Es[row * PE + b] - p - ubaa * FR[0];
+        nonfinite |= !isfinite(x);
+        float c = rintf(x / s);
+        c = fminf(fmaxf(c, fqmin), fqmax);
+        out_of_range |= (c < -128.f) || (c > 127.f);
+        e = (x - s * c) * lB * lA[b];
         Es[row * PE + b] = e;
         cs[row * T + b] = (signed char)(int)fminf(fmaxf(c, -128.f), 127.f);
+        if (a.preround && row_real && j0 + b < a.n) a.preround[gi * a.n + j0 + b] = x;
       }
-      const float* ur = Ua + b * PU;
-      for (int b2 = b + q; b2 < T; b2 += 4) {
-        float* rp = rT + b2 * PR + row;
-        *rp = fmaf(e, ur[b2], *rp);
+      e = __shfl_sync(FULL, e, gbase | sg);
+      // ---- push the error into the row's own accumulators (registers)
+      {
+        const int X = T + row - q - TPR * kb;
+        int jend = X > 0 ? (X + TPR - 1) / TPR : 0;
+        jend = jend < NFR ? jend : NFR;
+        const int jm = __reduce_max_sync(FULL, act ? jend : 0);
+        const float* ur = Ua + b * PU + TPR * kb + q - row;  // ur[TPR j] = Ua(b, b'')
+#pragma unroll
+        for (int jb = 0; jb < NFR; jb += 8) {
+          if (jb >= jm) break;
+          float w[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = jb + u;
+            w[u] = (j < NFR && act && j < jend && (j > 0 || q >= sg)) ? ur[TPR * j] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (jb + u < NFR) FR[jb + u] = fmaf(e, w[u], FR[jb + u]);
+        }
       }
+      // ---- publish the completed accumulator r(row, b)
+      if (act && q == sg) rT[b * PR + row] = FR[0];
+      __syncthreads();
     }
-    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NFR - 1; ++j) FR[j] = FR[j + 1];
+    FR[NFR - 1] = 0.f;
   }
 
   if (nonfinite) set_status(a.st, BAKRON_ERR_NONFINITE);
