@@ -174,23 +174,52 @@ ALayout antidiag_layout(int64_t m, int64_t n) {
 }
 
 struct PLayout {
-  int64_t kp;
-  size_t status, scal, C, Ginv, T, total;
+  int64_t kp[2];
+  size_t status, scal, C[2], Ginv[2], T[2], total;
 };
 
+// Each factor has its own scratch: A and B are prepared concurrently.
 PLayout prepare_layout(int64_t n, int64_t m) {
   PLayout L{};
-  L.kp = std::max(prepare_pad(n), prepare_pad(m));
+  L.kp[0] = prepare_pad(n);
+  L.kp[1] = prepare_pad(m);
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
-  const size_t kk = sizeof(float) * (size_t)L.kp * (size_t)L.kp;
   L.status = take(256);
   L.scal = take(256);
-  L.C = take(kk);
-  L.Ginv = take(kk);
-  L.T = take(kk);
+  for (int w = 0; w < 2; ++w) {
+    const size_t kk = sizeof(float) * (size_t)L.kp[w] * (size_t)L.kp[w];
+    L.C[w] = take(kk);
+    L.Ginv[w] = take(kk);
+    L.T[w] = take(kk);
+  }
   L.total = off;
   return L;
+}
+
+// A second stream (and fork/join events) per device, created once, on which
+// the B factor is prepared while A runs on the caller's stream.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+cudaError_t aux_stream(AuxStream** out) {
+  static std::mutex mu;
+  static AuxStream per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  AuxStream& a = per_dev[dev];
+  if (!a.s) {
+    if ((e = cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &a;
+  return cudaSuccess;
 }
 
 #define TRY_CUDA(x)                                        \
@@ -330,6 +359,12 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   DevStatus* st = (DevStatus*)(base + L.status);
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
   TRY_CUDA(cudaMemsetAsync(st->info, 0x7f, sizeof(st->info), s));
+  AuxStream* aux = nullptr;
+  if (B) {
+    TRY_CUDA(aux_stream(&aux));
+    TRY_CUDA(cudaEventRecord(aux->fork, s));
+    TRY_CUDA(cudaStreamWaitEvent(aux->s, aux->fork, 0));
+  }
   for (int which = 0; which < 2; ++which) {
     const float* X = which == 0 ? A : B;
     const int64_t k = which == 0 ? n : m;
@@ -338,14 +373,18 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
     pa.X = X; pa.k = k; pa.damp = which == 0 ? damp_A : damp_B;
     pa.U = which == 0 ? UA : UB;
     pa.L = which == 0 ? LA : LB;
-    pa.C = (float*)(base + L.C);
-    pa.Ginv = (float*)(base + L.Ginv);
-    pa.T = (float*)(base + L.T);
-    pa.scal = (float*)(base + L.scal);
-    pa.kp = prepare_pad(k);
+    pa.C = (float*)(base + L.C[which]);
+    pa.Ginv = (float*)(base + L.Ginv[which]);
+    pa.T = (float*)(base + L.T[which]);
+    pa.scal = (float*)(base + L.scal) + which;
+    pa.kp = L.kp[which];
     pa.which = which;
     pa.st = st;
-    TRY_CUDA(run_prepare_factor(pa, s));
+    TRY_CUDA(run_prepare_factor(pa, which == 0 ? s : aux->s));
+  }
+  if (aux) {
+    TRY_CUDA(cudaEventRecord(aux->join, aux->s));
+    TRY_CUDA(cudaStreamWaitEvent(s, aux->join, 0));
   }
   DevStatus h{};
   bakron_status r = finish(s, st, &h);

@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/bakron.h"
+#include "bakron.h"
 
 namespace bakron {
 

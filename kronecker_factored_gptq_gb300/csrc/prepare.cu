@@ -32,6 +32,8 @@ struct GemmArgs {
   float alpha, beta;
   int transB;        // 0: B is K x N row-major; 1: B is N x K row-major
   int lower_only;    // skip output tiles strictly above the diagonal
+  int klo_from_col;  // B lower triangular (B[k][n] = 0 for k < n): start K at the tile's first column
+  int khi_to_row;    // A lower triangular (A[m][k] = 0 for k > m): stop K after the tile's last row
   int64_t mclip_base, mclip_step, mclip_total;  // per-batch row limit:
   // rows available = min(M, mclip_total - (mclip_base + batch * mclip_step))
 };
@@ -60,7 +62,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
   const int lrow = tid >> 1, lk = (tid & 1) * 8;
-  for (int64_t k = 0; k < g.K; k += BK) {
+  int64_t kbeg = 0, kend = g.K;
+  if (g.klo_from_col) kbeg = c0 < kend ? c0 : kend;
+  if (g.khi_to_row && r0 + BM < kend) kend = r0 + BM;
+  for (int64_t k = kbeg; k < kend; k += BK) {
     {
       const float* pa = A + (r0 + lrow) * g.lda + k + lk;
 #pragma unroll
@@ -145,6 +150,8 @@ __global__ void flip_damp_kernel(const float* __restrict__ X, int64_t k, const f
 
 // Factor the diagonal block C[kb, kb] (128 x 128) in shared memory; write
 // G_kk (lower, zero upper) back and inv(G_kk) into Ginv's diagonal block.
+// Both loops are right-looking with one barrier per column / row; threads
+// form a 16 x 32 grid over (row, column) of the trailing lower triangle.
 constexpr size_t kPotrfSmem = sizeof(float) * 2 * NB * (NB + 1);
 
 __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Ginv, int64_t kp, int64_t kb,
@@ -152,60 +159,57 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Ginv,
   extern __shared__ __align__(16) float psm[];
   float (*G)[NB + 1] = reinterpret_cast<float (*)[NB + 1]>(psm);
   float (*X)[NB + 1] = reinterpret_cast<float (*)[NB + 1]>(psm + NB * (NB + 1));
-  __shared__ float piv;
   const int tid = threadIdx.x;
+  const int tx = tid & 31, ty = tid >> 5;
   const int64_t o = kb * NB;
   for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
     G[r][c] = (c <= r) ? C[(o + r) * kp + o + c] : 0.f;
+    X[r][c] = 0.f;
   }
   __syncthreads();
+  // Cholesky: at column j every thread reads the pivot, updates its share of
+  // the trailing lower triangle with the scaled column, then column j is
+  // scaled in place (it is not read again).
   for (int j = 0; j < NB; ++j) {
-    if (tid == 0) {
-      float d = G[j][j];
-      if (!(d > 0.f) || !isfinite(d)) {
-        const int64_t f = o + j;  // flipped index
-        if (f < k_real) {
-          // the smallest flipped index fails first; keep the first failure
-          atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)f);
-          set_status(st, BAKRON_ERR_NOT_PD);
-        }
-        d = 1.f;
+    float d = G[j][j];
+    const bool bad = !(d > 0.f) || !isfinite(d);
+    if (bad) {
+      if (tid == 0 && o + j < k_real) {
+        atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + j));
+        set_status(st, BAKRON_ERR_NOT_PD);
       }
-      piv = sqrtf(d);
-      G[j][j] = piv;
+      d = 1.f;
+    }
+    const float piv = sqrtf(d), inv = 1.f / piv;
+    for (int r = j + 1 + ty; r < NB; r += 16) {
+      const float lr = G[r][j] * inv;
+      for (int c = j + 1 + tx; c <= r; c += 32) G[r][c] -= lr * (G[c][j] * inv);
     }
     __syncthreads();
-    const float pj = piv;
-    for (int r = j + 1 + tid; r < NB; r += blockDim.x) G[r][j] /= pj;
-    __syncthreads();
-    // trailing update of the lower part: G[r][c] -= G[r][j] G[c][j], j < c <= r
-    const int rem = NB - 1 - j;
-    for (int idx = tid; idx < rem * rem; idx += blockDim.x) {
-      const int r = j + 1 + idx / rem, c = j + 1 + idx % rem;
-      if (c <= r) G[r][c] -= G[r][j] * G[c][j];
-    }
-    __syncthreads();
-  }
-  // inverse of the lower-triangular G: 4 threads per column
-  {
-    const int col = tid >> 2, q = tid & 3;
-    if (q == 0) X[col][col] = 1.f / G[col][col];
-    for (int r = 0; r < NB; ++r) {
-      // column col of X: rows r > col depend on rows col..r-1
-      __syncwarp();
-      float sum = 0.f;
-      if (r > col)
-        for (int l = col + q; l < r; l += 4) sum = fmaf(G[r][l], X[l][col], sum);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      if (q == 0) {
-        if (r > col) X[r][col] = -sum / G[r][r];
-        else if (r < col) X[r][col] = 0.f;
-      }
+    if (tid < NB) {
+      if (tid > j) G[tid][j] *= inv;
+      else if (tid == j) G[j][j] = piv;
     }
   }
   __syncthreads();
+  // inverse, row by row: X[r][c] = (delta_rc - acc[r][c]) / G[r][r] with acc
+  // kept in X's strict lower part until row r is final; then the rows below
+  // accumulate G[r'][r] X[r][c].  Row r of X is final at step r.
+  for (int r = 0; r < NB; ++r) {
+    const float ir = 1.f / G[r][r];
+    // rows r' > r, columns c <= r
+    for (int rp = r + 1 + ty; rp < NB; rp += 16) {
+      const float g = G[rp][r];
+      for (int c = tx; c <= r; c += 32) {
+        const float x = ((c == r ? 1.f : 0.f) - X[r][c]) * ir;
+        X[rp][c] += g * x;
+      }
+    }
+    __syncthreads();
+    if (tid <= r) X[r][tid] = ((tid == r ? 1.f : 0.f) - X[r][tid]) * ir;
+    __syncthreads();
+  }
   for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
     C[(o + r) * kp + o + c] = (c <= r) ? G[r][c] : 0.f;
@@ -304,6 +308,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     g.C = a.T; g.ldc = b; g.sC = b * b;
     g.M = b; g.N = b; g.K = b; g.alpha = 1.f; g.beta = 0.f;
     g.mclip_base = b; g.mclip_step = 2 * b; g.mclip_total = kp;
+    g.klo_from_col = 1;  // inv(G11) is lower triangular
     BK_TRY(gemm(g, npairs, s));
     // X21 = -inv(G22) * T_p
     GemmArgs h{};
@@ -312,6 +317,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     h.C = a.Ginv + b * kp; h.ldc = kp; h.sC = pstride;
     h.M = b; h.N = b; h.K = b; h.alpha = -1.f; h.beta = 0.f;
     h.mclip_base = b; h.mclip_step = 2 * b; h.mclip_total = kp;
+    h.khi_to_row = 1;    // inv(G22) is lower triangular
     const int64_t last = npairs - 1;
     const int64_t last_avail = kp - (b + last * 2 * b);  // rows of the last second block
     const int64_t nfull = last_avail >= b ? npairs : last;
