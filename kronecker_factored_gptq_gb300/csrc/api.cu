@@ -175,7 +175,8 @@ ALayout antidiag_layout(int64_t m, int64_t n) {
 
 struct PLayout {
   int64_t kp[2];
-  size_t status, scal, C[2], Ginv[2], T[2], total;
+  size_t status, scal, items[2], C[2], Chi[2], Clo[2], Gihi[2], Gilo[2], GiThi[2], GiTlo[2],
+      Thi[2], Tlo[2], total;
 };
 
 // Each factor has its own scratch: A and B are prepared concurrently.
@@ -189,9 +190,16 @@ PLayout prepare_layout(int64_t n, int64_t m) {
   L.scal = take(256);
   for (int w = 0; w < 2; ++w) {
     const size_t kk = sizeof(float) * (size_t)L.kp[w] * (size_t)L.kp[w];
+    L.items[w] = take(sizeof(WorkItem) * (size_t)(prepare_items_count(L.kp[w]) + 1));
     L.C[w] = take(kk);
-    L.Ginv[w] = take(kk);
-    L.T[w] = take(kk);
+    L.Chi[w] = take(kk);
+    L.Clo[w] = take(kk);
+    L.Gihi[w] = take(kk);
+    L.Gilo[w] = take(kk);
+    L.GiThi[w] = take(kk);
+    L.GiTlo[w] = take(kk);
+    L.Thi[w] = take(kk);
+    L.Tlo[w] = take(kk);
   }
   L.total = off;
   return L;
@@ -354,6 +362,7 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   if (n > (1 << 20) || m > (1 << 20)) return BAKRON_ERR_INVALID_ARG;
   const PLayout L = prepare_layout(n, m);
   if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
+  if (!prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   char* base = (char*)ws;
   DevStatus* st = (DevStatus*)(base + L.status);
@@ -374,8 +383,15 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
     pa.U = which == 0 ? UA : UB;
     pa.L = which == 0 ? LA : LB;
     pa.C = (float*)(base + L.C[which]);
-    pa.Ginv = (float*)(base + L.Ginv[which]);
-    pa.T = (float*)(base + L.T[which]);
+    pa.Chi = (float*)(base + L.Chi[which]);
+    pa.Clo = (float*)(base + L.Clo[which]);
+    pa.Gihi = (float*)(base + L.Gihi[which]);
+    pa.Gilo = (float*)(base + L.Gilo[which]);
+    pa.GiThi = (float*)(base + L.GiThi[which]);
+    pa.GiTlo = (float*)(base + L.GiTlo[which]);
+    pa.Thi = (float*)(base + L.Thi[which]);
+    pa.Tlo = (float*)(base + L.Tlo[which]);
+    pa.items = (WorkItem*)(base + L.items[which]);
     pa.scal = (float*)(base + L.scal) + which;
     pa.kp = L.kp[which];
     pa.which = which;

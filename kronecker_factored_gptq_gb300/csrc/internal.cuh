@@ -50,8 +50,10 @@ struct PropArgs {
   float* out_hi; float* out_lo; int64_t ldo;   // stage 1: Y^T split
   float* wt; int64_t ldw;                      // stage 2: W~ -= C
   const WorkItem* items; int n_items;
-  int stage;  // 1 or 2
+  int stage;  // 1: out = split(alpha C) [and tr = split(alpha C)^T]; 2: wt -= C
   int max_k;  // longest K range of the items, in tiles
+  float alpha;                       // stage 1 scale (0 means 1)
+  float* tr_hi; float* tr_lo; int64_t ldt;  // stage 1, nullable: transposed split store
   DevStatus* st;
 };
 
@@ -104,15 +106,19 @@ cudaError_t launch_antidiag(const AntidiagArgs& a, int* unsupported, cudaStream_
 struct PrepareFactorArgs {
   const float* X; int64_t k; float damp;
   float* U; float* L;            // outputs (L nullable)
-  float* C;                      // Kp x Kp scratch (flipped, then G)
-  float* Ginv;                   // Kp x Kp scratch (G^{-1})
-  float* T;                      // Kp x Kp scratch
-  float* scal;                   // device scalars (lambda)
+  float* C;                      // Kp x Kp: flipped matrix, then G (plain)
+  float* Chi; float* Clo;        // Kp x Kp: split panels of G (strictly lower blocks)
+  float* Gihi; float* Gilo;      // Kp x Kp: split G^{-1} (lower)
+  float* GiThi; float* GiTlo;    // Kp x Kp: split (G^{-1})^T (upper)
+  float* Thi; float* Tlo;        // Kp x Kp scratch: panel products, then T^T split
+  float* scal;                   // device scalar (lambda)
+  WorkItem* items;               // device buffer of prepare_items_count(kp) items
   int64_t kp;
   int which;                     // 0 = A, 1 = B (info slot)
   DevStatus* st;
 };
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s);
 int64_t prepare_pad(int64_t k);
+int64_t prepare_items_count(int64_t kp);
 
 }  // namespace bakron

@@ -10,13 +10,21 @@
 //   1. lambda = damp * mean(diag X);  C = J (X + lambda I) J          (flip)
 //   2. blocked right-looking Cholesky of C, block 128:
 //        diagonal block: one CTA factors it and inverts its factor in smem;
-//        panel: C21 <- C21 * inv(G11)^T  (product, via scratch);
-//        trailing: C22 -= C21 C21^T       (lower tiles only)
-//   3. G^{-1} by recursive doubling over block pairs:
-//        inv([[G11, 0], [G21, G22]]) has lower-left -inv(G22) G21 inv(G11)
+//        panel: P = C21 inv(G11)^T (fp32 FMA product), stored plain and
+//               split (hi = tf32, lo = rest) for the tensor cores;
+//        trailing: C22 -= P P^T on the lower tiles (tcgen05, 3xTF32)
+//   3. G^{-1} by recursive doubling over block pairs, all on tcgen05 with
+//      K-major operands: with G^{-1} and (G^{-1})^T both kept split,
+//        T^T = inv(G11)^T G21^T,   X21 = -inv(G22) T   (stored straight and
+//        transposed), skipping the zero blocks of the triangular factors
 //   4. U = J G^{-1} J, L = J G^T J        (flip back)
 // A non-positive or non-finite pivot records the first failing index and
 // BAKRON_ERR_NOT_PD; the pivot is replaced by 1 so the rest stays finite.
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <vector>
+
 #include "internal.cuh"
 
 namespace bakron {
@@ -154,14 +162,17 @@ __global__ void flip_damp_kernel(const float* __restrict__ X, int64_t k, const f
 // form a 16 x 32 grid over (row, column) of the trailing lower triangle.
 constexpr size_t kPotrfSmem = sizeof(float) * 2 * NB * (NB + 1);
 
-__global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Ginv, int64_t kp, int64_t kb,
-                                                          int64_t k_real, DevStatus* st, int which) {
+__global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi, float* Gilo,
+                                                          float* GiThi, float* GiTlo, float* inv_plain,
+                                                          int64_t kp, int64_t kb, int64_t k_real,
+                                                          DevStatus* st, int which) {
   extern __shared__ __align__(16) float psm[];
   float (*G)[NB + 1] = reinterpret_cast<float (*)[NB + 1]>(psm);
   float (*X)[NB + 1] = reinterpret_cast<float (*)[NB + 1]>(psm + NB * (NB + 1));
   const int tid = threadIdx.x;
   const int tx = tid & 31, ty = tid >> 5;
   const int64_t o = kb * NB;
+#pragma unroll 8
   for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
     G[r][c] = (c <= r) ? C[(o + r) * kp + o + c] : 0.f;
@@ -182,9 +193,32 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Ginv,
       d = 1.f;
     }
     const float piv = sqrtf(d), inv = 1.f / piv;
-    for (int r = j + 1 + ty; r < NB; r += 16) {
-      const float lr = G[r][j] * inv;
-      for (int c = j + 1 + tx; c <= r; c += 32) G[r][c] -= lr * (G[c][j] * inv);
+    // rows j+1+ty+16i (a warp-uniform count), 4 column slots per row,
+    // loaded first and stored after the update
+    {
+      float lc[4];
+#pragma unroll
+      for (int l = 0; l < 4; ++l) {
+        const int c = j + 1 + tx + 32 * l;
+        lc[l] = c < NB ? G[c][j] * inv : 0.f;
+      }
+      const int rem = NB - 1 - j;
+      const int nr = rem > ty ? (rem - 1 - ty) / 16 + 1 : 0;
+      for (int i = 0; i < nr; ++i) {
+        const int r = j + 1 + ty + 16 * i;
+        const float lr = G[r][j] * inv;
+        float v[4];
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+          const int c = j + 1 + tx + 32 * l;
+          v[l] = c <= r ? G[r][c] : 0.f;
+        }
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+          const int c = j + 1 + tx + 32 * l;
+          if (c <= r) G[r][c] = v[l] - lr * lc[l];
+        }
+      }
     }
     __syncthreads();
     if (tid < NB) {
@@ -198,12 +232,26 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Ginv,
   // accumulate G[r'][r] X[r][c].  Row r of X is final at step r.
   for (int r = 0; r < NB; ++r) {
     const float ir = 1.f / G[r][r];
-    // rows r' > r, columns c <= r
-    for (int rp = r + 1 + ty; rp < NB; rp += 16) {
-      const float g = G[rp][r];
-      for (int c = tx; c <= r; c += 32) {
-        const float x = ((c == r ? 1.f : 0.f) - X[r][c]) * ir;
-        X[rp][c] += g * x;
+    // rows r' > r (warp-uniform count), columns c <= r
+    {
+      float x[4];
+#pragma unroll
+      for (int l = 0; l < 4; ++l) {
+        const int c = tx + 32 * l;
+        x[l] = c <= r ? ((c == r ? 1.f : 0.f) - X[r][c]) * ir : 0.f;
+      }
+      const int rem = NB - 1 - r;
+      const int nr = rem > ty ? (rem - 1 - ty) / 16 + 1 : 0;
+      const int lmax = r / 32 + 1;
+      for (int i = 0; i < nr; ++i) {
+        const int rp = r + 1 + ty + 16 * i;
+        const float g = G[rp][r];
+        float v[4];
+#pragma unroll
+        for (int l = 0; l < 4; ++l) v[l] = (l < lmax && tx + 32 * l <= r) ? X[rp][tx + 32 * l] : 0.f;
+#pragma unroll
+        for (int l = 0; l < 4; ++l)
+          if (l < lmax && tx + 32 * l <= r) X[rp][tx + 32 * l] = v[l] + g * x[l];
       }
     }
     __syncthreads();
@@ -213,28 +261,46 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Ginv,
   for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
     C[(o + r) * kp + o + c] = (c <= r) ? G[r][c] : 0.f;
-    Ginv[(o + r) * kp + o + c] = (c <= r) ? X[r][c] : 0.f;
+    const float x = (c <= r) ? X[r][c] : 0.f;
+    const float h = tf32_round(x);
+    Gihi[(o + r) * kp + o + c] = h;
+    Gilo[(o + r) * kp + o + c] = x - h;
+    inv_plain[r * NB + c] = x;
+    // transposed: (G^{-1})^T[c][r] (coalesced over r for fixed c is not
+    // possible here; the block is 64 KiB)
+    const float xt = (r <= c) ? X[c][r] : 0.f;
+    const float ht = tf32_round(xt);
+    GiThi[(o + r) * kp + o + c] = ht;
+    GiTlo[(o + r) * kp + o + c] = xt - ht;
   }
 }
 
-__global__ void copy_block_kernel(const float* __restrict__ src, int64_t lds, float* __restrict__ dst,
-                                  int64_t ldd, int64_t rows, int64_t cols) {
+// dst = src (plain) and (dhi, dlo) = split(src), rows x cols
+__global__ void copy_split_kernel(const float* __restrict__ src, int64_t lds, float* __restrict__ dst,
+                                  float* __restrict__ dhi, float* __restrict__ dlo, int64_t ldd,
+                                  int64_t rows, int64_t cols) {
   const int64_t total = rows * cols;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = t / cols, c = t - r * cols;
-    dst[r * ldd + c] = src[r * lds + c];
+    const float v = src[r * lds + c];
+    const float h = tf32_round(v);
+    dst[r * ldd + c] = v;
+    dhi[r * ldd + c] = h;
+    dlo[r * ldd + c] = v - h;
   }
 }
 
 // U[i][j] = Ginv[k-1-i][k-1-j] (upper), L[i][j] = G[k-1-j][k-1-i] (lower)
-__global__ void finalize_kernel(const float* __restrict__ G, const float* __restrict__ Ginv, int64_t kp,
-                                int64_t k, float* __restrict__ U, float* __restrict__ L) {
+__global__ void finalize_kernel(const float* __restrict__ G, const float* __restrict__ Gihi,
+                                const float* __restrict__ Gilo, int64_t kp, int64_t k,
+                                float* __restrict__ U, float* __restrict__ L) {
   const int64_t total = k * k;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = t / k, j = t - i * k;
-    U[t] = (j >= i) ? Ginv[(k - 1 - i) * kp + (k - 1 - j)] : 0.f;
+    const int64_t g = (k - 1 - i) * kp + (k - 1 - j);
+    U[t] = (j >= i) ? Gihi[g] + Gilo[g] : 0.f;
     if (L) L[t] = (j <= i) ? G[(k - 1 - j) * kp + (k - 1 - i)] : 0.f;
   }
 }
@@ -254,6 +320,58 @@ int64_t prepare_pad(int64_t k) { return ((k + NB - 1) / NB) * NB; }
     if (e_ != cudaSuccess) return e_;   \
   } while (0)
 
+namespace {
+// Work items of the tensor-core products of one factor of padded order kp:
+// for every Cholesky step kb the lower tiles of the trailing matrix, then for
+// every doubling level the T^T tiles and the X21 tiles.
+struct PrepItems {
+  std::vector<WorkItem> items;
+  std::vector<int> syrk_off, syrk_n;   // per kb
+  std::vector<int> t_off, t_n, x_off, x_n, t_maxk, x_maxk;  // per level
+};
+
+const PrepItems& prep_items(int64_t kp) {
+  static std::mutex mu;
+  static std::map<int64_t, PrepItems> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(kp);
+  if (it != cache.end()) return it->second;
+  PrepItems P;
+  const int nb = (int)(kp / NB);
+  for (int kb = 0; kb < nb; ++kb) {
+    P.syrk_off.push_back((int)P.items.size());
+    for (int r = kb + 1; r < nb; ++r)
+      for (int c = kb + 1; c <= r; ++c) P.items.push_back(WorkItem{r, c, kb, kb + 1});
+    P.syrk_n.push_back((int)P.items.size() - P.syrk_off.back());
+  }
+  for (int B = 1; B < nb; B *= 2) {
+    P.t_off.push_back((int)P.items.size());
+    int mk = 0;
+    for (int p0 = 0; p0 < nb; p0 += 2 * B) {
+      const int b1 = p0, e1 = p0 + B, b2 = p0 + B, e2 = std::min(p0 + 2 * B, nb);
+      if (b2 >= e2) continue;
+      for (int r = b1; r < e1; ++r)
+        for (int n = b2; n < e2; ++n) { P.items.push_back(WorkItem{r, n, r, e1}); mk = std::max(mk, e1 - r); }
+    }
+    P.t_n.push_back((int)P.items.size() - P.t_off.back());
+    P.t_maxk.push_back(mk);
+    P.x_off.push_back((int)P.items.size());
+    mk = 0;
+    for (int p0 = 0; p0 < nb; p0 += 2 * B) {
+      const int b1 = p0, e1 = p0 + B, b2 = p0 + B, e2 = std::min(p0 + 2 * B, nb);
+      if (b2 >= e2) continue;
+      for (int r = b2; r < e2; ++r)
+        for (int n = b1; n < e1; ++n) { P.items.push_back(WorkItem{r, n, b2, r + 1}); mk = std::max(mk, r + 1 - b2); }
+    }
+    P.x_n.push_back((int)P.items.size() - P.x_off.back());
+    P.x_maxk.push_back(mk);
+  }
+  return cache.emplace(kp, std::move(P)).first->second;
+}
+}  // namespace
+
+int64_t prepare_items_count(int64_t kp) { return kp > 0 ? (int64_t)prep_items(kp).items.size() : 0; }
+
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   const int64_t k = a.k, kp = a.kp;
   const int64_t nblk = kp / NB;
@@ -263,76 +381,69 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
                                 (int)kPotrfSmem));
     attr_set = true;
   }
-  BK_TRY(cudaMemsetAsync(a.Ginv, 0, sizeof(float) * kp * kp, s));
+  const PrepItems& P = prep_items(kp);
+  if (!P.items.empty())
+    BK_TRY(cudaMemcpyAsync(a.items, P.items.data(), sizeof(WorkItem) * P.items.size(),
+                           cudaMemcpyHostToDevice, s));
   count_launch();
   diag_mean_kernel<<<1, 256, 0, s>>>(a.X, k, a.damp, a.scal);
   BK_TRY(cudaGetLastError());
   count_launch();
   flip_damp_kernel<<<grid_for(kp * kp), 256, 0, s>>>(a.X, k, a.scal, a.C, kp);
   BK_TRY(cudaGetLastError());
+  float* inv_plain = a.Tlo;   // 128 x 128 scratch during the Cholesky sweep
   for (int64_t kb = 0; kb < nblk; ++kb) {
     count_launch();
-  potrf_block_kernel<<<1, 512, kPotrfSmem, s>>>(a.C, a.Ginv, kp, kb, k, a.st, a.which);
+    potrf_block_kernel<<<1, 512, kPotrfSmem, s>>>(a.C, a.Gihi, a.Gilo, a.GiThi, a.GiTlo, inv_plain,
+                                                  kp, kb, k, a.st, a.which);
     BK_TRY(cudaGetLastError());
     const int64_t rest = kp - (kb + 1) * NB;
     if (rest <= 0) break;
     float* panel = a.C + (kb + 1) * NB * kp + kb * NB;
-    // T = panel * inv(G_kk)^T   (rest x 128), stored with ld = NB
+    // P = panel * inv(G_kk)^T  (rest x 128, ld = NB) in Thi
     GemmArgs g{};
     g.A = panel; g.lda = kp;
-    g.B = a.Ginv + kb * NB * kp + kb * NB; g.ldb = kp; g.transB = 1;
-    g.C = a.T; g.ldc = NB;
+    g.B = inv_plain; g.ldb = NB; g.transB = 1;
+    g.C = a.Thi; g.ldc = NB;
     g.M = rest; g.N = NB; g.K = NB; g.alpha = 1.f; g.beta = 0.f;
     BK_TRY(gemm(g, 1, s));
+    const int64_t off = (kb + 1) * NB * kp + kb * NB;
     count_launch();
-  copy_block_kernel<<<grid_for(rest * NB), 256, 0, s>>>(a.T, NB, panel, kp, rest, NB);
+    copy_split_kernel<<<grid_for(rest * NB), 256, 0, s>>>(a.Thi, NB, a.C + off, a.Chi + off, a.Clo + off,
+                                                          kp, rest, NB);
     BK_TRY(cudaGetLastError());
-    // trailing: C22 -= T T^T (lower tiles)
-    GemmArgs h{};
-    h.A = a.T; h.lda = NB;
-    h.B = a.T; h.ldb = NB; h.transB = 1;
-    h.C = a.C + (kb + 1) * NB * kp + (kb + 1) * NB; h.ldc = kp;
-    h.M = rest; h.N = rest; h.K = NB; h.alpha = -1.f; h.beta = 1.f; h.lower_only = 1;
-    BK_TRY(gemm(h, 1, s));
+    // trailing: C22 -= P P^T on the lower tiles (tensor cores)
+    PropArgs q{};
+    q.A_hi = a.Chi; q.A_lo = a.Clo; q.lda = kp; q.a_rows = kp;
+    q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
+    q.wt = a.C; q.ldw = kp;
+    q.items = a.items + P.syrk_off[kb]; q.n_items = P.syrk_n[kb]; q.max_k = 1;
+    q.stage = 2;
+    q.st = a.st;
+    BK_TRY(launch_prop_tc(q, s));
   }
-  // recursive doubling for G^{-1}: level b pairs blocks [2pb, 2pb+b) and
-  // [2pb+b, 2pb+2b); the second block of the last pair may be short (or
-  // absent), so its rows and the K of the second product are clipped.
-  for (int64_t b = NB; b < kp; b *= 2) {
-    const int64_t npairs = (kp + 2 * b - 1) / (2 * b);
-    const int64_t pstride = 2 * b * kp + 2 * b;
-    // T_p = G21 * inv(G11)
-    GemmArgs g{};
-    g.A = a.C + b * kp; g.lda = kp; g.sA = pstride;
-    g.B = a.Ginv; g.ldb = kp; g.sB = pstride; g.transB = 0;
-    g.C = a.T; g.ldc = b; g.sC = b * b;
-    g.M = b; g.N = b; g.K = b; g.alpha = 1.f; g.beta = 0.f;
-    g.mclip_base = b; g.mclip_step = 2 * b; g.mclip_total = kp;
-    g.klo_from_col = 1;  // inv(G11) is lower triangular
-    BK_TRY(gemm(g, npairs, s));
-    // X21 = -inv(G22) * T_p
-    GemmArgs h{};
-    h.A = a.Ginv + b * kp + b; h.lda = kp; h.sA = pstride;
-    h.B = a.T; h.ldb = b; h.sB = b * b; h.transB = 0;
-    h.C = a.Ginv + b * kp; h.ldc = kp; h.sC = pstride;
-    h.M = b; h.N = b; h.K = b; h.alpha = -1.f; h.beta = 0.f;
-    h.mclip_base = b; h.mclip_step = 2 * b; h.mclip_total = kp;
-    h.khi_to_row = 1;    // inv(G22) is lower triangular
-    const int64_t last = npairs - 1;
-    const int64_t last_avail = kp - (b + last * 2 * b);  // rows of the last second block
-    const int64_t nfull = last_avail >= b ? npairs : last;
-    BK_TRY(gemm(h, nfull, s));
-    if (last_avail > 0 && last_avail < b) {
-      GemmArgs hl = h;
-      hl.A = h.A + last * pstride; hl.B = h.B + last * (b * b); hl.C = h.C + last * pstride;
-      hl.sA = hl.sB = hl.sC = 0;
-      hl.mclip_base = b + last * 2 * b; hl.mclip_step = 0;
-      hl.K = last_avail;
-      BK_TRY(gemm(hl, 1, s));
-    }
+  // G^{-1} by recursive doubling (tensor cores)
+  for (size_t lvl = 0; lvl < P.t_off.size(); ++lvl) {
+    PropArgs t{};
+    t.A_hi = a.GiThi; t.A_lo = a.GiTlo; t.lda = kp; t.a_rows = kp;
+    t.B_hi = a.Chi; t.B_lo = a.Clo; t.ldb = kp; t.b_rows = kp;
+    t.out_hi = a.Thi; t.out_lo = a.Tlo; t.ldo = kp;
+    t.items = a.items + P.t_off[lvl]; t.n_items = P.t_n[lvl]; t.max_k = P.t_maxk[lvl];
+    t.stage = 1; t.alpha = 1.f;
+    t.st = a.st;
+    BK_TRY(launch_prop_tc(t, s));
+    PropArgs x{};
+    x.A_hi = a.Gihi; x.A_lo = a.Gilo; x.lda = kp; x.a_rows = kp;
+    x.B_hi = a.Thi; x.B_lo = a.Tlo; x.ldb = kp; x.b_rows = kp;
+    x.out_hi = a.Gihi; x.out_lo = a.Gilo; x.ldo = kp;
+    x.tr_hi = a.GiThi; x.tr_lo = a.GiTlo; x.ldt = kp;
+    x.items = a.items + P.x_off[lvl]; x.n_items = P.x_n[lvl]; x.max_k = P.x_maxk[lvl];
+    x.stage = 1; x.alpha = -1.f;
+    x.st = a.st;
+    BK_TRY(launch_prop_tc(x, s));
   }
   count_launch();
-  finalize_kernel<<<grid_for(k * k), 256, 0, s>>>(a.C, a.Ginv, kp, k, a.U, a.L);
+  finalize_kernel<<<grid_for(k * k), 256, 0, s>>>(a.C, a.Gihi, a.Gilo, kp, k, a.U, a.L);
   return cudaGetLastError();
 }
 

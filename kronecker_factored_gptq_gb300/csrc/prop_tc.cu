@@ -242,6 +242,22 @@ __global__ void __launch_bounds__(128, 1)
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ch * 32), v);
       if (p.stage == 1) {
+        if (p.alpha != 0.f && p.alpha != 1.f) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] *= p.alpha;
+        }
+        if (p.tr_hi) {
+          // transposed split store: lane = output row, so for each column the
+          // 32 lanes of a warp write 32 consecutive floats
+          const int64_t tcol = (int64_t)it.r * BM + row;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int64_t trow = (int64_t)it.c * BN + ch * 32 + q;
+            const float h = tf32_round(v[q]);
+            p.tr_hi[trow * p.ldt + tcol] = h;
+            p.tr_lo[trow * p.ldt + tcol] = v[q] - h;
+          }
+        }
         float* oh = p.out_hi + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN + ch * 32;
         float* ol = p.out_lo + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN + ch * 32;
 #pragma unroll
