@@ -157,118 +157,185 @@ __global__ void flip_damp_kernel(const float* __restrict__ X, int64_t k, const f
 }
 
 // Factor the diagonal block C[kb, kb] (128 x 128) in shared memory; write
-// G_kk (lower, zero upper) back and inv(G_kk) into Ginv's diagonal block.
-// Both loops are right-looking with one barrier per column / row; threads
-// form a 16 x 32 grid over (row, column) of the trailing lower triangle.
-constexpr size_t kPotrfSmem = sizeof(float) * 2 * NB * (NB + 1);
+// G_kk (lower, zero upper) back, inv(G_kk) split into Ginv's and (transposed)
+// into Ginv^T's diagonal block, and plainly into inv_plain (128 x 128).
+//
+// Blocked by 32: for each 32-wide column panel, one warp factors the 32 x 32
+// diagonal sub-block in registers (lane = row, shuffles), the rows below
+// solve against it (one thread per row), and all threads apply the trailing
+// update with 2-D register blocks.  The inverse starts from the four 32 x 32
+// diagonal inverses (one warp each, lane = column) and doubles twice,
+// X21 = -inv(G22) G21 inv(G11), with shared-memory products.
+constexpr size_t kPotrfSmem = sizeof(float) * 3 * NB * (NB + 1);
+constexpr int PP = NB + 1;
+
+// C = alpha * A * B over an M x N output (M, N multiples of 16, K <= 128),
+// A (M x K), B (K x N), C all row-major in shared memory with pitch PP.
+// kmax_row: A lower triangular (A[m][k] = 0 for k > m) -> K limited per row.
+__device__ __forceinline__ void smem_mm(float* C, const float* A, const float* B, int M, int N, int K, float alpha,
+                        bool a_lower) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int nbn = N / 2, nblocks = (M / 2) * nbn;
+  for (int blk = tid; blk < nblocks; blk += nth) {
+    const int m = (blk / nbn) * 2, n = (blk % nbn) * 2;
+    const int kend = a_lower ? min(K, m + 2) : K;
+    float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < kend; ++k) {
+      const float a0 = A[m * PP + k], a1 = A[(m + 1) * PP + k];
+      const float b0 = B[k * PP + n], b1 = B[k * PP + n + 1];
+      c00 = fmaf(a0, b0, c00); c01 = fmaf(a0, b1, c01);
+      c10 = fmaf(a1, b0, c10); c11 = fmaf(a1, b1, c11);
+    }
+    C[m * PP + n] = alpha * c00; C[m * PP + n + 1] = alpha * c01;
+    C[(m + 1) * PP + n] = alpha * c10; C[(m + 1) * PP + n + 1] = alpha * c11;
+  }
+}
 
 __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi, float* Gilo,
                                                           float* GiThi, float* GiTlo, float* inv_plain,
                                                           int64_t kp, int64_t kb, int64_t k_real,
                                                           DevStatus* st, int which) {
   extern __shared__ __align__(16) float psm[];
-  float (*G)[NB + 1] = reinterpret_cast<float (*)[NB + 1]>(psm);
-  float (*X)[NB + 1] = reinterpret_cast<float (*)[NB + 1]>(psm + NB * (NB + 1));
-  const int tid = threadIdx.x;
-  const int tx = tid & 31, ty = tid >> 5;
+  float* G = psm;                  // [NB][PP] the block, then its factor
+  float* X = G + NB * PP;          // [NB][PP] the inverse
+  float* S = X + NB * PP;          // [NB][PP] scratch
+  const unsigned FULLM = 0xffffffffu;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t o = kb * NB;
 #pragma unroll 8
   for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
-    G[r][c] = (c <= r) ? C[(o + r) * kp + o + c] : 0.f;
-    X[r][c] = 0.f;
+    G[r * PP + c] = (c <= r) ? C[(o + r) * kp + o + c] : 0.f;
+    X[r * PP + c] = 0.f;
   }
   __syncthreads();
-  // Cholesky: at column j every thread reads the pivot, updates its share of
-  // the trailing lower triangle with the scaled column, then column j is
-  // scaled in place (it is not read again).
-  for (int j = 0; j < NB; ++j) {
-    float d = G[j][j];
-    const bool bad = !(d > 0.f) || !isfinite(d);
-    if (bad) {
-      if (tid == 0 && o + j < k_real) {
-        atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + j));
-        set_status(st, BAKRON_ERR_NOT_PD);
-      }
-      d = 1.f;
-    }
-    const float piv = sqrtf(d), inv = 1.f / piv;
-    // rows j+1+ty+16i (a warp-uniform count), 4 column slots per row,
-    // loaded first and stored after the update
-    {
-      float lc[4];
+  for (int sb = 0; sb < NB / 32; ++sb) {
+    const int q = sb * 32;
+    // (1) diagonal 32 x 32 sub-block, warp 0, lane = row
+    if (warp == 0) {
+      float a[32];
 #pragma unroll
-      for (int l = 0; l < 4; ++l) {
-        const int c = j + 1 + tx + 32 * l;
-        lc[l] = c < NB ? G[c][j] * inv : 0.f;
-      }
-      const int rem = NB - 1 - j;
-      const int nr = rem > ty ? (rem - 1 - ty) / 16 + 1 : 0;
-      for (int i = 0; i < nr; ++i) {
-        const int r = j + 1 + ty + 16 * i;
-        const float lr = G[r][j] * inv;
-        float v[4];
+      for (int k = 0; k < 32; ++k) a[k] = (k <= lane) ? G[(q + lane) * PP + q + k] : 0.f;
 #pragma unroll
-        for (int l = 0; l < 4; ++l) {
-          const int c = j + 1 + tx + 32 * l;
-          v[l] = c <= r ? G[r][c] : 0.f;
+      for (int j = 0; j < 32; ++j) {
+        float d = __shfl_sync(FULLM, a[j], j);
+        if (!(d > 0.f) || !isfinite(d)) {
+          if (lane == 0 && o + q + j < k_real) {
+            atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + j));
+            set_status(st, BAKRON_ERR_NOT_PD);
+          }
+          d = 1.f;
         }
+        const float piv = sqrtf(d), inv = 1.f / piv;
+        const float l = a[j] * inv;
+        if (lane == j) a[j] = piv;
+        else if (lane > j) a[j] = l;
 #pragma unroll
-        for (int l = 0; l < 4; ++l) {
-          const int c = j + 1 + tx + 32 * l;
-          if (c <= r) G[r][c] = v[l] - lr * lc[l];
+        for (int k = 0; k < 32; ++k) {
+          if (k > j) {
+            const float lk = __shfl_sync(FULLM, l, k);
+            if (lane >= k) a[k] -= l * lk;
+          }
         }
       }
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (k <= lane) G[(q + lane) * PP + q + k] = a[k];
     }
     __syncthreads();
-    if (tid < NB) {
-      if (tid > j) G[tid][j] *= inv;
-      else if (tid == j) G[j][j] = piv;
+    const int base = q + 32, n2 = NB - base;
+    if (n2 <= 0) break;
+    // (2) rows below: l[c] = (G[r][q+c] - sum_{t<c} l[t] L11[c][t]) / L11[c][c]
+    if (tid < n2) {
+      const int r = base + tid;
+      float l[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) l[c] = G[r * PP + q + c];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float acc = l[c];
+#pragma unroll
+        for (int t = 0; t < c; ++t) acc = fmaf(-l[t], G[(q + c) * PP + q + t], acc);
+        l[c] = acc / G[(q + c) * PP + q + c];
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) G[r * PP + q + c] = l[c];
     }
+    __syncthreads();
+    // (3) trailing lower triangle: G[r][c] -= sum_t L21[r][t] L21[c][t]
+    {
+      const int tx = tid & 31, ty = tid >> 5;    // rows base+ty+16i, cols base+tx+32l
+      float acc[6][3];
+#pragma unroll
+      for (int i = 0; i < 6; ++i)
+#pragma unroll
+        for (int l = 0; l < 3; ++l) acc[i][l] = 0.f;
+      for (int t = 0; t < 32; ++t) {
+        float ar[6], bc[3];
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+          const int r = base + ty + 16 * i;
+          ar[i] = r < NB ? G[r * PP + q + t] : 0.f;
+        }
+#pragma unroll
+        for (int l = 0; l < 3; ++l) {
+          const int c = base + tx + 32 * l;
+          bc[l] = c < NB ? G[c * PP + q + t] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 6; ++i)
+#pragma unroll
+          for (int l = 0; l < 3; ++l) acc[i][l] = fmaf(ar[i], bc[l], acc[i][l]);
+      }
+      __syncthreads();   // every read of this panel precedes the writes below
+#pragma unroll
+      for (int i = 0; i < 6; ++i)
+#pragma unroll
+        for (int l = 0; l < 3; ++l) {
+          const int r = base + ty + 16 * i, c = base + tx + 32 * l;
+          if (r < NB && c <= r) G[r * PP + c] -= acc[i][l];
+        }
+    }
+    __syncthreads();
+  }
+  // inverse: four 32 x 32 diagonal inverses, warp w < 4 for block w, lane = column
+  if (warp < NB / 32) {
+    const int q = warp * 32;
+    float x[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      float acc = (r == lane) ? 1.f : 0.f;
+#pragma unroll
+      for (int t = 0; t < r; ++t) acc = fmaf(-G[(q + r) * PP + q + t], x[t], acc);
+      x[r] = acc / G[(q + r) * PP + q + r];
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) X[(q + r) * PP + q + lane] = x[r];
   }
   __syncthreads();
-  // inverse, row by row: X[r][c] = (delta_rc - acc[r][c]) / G[r][r] with acc
-  // kept in X's strict lower part until row r is final; then the rows below
-  // accumulate G[r'][r] X[r][c].  Row r of X is final at step r.
-  for (int r = 0; r < NB; ++r) {
-    const float ir = 1.f / G[r][r];
-    // rows r' > r (warp-uniform count), columns c <= r
-    {
-      float x[4];
-#pragma unroll
-      for (int l = 0; l < 4; ++l) {
-        const int c = tx + 32 * l;
-        x[l] = c <= r ? ((c == r ? 1.f : 0.f) - X[r][c]) * ir : 0.f;
-      }
-      const int rem = NB - 1 - r;
-      const int nr = rem > ty ? (rem - 1 - ty) / 16 + 1 : 0;
-      const int lmax = r / 32 + 1;
-      for (int i = 0; i < nr; ++i) {
-        const int rp = r + 1 + ty + 16 * i;
-        const float g = G[rp][r];
-        float v[4];
-#pragma unroll
-        for (int l = 0; l < 4; ++l) v[l] = (l < lmax && tx + 32 * l <= r) ? X[rp][tx + 32 * l] : 0.f;
-#pragma unroll
-        for (int l = 0; l < 4; ++l)
-          if (l < lmax && tx + 32 * l <= r) X[rp][tx + 32 * l] = v[l] + g * x[l];
-      }
+  // doubling: b = 32, 64.  X21 = -inv(G22) (G21 inv(G11)) for pairs of blocks
+  for (int b = 32; b < NB; b *= 2) {
+    for (int p0 = 0; p0 < NB; p0 += 2 * b) {
+      // S = G21 * inv(G11)  (b x b), placed at S[p0+b.., p0..]
+      smem_mm(S + (p0 + b) * PP + p0, G + (p0 + b) * PP + p0, X + p0 * PP + p0, b, b, b, 1.f, false);
     }
     __syncthreads();
-    if (tid <= r) X[r][tid] = ((tid == r ? 1.f : 0.f) - X[r][tid]) * ir;
+    for (int p0 = 0; p0 < NB; p0 += 2 * b) {
+      smem_mm(X + (p0 + b) * PP + p0, X + (p0 + b) * PP + p0 + b, S + (p0 + b) * PP + p0, b, b, b,
+              -1.f, true);
+    }
     __syncthreads();
   }
   for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
-    C[(o + r) * kp + o + c] = (c <= r) ? G[r][c] : 0.f;
-    const float x = (c <= r) ? X[r][c] : 0.f;
+    C[(o + r) * kp + o + c] = (c <= r) ? G[r * PP + c] : 0.f;
+    const float x = (c <= r) ? X[r * PP + c] : 0.f;
     const float h = tf32_round(x);
     Gihi[(o + r) * kp + o + c] = h;
     Gilo[(o + r) * kp + o + c] = x - h;
     inv_plain[r * NB + c] = x;
-    // transposed: (G^{-1})^T[c][r] (coalesced over r for fixed c is not
-    // possible here; the block is 64 KiB)
-    const float xt = (r <= c) ? X[c][r] : 0.f;
+    const float xt = (r <= c) ? X[c * PP + r] : 0.f;
     const float ht = tf32_round(xt);
     GiThi[(o + r) * kp + o + c] = ht;
     GiTlo[(o + r) * kp + o + c] = xt - ht;
