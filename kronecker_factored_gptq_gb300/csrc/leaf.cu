@@ -41,15 +41,17 @@ constexpr int PR = T + TPR;         // rT pitch (TPR mod 32): conflict-free colu
 constexpr int PU = T + TPR - 1;     // Ua pitch (TPR - 1 mod 32): conflict-free row reads
 constexpr int PE = T;               // Es pitch
 constexpr int NSTEP = 2 * T - 1;
+// rT has one extra all-zero row (index T): inactive rows read it instead of
+// predicating every load
 constexpr size_t kLeafSmem =
-    sizeof(float) * ((size_t)T * PR + (size_t)T * PU + (size_t)T * PE + T) + (size_t)T * T;
+    sizeof(float) * ((size_t)(T + 1) * PR + (size_t)T * PU + (size_t)T * PE + T) + (size_t)T * T;
 constexpr unsigned FULL = 0xffffffffu;
 }  // namespace
 
 __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   extern __shared__ __align__(16) float smem[];
-  float* rT = smem;                       // [T][PR] completed row accumulators, transposed
-  float* Ua = rT + T * PR;                // [T][PU]
+  float* rT = smem;                       // [T+1][PR] completed row accumulators, transposed
+  float* Ua = rT + (T + 1) * PR;          // [T][PU]
   float* Es = Ua + T * PU;                // [T][PE]: x0, then the scaled error
   float* lA = Es + T * PE;                // [T]: 1 / Ua(b, b)
   signed char* cs = reinterpret_cast<signed char*>(lA + T);  // [T][T] codes
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
     const int r = idx / T, c = idx - r * T;
     Es[r * PE + c] = a.wt[(i0 + r) * a.ldw + j0 + c];
   }
-  for (int idx = tid; idx < T * PR; idx += NTHR) rT[idx] = 0.f;
+  for (int idx = tid; idx < (T + 1) * PR; idx += NTHR) rT[idx] = 0.f;
 
   float ub[CH];
   {
@@ -115,14 +117,14 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         // ub[t >= cnt] are 0 and rT is zero-initialised, so a group may run
         // past cnt); two accumulators shorten the dependent chain
         const int cm = __reduce_max_sync(FULL, act ? cnt : 0);
-        const float* rc = rT + b * PR + q;
+        const float* rc = rT + (act ? b : T) * PR + q;   // row T is all zero
         float p1 = 0.f;
 #pragma unroll
         for (int tb = 0; tb < CH; tb += 8) {
           if (tb >= cm) break;
           float v[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = act ? rc[TPR * (tb + u)] : 0.f;
+          for (int u = 0; u < 8; ++u) v[u] = rc[TPR * (tb + u)];
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
             p = fmaf(ub[tb + u], v[u], p);
@@ -153,16 +155,21 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         int jend = X > 0 ? (X + TPR - 1) / TPR : 0;
         jend = jend < NFR ? jend : NFR;
         const int jm = __reduce_max_sync(FULL, act ? jend : 0);
-        const float* ur = Ua + b * PU + TPR * kb + q - row;  // ur[TPR j] = Ua(b, b'')
+        // ur[TPR j] = Ua(b, b'').  The update is not predicated per element:
+        // entries with b'' >= T or left of the current column are registers
+        // that are never published again (the row is done with them, or they
+        // drop out at the next shift), and an inactive row has e = 0 and reads
+        // finite shared values; every address stays inside this CTA's shared
+        // memory.  Only the number of 8-groups is bounded.
+        const float* ur = Ua + b * PU + TPR * kb + q - row;
+        if (act && (q >= sg)) FR[0] = fmaf(e, ur[0], FR[0]);
 #pragma unroll
-        for (int jb = 0; jb < NFR; jb += 8) {
+        for (int jb = 1; jb < NFR; jb += 8) {
           if (jb >= jm) break;
           float w[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = jb + u;
-            w[u] = (j < NFR && act && j < jend && (j > 0 || q >= sg)) ? ur[TPR * j] : 0.f;
-          }
+          for (int u = 0; u < 8; ++u)
+            if (jb + u < NFR) w[u] = ur[TPR * (jb + u)];
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             if (jb + u < NFR) FR[jb + u] = fmaf(e, w[u], FR[jb + u]);
