@@ -169,7 +169,7 @@ bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n,
  * and fragment the pool), or code that cannot keep a workspace between
  * calls.  The paper has no counterpart; this is a deployment convenience.
  * Same arguments and result as bakron_quantize with default options and no
- * preround output, but no workspace: the library uses a fixed 12 MiB scratch
+ * preround output, but no workspace: the library uses a fixed 16 MiB scratch
  * array of its own on each GPU (held until the process exits), so m and n
  * must be at most 512 (larger sizes return BAKRON_ERR_INVALID_ARG).  The
  * first call on a device resolves that array's address (make it before any

@@ -35,18 +35,26 @@ constexpr int T = kTile;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+struct Chunk {
+  int off, n, maxk;     // stage-2 items
+  int dlo, dhi;         // target tile anti-diagonals [dlo, dhi)
+  double flops;
+};
+
 struct Op {
   int kind;                // 0 = leaf, 1 = propagation
   int D, I0, ntiles;       // leaf
-  int off1, n1, off2, n2;  // propagation: item ranges of stage 1 and stage 2
-  int maxk1, maxk2;        // longest K range (tiles) of each stage
-  double flops1, flops2;
+  int off1, n1, maxk1;     // propagation stage 1
+  int depth;               // recursion depth (selects the Y buffer and side stream)
+  int chunk0, nchunks;     // stage-2 chunks (first one is urgent)
+  double flops1;
 };
 
 struct Schedule {
-  int M = 0, N = 0;
+  int M = 0, N = 0, max_depth = 0;
   std::vector<WorkItem> items;
   std::vector<Op> ops;
+  std::vector<Chunk> chunks;
 };
 
 // Items of one stage are sorted longest-K first so the big tiles start early.
@@ -56,13 +64,19 @@ void sort_items(std::vector<WorkItem>& v, size_t from) {
   });
 }
 
-void build_prop(Schedule& s, int D0, int Dm, int D1) {
+// Stage 2 of a propagation into band [Dm, D1) is split by target tile
+// anti-diagonal into chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...: the
+// first is needed by the very next leaf, the others only later, so they run
+// on a side stream while the next leaves proceed.
+void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
   const int M = s.M, N = s.N;
   Op op{};
   op.kind = 1;
+  op.depth = depth;
+  s.max_depth = std::max(s.max_depth, depth);
   op.off1 = (int)s.items.size();
-  double f1 = 0, f2 = 0;
-  int mk1 = 0, mk2 = 0;
+  double f1 = 0;
+  int mk1 = 0;
   for (int I = 0; I < M; ++I) {
     const int jlo = std::max(D0 - I, 0), jhi = std::min(Dm - I, N);
     if (jlo >= jhi) continue;
@@ -77,27 +91,37 @@ void build_prop(Schedule& s, int D0, int Dm, int D1) {
   }
   sort_items(s.items, op.off1);
   op.n1 = (int)s.items.size() - op.off1;
-  op.off2 = (int)s.items.size();
-  for (int Ip = 0; Ip < M; ++Ip) {
-    for (int Jp = std::max(Dm - Ip, 0); Jp < std::min(D1 - Ip, N); ++Jp) {
-      const int ilo = std::max(std::max(0, D0 - Jp), D0 - N + 1);
-      const int ihi = std::min(Ip, Dm - 1);
-      if (ilo > ihi) continue;
-      s.items.push_back(WorkItem{Ip, Jp, ilo, ihi + 1});
-      f2 += 2.0 * T * T * T * (ihi + 1 - ilo);
-      mk2 = std::max(mk2, ihi + 1 - ilo);
-    }
-  }
-  sort_items(s.items, op.off2);
-  op.n2 = (int)s.items.size() - op.off2;
   op.flops1 = f1;
-  op.flops2 = f2;
   op.maxk1 = mk1;
-  op.maxk2 = mk2;
+  op.chunk0 = (int)s.chunks.size();
+  int lo = Dm, width = 1;
+  while (lo < D1) {
+    const int hi = std::min(D1, lo + width);
+    Chunk c{};
+    c.off = (int)s.items.size();
+    c.dlo = lo;
+    c.dhi = hi;
+    for (int Ip = 0; Ip < M; ++Ip) {
+      for (int Jp = std::max(lo - Ip, 0); Jp < std::min(hi - Ip, N); ++Jp) {
+        const int ilo = std::max(std::max(0, D0 - Jp), D0 - N + 1);
+        const int ihi = std::min(Ip, Dm - 1);
+        if (ilo > ihi) continue;
+        s.items.push_back(WorkItem{Ip, Jp, ilo, ihi + 1});
+        c.flops += 2.0 * T * T * T * (ihi + 1 - ilo);
+        c.maxk = std::max(c.maxk, ihi + 1 - ilo);
+      }
+    }
+    sort_items(s.items, c.off);
+    c.n = (int)s.items.size() - c.off;
+    s.chunks.push_back(c);
+    lo = hi;
+    if (lo > Dm + 1) width *= 2;
+  }
+  op.nchunks = (int)s.chunks.size() - op.chunk0;
   s.ops.push_back(op);
 }
 
-void build_rec(Schedule& s, int D0, int D1) {
+void build_rec(Schedule& s, int D0, int D1, int depth) {
   if (D1 - D0 <= 1) {
     Op op{};
     op.kind = 0;
@@ -108,9 +132,9 @@ void build_rec(Schedule& s, int D0, int D1) {
     return;
   }
   const int Dm = (D0 + D1) / 2;
-  build_rec(s, D0, Dm);
-  build_prop(s, D0, Dm, D1);
-  build_rec(s, Dm, D1);
+  build_rec(s, D0, Dm, depth + 1);
+  build_prop(s, D0, Dm, D1, depth);
+  build_rec(s, Dm, D1, depth + 1);
 }
 
 const Schedule& get_schedule(int M, int N) {
@@ -123,13 +147,17 @@ const Schedule& get_schedule(int M, int N) {
   Schedule s;
   s.M = M;
   s.N = N;
-  build_rec(s, 0, M + N - 1);
+  build_rec(s, 0, M + N - 1, 0);
   return cache.emplace(key, std::move(s)).first->second;
 }
 
+constexpr int kMaxDepth = 24;
+
 struct QLayout {
   int64_t M, N, Mp, Np;
-  size_t status, sched, scale, wt, ehi, elo, yhi, ylo, lathi, latlo, lbthi, lbtlo, total;
+  int ndepth;
+  size_t status, sched, scale, wt, ehi, elo, yhi[kMaxDepth], ylo[kMaxDepth], lathi, latlo, lbthi,
+      lbtlo, total;
 };
 
 QLayout quantize_layout(int64_t m, int64_t n) {
@@ -139,6 +167,7 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   L.Mp = L.M * T;
   L.Np = L.N * T;
   const Schedule& s = get_schedule((int)L.M, (int)L.N);
+  L.ndepth = s.ops.size() > 1 ? s.max_depth + 1 : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
   const size_t f = sizeof(float);
@@ -148,8 +177,12 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   L.wt = take(f * L.Mp * L.Np);
   L.ehi = take(f * L.Mp * L.Np);
   L.elo = take(f * L.Mp * L.Np);
-  L.yhi = take(f * L.Np * L.Mp);
-  L.ylo = take(f * L.Np * L.Mp);
+  // one Y^T pair per recursion depth: a propagation's deferred chunks may
+  // still be reading its Y^T while deeper propagations write theirs
+  for (int d = 0; d < L.ndepth; ++d) {
+    L.yhi[d] = take(f * L.Np * L.Mp);
+    L.ylo[d] = take(f * L.Np * L.Mp);
+  }
   L.lathi = take(f * L.Np * L.Np);
   L.latlo = take(f * L.Np * L.Np);
   L.lbthi = take(f * L.Mp * L.Mp);
@@ -230,6 +263,49 @@ cudaError_t aux_stream(AuxStream** out) {
   return cudaSuccess;
 }
 
+// Streams of the solve, per device, created once: a high-priority critical
+// stream (leaves, stage 1, urgent stage-2 chunks) and one default-priority
+// side stream per recursion depth (deferred stage-2 chunks), plus a pool of
+// reusable events.  Calls are synchronous, so the pool is reused per call.
+struct SolveStreams {
+  cudaStream_t crit = nullptr;
+  cudaStream_t side[kMaxDepth] = {};
+  std::vector<cudaEvent_t> events;
+  std::mutex mu;
+};
+
+cudaError_t solve_streams(SolveStreams** out) {
+  static std::mutex mu;
+  static SolveStreams per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  SolveStreams& ss = per_dev[dev];
+  if (!ss.crit) {
+    int lo = 0, hi = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&ss.crit, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
+    for (int d = 0; d < kMaxDepth; ++d)
+      if ((e = cudaStreamCreateWithPriority(&ss.side[d], cudaStreamNonBlocking, lo)) != cudaSuccess)
+        return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
+cudaError_t pool_event(SolveStreams* ss, size_t idx, cudaEvent_t* ev) {
+  while (ss->events.size() <= idx) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (r != cudaSuccess) return r;
+    ss->events.push_back(e);
+  }
+  *ev = ss->events[idx];
+  return cudaSuccess;
+}
+
 #define TRY_CUDA(x)                                        \
   do {                                                     \
     cudaError_t e_ = (x);                                  \
@@ -273,6 +349,10 @@ struct PhaseTimer {
     if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return; }
     cudaEventRecord(b, s);
     rec.push_back({cat, {a, b}});
+  }
+  void adopt(PhaseTimer& other) {
+    for (auto& r : other.rec) rec.push_back(r);
+    other.rec.clear();
   }
   void collect() {
     if (!out) return;
@@ -429,6 +509,11 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   if (o.use_3xtf32 && !prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
   const Schedule& sch = get_schedule((int)L.M, (int)L.N);
   cudaStream_t s = (cudaStream_t)stream;
+  SolveStreams* ss = nullptr;
+  TRY_CUDA(solve_streams(&ss));
+  std::lock_guard<std::mutex> slk(ss->mu);
+  size_t nev = 0;
+  auto next_event = [&](cudaEvent_t* ev) { return pool_event(ss, nev++, ev); };
   char* base = (char*)ws;
   DevStatus* st = (DevStatus*)(base + L.status);
   WorkItem* items = (WorkItem*)(base + L.sched);
@@ -436,26 +521,32 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   float* wt = (float*)(base + L.wt);
   float* ehi = (float*)(base + L.ehi);
   float* elo = (float*)(base + L.elo);
-  float* yhi = (float*)(base + L.yhi);
-  float* ylo = (float*)(base + L.ylo);
   float* lathi = (float*)(base + L.lathi);
   float* latlo = (float*)(base + L.latlo);
   float* lbthi = (float*)(base + L.lbthi);
   float* lbtlo = (float*)(base + L.lbtlo);
   if (o.times) std::memset(o.times, 0, sizeof(*o.times));
-  PhaseTimer pt(o.times, s);
 
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
   if (!sch.items.empty())
     TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
                              cudaMemcpyHostToDevice, s));
+  // fork onto the critical stream
+  cudaStream_t cs = ss->crit;
+  {
+    cudaEvent_t ev;
+    TRY_CUDA(next_event(&ev));
+    TRY_CUDA(cudaEventRecord(ev, s));
+    TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+  }
+  PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
-    TRY_CUDA(launch_check_finite(scale, m, st, s));
-    TRY_CUDA(launch_pad_scale(scale, m, sp, L.Mp, s));
-    TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, s));
-    TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, s));
-    TRY_CUDA(launch_transpose_split(UB, m, lbthi, lbtlo, L.Mp, s));
+    TRY_CUDA(launch_check_finite(scale, m, st, cs));
+    TRY_CUDA(launch_pad_scale(scale, m, sp, L.Mp, cs));
+    TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
+    TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
+    TRY_CUDA(launch_transpose_split(UB, m, lbthi, lbtlo, L.Mp, cs));
     pt.end(3, ev);
   }
   LeafArgs la{};
@@ -467,36 +558,74 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   la.V = V; la.codes = codes; la.preround = preround;
   la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
   la.st = st;
-  PropArgs p1{};
-  p1.A_hi = lathi; p1.A_lo = latlo; p1.lda = L.Np; p1.a_rows = L.Np;
-  p1.B_hi = ehi; p1.B_lo = elo; p1.ldb = L.Np; p1.b_rows = L.Mp;
-  p1.out_hi = yhi; p1.out_lo = ylo; p1.ldo = L.Mp;
-  p1.stage = 1;
-  p1.st = st;
-  PropArgs p2{};
-  p2.A_hi = lbthi; p2.A_lo = lbtlo; p2.lda = L.Mp; p2.a_rows = L.Mp;
-  p2.B_hi = yhi; p2.B_lo = ylo; p2.ldb = L.Mp; p2.b_rows = L.Np;
-  p2.wt = wt; p2.ldw = L.Np;
-  p2.stage = 2;
-  p2.st = st;
+  // events each leaf must wait for (deferred chunks covering its diagonal)
+  std::vector<std::vector<cudaEvent_t>> waits((size_t)(L.M + L.N));
   for (const Op& op : sch.ops) {
     if (op.kind == 0) {
+      for (cudaEvent_t ev : waits[op.D]) TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
       la.D = op.D;
       la.I0 = op.I0;
       cudaEvent_t ev = pt.begin();
-      TRY_CUDA(launch_leaf(la, op.ntiles, s));
+      TRY_CUDA(launch_leaf(la, op.ntiles, cs));
       pt.end(0, ev);
-    } else {
-      p1.items = items + op.off1; p1.n_items = op.n1; p1.max_k = op.maxk1;
-      p2.items = items + op.off2; p2.n_items = op.n2; p2.max_k = op.maxk2;
-      cudaEvent_t ev = pt.begin();
-      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p1, s) : launch_prop_simt(p1, s));
-      pt.end(1, ev);
-      ev = pt.begin();
-      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p2, s) : launch_prop_simt(p2, s));
-      pt.end(2, ev);
-      if (o.times) o.times->prop_flops += op.flops1 + op.flops2;
+      continue;
     }
+    float* yhi = (float*)(base + L.yhi[op.depth]);
+    float* ylo = (float*)(base + L.ylo[op.depth]);
+    PropArgs p1{};
+    p1.A_hi = lathi; p1.A_lo = latlo; p1.lda = L.Np; p1.a_rows = L.Np;
+    p1.B_hi = ehi; p1.B_lo = elo; p1.ldb = L.Np; p1.b_rows = L.Mp;
+    p1.out_hi = yhi; p1.out_lo = ylo; p1.ldo = L.Mp;
+    p1.stage = 1;
+    p1.st = st;
+    p1.items = items + op.off1; p1.n_items = op.n1; p1.max_k = op.maxk1;
+    PropArgs p2{};
+    p2.A_hi = lbthi; p2.A_lo = lbtlo; p2.lda = L.Mp; p2.a_rows = L.Mp;
+    p2.B_hi = yhi; p2.B_lo = ylo; p2.ldb = L.Mp; p2.b_rows = L.Np;
+    p2.wt = wt; p2.ldw = L.Np;
+    p2.stage = 2;
+    p2.st = st;
+    {
+      cudaEvent_t ev = pt.begin();
+      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p1, cs) : launch_prop_simt(p1, cs));
+      pt.end(1, ev);
+    }
+    cudaEvent_t ev_s1 = nullptr;
+    if (op.nchunks > 1) {
+      TRY_CUDA(next_event(&ev_s1));
+      TRY_CUDA(cudaEventRecord(ev_s1, cs));
+    }
+    for (int c = 0; c < op.nchunks; ++c) {
+      const Chunk& ch = sch.chunks[op.chunk0 + c];
+      if (o.times) o.times->prop_flops += ch.flops;
+      if (ch.n == 0) continue;
+      p2.items = items + ch.off; p2.n_items = ch.n; p2.max_k = ch.maxk;
+      cudaStream_t cstr = c == 0 ? cs : ss->side[op.depth];
+      if (c > 0) TRY_CUDA(cudaStreamWaitEvent(cstr, ev_s1, 0));
+      PhaseTimer* tm = &pt;
+      PhaseTimer side_pt(o.times, cstr);
+      if (c > 0) tm = &side_pt;
+      cudaEvent_t ev = tm->begin();
+      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p2, cstr) : launch_prop_simt(p2, cstr));
+      tm->end(2, ev);
+      if (c > 0) {
+        side_pt.s = cstr;
+        pt.adopt(side_pt);
+        cudaEvent_t done;
+        TRY_CUDA(next_event(&done));
+        TRY_CUDA(cudaEventRecord(done, cstr));
+        for (int d = ch.dlo; d < ch.dhi; ++d) waits[d].push_back(done);
+      }
+    }
+    if (o.times) o.times->prop_flops += op.flops1;
+  }
+  // join back onto the caller's stream (every deferred chunk was waited for
+  // by the leaf of its diagonals, so the critical stream is last)
+  {
+    cudaEvent_t ev;
+    TRY_CUDA(next_event(&ev));
+    TRY_CUDA(cudaEventRecord(ev, cs));
+    TRY_CUDA(cudaStreamWaitEvent(s, ev, 0));
   }
   DevStatus h{};
   bakron_status r = finish(s, st, &h);

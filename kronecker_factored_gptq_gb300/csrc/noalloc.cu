@@ -27,7 +27,7 @@
 namespace bakron {
 
 constexpr int64_t kNoAllocMaxDim = 512;
-constexpr size_t kNoAllocBytes = (size_t)12 << 20;  // 12 MiB
+constexpr size_t kNoAllocBytes = (size_t)16 << 20;  // 16 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 

@@ -84,10 +84,8 @@ __global__ void __launch_bounds__(256) prop_simt_kernel(PropArgs p) {
         *reinterpret_cast<float4*>(p.out_lo + r * p.ldo + c) = l;
       } else {
         float4* w = reinterpret_cast<float4*>(p.wt + r * p.ldw + c);
-        float4 v = *w;
-        v.x -= acc[i][jh * 4 + 0]; v.y -= acc[i][jh * 4 + 1];
-        v.z -= acc[i][jh * 4 + 2]; v.w -= acc[i][jh * 4 + 3];
-        *w = v;
+        atomicAdd(w, make_float4(-acc[i][jh * 4 + 0], -acc[i][jh * 4 + 1], -acc[i][jh * 4 + 2],
+                                 -acc[i][jh * 4 + 3]));
       }
     }
   }

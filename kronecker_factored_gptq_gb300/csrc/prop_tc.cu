@@ -271,14 +271,13 @@ __global__ void __launch_bounds__(128, 1)
           reinterpret_cast<float4*>(ol)[q] = l;
         }
       } else {
+        // atomic: propagations of different recursion depths may update the
+        // same tile concurrently (they run on different streams)
         float4* w = reinterpret_cast<float4*>(p.wt + ((int64_t)it.r * BM + row) * p.ldw +
                                               (int64_t)it.c * BN + ch * 32);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 x = w[q];
-          x.x -= v[4 * q + 0]; x.y -= v[4 * q + 1]; x.z -= v[4 * q + 2]; x.w -= v[4 * q + 3];
-          w[q] = x;
-        }
+        for (int q = 0; q < 8; ++q)
+          atomicAdd(w + q, make_float4(-v[4 * q + 0], -v[4 * q + 1], -v[4 * q + 2], -v[4 * q + 3]));
       }
     }
   }
