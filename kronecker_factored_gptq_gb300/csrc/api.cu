@@ -555,6 +555,7 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   la.lbt_hi = lbthi; la.lbt_lo = lbtlo; la.ldb = L.Mp;
   la.scale = sp;
   la.e_hi = ehi; la.e_lo = elo;
+  la.round_lo = o.use_3xtf32;
   la.V = V; la.codes = codes; la.preround = preround;
   la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
   la.st = st;

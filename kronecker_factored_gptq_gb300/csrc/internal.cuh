@@ -63,6 +63,7 @@ struct LeafArgs {
   const float* lbt_hi; const float* lbt_lo; int64_t ldb;  // U_B^T split (Mp x Mp)
   const float* scale;                // padded row scales (Mp)
   float* e_hi; float* e_lo;          // scaled errors, split (Mp x Np, ld = ldw)
+  int round_lo;                      // e_lo rounded to tf32 (read by the tensor cores)
   float* V; int8_t* codes; float* preround;  // outputs, m x n (preround nullable)
   int64_t m, n;
   int qmin, qmax;

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
     const float h = tf32_round(e);
     const int64_t g = (i0 + r) * a.ldw + j0 + cc;
     a.e_hi[g] = h;
-    a.e_lo[g] = e - h;
+    a.e_lo[g] = a.round_lo ? tf32_round(e - h) : e - h;
     const int64_t ii = i0 + r, jj = j0 + cc;
     if (ii < a.m && jj < a.n) {
       const signed char code = cs[r * T + cc];

@@ -6,20 +6,32 @@
 // products) are both "C[r][c] = sum_k A[r][k] B[c][k]" over lists of
 // 128 x 128 output tiles with per-tile K ranges.  Each operand is stored
 // pre-split, x = hi + lo with hi = tf32(x); the tensor core accumulates
-//     C = A_hi B_hi + A_hi B_lo + A_lo B_hi
-// in fp32 (TMEM), dropping only A_lo B_lo (relative size 2^-22), which keeps
-// the products at fp32 accuracy.
+//     C = A_hi B_hi + (A_hi B_lo + A_lo B_hi)
+// dropping only A_lo B_lo (relative size 2^-22).
 //
-// One CTA (4 warps) per work item:
+// Accuracy of the accumulation.  Inside one MMA chain the tensor core keeps
+// the fp32 accumulator with truncating additions, so a chain of thousands
+// of MMAs drifts far beyond fp32 rounding.  The chain is therefore cut after
+// every 128-wide K tile: each K tile accumulates into a fresh TMEM buffer
+// (the main A_hi B_hi products and the small correction products in separate
+// buffers), and the epilogue warps add the finished buffer into fp32
+// registers with round-to-nearest additions while the tensor core fills the
+// other buffer of the pair.  The low parts this kernel writes for its own
+// consumers are rounded to tf32 (round to nearest), so the tensor core reads
+// them exactly.
+//
+// One CTA (8 warps) per work item:
 //   warp 0, one thread: TMA producer, 3-stage ring of 32-wide K slices, each
 //     stage holding A_hi, A_lo, B_hi, B_lo as 128 x 32 fp32 tiles with the
 //     128-byte swizzle (64 KiB per stage);
 //   warp 1, one thread: issues tcgen05.mma (M = N = 128, K = 8 per
-//     instruction, 3 per K step) and commits each stage back to the producer;
-//   warp 2: allocates / frees the 128 TMEM columns of the accumulator;
-//   all 4 warps: epilogue, TMEM -> registers (warp w owns lanes 32w..32w+31,
-//     i.e. output rows) -> global: stage 1 writes C split into (hi, lo),
-//     stage 2 subtracts C from W~.
+//     instruction, 3 per K step) and commits each stage back to the producer
+//     and each finished K tile to the epilogue;
+//   warp 2: allocates / frees the 512 TMEM columns (main and correction
+//     accumulators, two of each);
+//   warps 4-7: epilogue, TMEM -> registers (warp 4 + q owns TMEM lanes
+//     32q..32q+31, i.e. output rows) -> running fp32 sums -> global: stage 1
+//     writes C split into (hi, lo), stage 2 subtracts C from W~.
 // Every mbarrier wait is bounded (clock64 budget); on expiry the CTA records
 // BAKRON_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs (with a
 // bound again), frees TMEM and returns.
@@ -37,7 +49,9 @@ constexpr int STAGES = 3;
 constexpr uint32_t TILE_BYTES = BM * BKF * 4;    // 16 KiB
 constexpr uint32_t STAGE_BYTES = 4 * TILE_BYTES; // A_hi, A_lo, B_hi, B_lo
 constexpr size_t kSmem = (size_t)STAGES * STAGE_BYTES + 1024;
-constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t TMEM_COLS = 512;             // main[2] at 0, 128; corr[2] at 256, 384
+constexpr int SPC = kTile / BKF;                 // K slices per accumulation chunk
+constexpr int NTHREADS = 256;
 constexpr long long kBudget = 400000000LL;       // ~0.2 s of SM clock per wait
 
 // instruction descriptor, kind::tf32: D fp32, A/B tf32, both K-major, M=N=128
@@ -126,18 +140,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 }  // namespace
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     prop_tc_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
                    const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
                    PropArgs p, DevStatus* st) {
   extern __shared__ __align__(1024) unsigned char dsm[];
-  __shared__ __align__(8) unsigned long long bar_full[STAGES], bar_empty[STAGES], bar_done;
+  __shared__ __align__(8) unsigned long long bar_full[STAGES], bar_empty[STAGES];
+  __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2], bar_done;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[blockIdx.x];
-  const int nk = (it.k1 - it.k0) * (kTile / BKF);
+  const int nk = (it.k1 - it.k0) * SPC;     // K slices
+  const int nc = it.k1 - it.k0;             // accumulation chunks (K tiles)
   // 1024-byte aligned stage ring
   const uint32_t base_raw = smem_u32(dsm);
   const uint32_t sbase = (base_raw + 1023u) & ~1023u;
@@ -147,6 +163,10 @@ __global__ void __launch_bounds__(128, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
       mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);   // one arrival per epilogue warp
     }
     mbar_init(smem_u32(&bar_done), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -199,6 +219,14 @@ __global__ void __launch_bounds__(128, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     for (int i = 0; i < nk; ++i) {
+      const int c = i / SPC, b = c & 1;
+      const bool first = (i % SPC) == 0;
+      if (first && c >= 2 &&
+          !mbar_wait(smem_u32(&acc_empty[b]), (uint32_t)((c / 2 - 1) & 1), abortp)) {
+        set_status(st, BAKRON_ERR_TIMEOUT);
+        *abortp = 1;
+        break;
+      }
       const int s = i % STAGES;
       const uint32_t u = (uint32_t)(i / STAGES);
       if (!mbar_wait(smem_u32(&bar_full[s]), u & 1u, abortp)) {
@@ -210,76 +238,106 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t sd = sbase + (uint32_t)s * STAGE_BYTES;
       const uint64_t ahi = desc_sw128(sd), alo = desc_sw128(sd + TILE_BYTES);
       const uint64_t bhi = desc_sw128(sd + 2 * TILE_BYTES), blo = desc_sw128(sd + 3 * TILE_BYTES);
+      const uint32_t tm_main = tmem + (uint32_t)(b * 128);
+      const uint32_t tm_corr = tmem + 256u + (uint32_t)(b * 128);
 #pragma unroll
       for (int j = 0; j < BKF / 8; ++j) {
         const uint64_t o = (uint64_t)(j * 32 >> 4);  // 8 tf32 = 32 bytes along K
-        mma_tf32(tmem, ahi + o, bhi + o, (i > 0 || j > 0) ? 1u : 0u);
-        mma_tf32(tmem, ahi + o, blo + o, 1u);
-        mma_tf32(tmem, alo + o, bhi + o, 1u);
+        const uint32_t acc = (first && j == 0) ? 0u : 1u;
+        mma_tf32(tm_main, ahi + o, bhi + o, acc);
+        mma_tf32(tm_corr, ahi + o, blo + o, acc);
+        mma_tf32(tm_corr, alo + o, bhi + o, 1u);
       }
       mma_commit(smem_u32(&bar_empty[s]));
+      if ((i % SPC) == SPC - 1) mma_commit(smem_u32(&acc_full[b]));
     }
     mma_commit(smem_u32(&bar_done));
-  }
-  __syncwarp();
-
-  // ---------------- epilogue (all 4 warps)
-  bool ok = true;
-  {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(smem_u32(&bar_done), 0u)) {
-      if (clock64() - t0 > kBudget) { ok = false; break; }
+  } else if (warp >= 4) {
+    // ---------------- epilogue: running fp32 sums of the K-tile chunks
+    const int q = warp - 4;                 // TMEM lane quarter (warp % 4)
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    float acc[BN];
+#pragma unroll
+    for (int t = 0; t < BN; ++t) acc[t] = 0.f;
+    bool ok = true;
+    for (int c = 0; c < nc && ok; ++c) {
+      const int b = c & 1;
+      ok = mbar_wait(smem_u32(&acc_full[b]), (uint32_t)((c / 2) & 1), abortp);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      fence_after_sync();
+#pragma unroll
+      for (int g = 0; g < BN / 32; ++g) {
+        float v[32];
+        tmem_ld32(tmem + lane_off + (uint32_t)(b * 128 + g * 32), v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[g * 32 + t] += v[t];
+        tmem_ld32(tmem + lane_off + 256u + (uint32_t)(b * 128 + g * 32), v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[g * 32 + t] += v[t];
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&acc_empty[b]))
+                                  : "memory");
     }
-  }
-  if (!ok) set_status(st, BAKRON_ERR_TIMEOUT);
-  fence_after_sync();
-  ok = ok && (*abortp == 0);
-  ok = __all_sync(0xffffffffu, ok);
-  if (ok) {
-    const int row = warp * 32 + lane;
-#pragma unroll 1
-    for (int ch = 0; ch < BN / 32; ++ch) {
-      float v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ch * 32), v);
+    if (!ok) {
+      set_status(st, BAKRON_ERR_TIMEOUT);
+      *abortp = 1;
+    }
+    if (ok) {
+      const int row = q * 32 + lane;
       if (p.stage == 1) {
         if (p.alpha != 0.f && p.alpha != 1.f) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] *= p.alpha;
+          for (int t = 0; t < BN; ++t) acc[t] *= p.alpha;
         }
         if (p.tr_hi) {
           // transposed split store: lane = output row, so for each column the
           // 32 lanes of a warp write 32 consecutive floats
           const int64_t tcol = (int64_t)it.r * BM + row;
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int64_t trow = (int64_t)it.c * BN + ch * 32 + q;
-            const float h = tf32_round(v[q]);
+          for (int t = 0; t < BN; ++t) {
+            const int64_t trow = (int64_t)it.c * BN + t;
+            const float h = tf32_round(acc[t]);
             p.tr_hi[trow * p.ldt + tcol] = h;
-            p.tr_lo[trow * p.ldt + tcol] = v[q] - h;
+            p.tr_lo[trow * p.ldt + tcol] = tf32_round(acc[t] - h);
           }
         }
-        float* oh = p.out_hi + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN + ch * 32;
-        float* ol = p.out_lo + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN + ch * 32;
+        float* oh = p.out_hi + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN;
+        float* ol = p.out_lo + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int t = 0; t < BN / 4; ++t) {
           float4 h, l;
-          h.x = tf32_round(v[4 * q + 0]); l.x = v[4 * q + 0] - h.x;
-          h.y = tf32_round(v[4 * q + 1]); l.y = v[4 * q + 1] - h.y;
-          h.z = tf32_round(v[4 * q + 2]); l.z = v[4 * q + 2] - h.z;
-          h.w = tf32_round(v[4 * q + 3]); l.w = v[4 * q + 3] - h.w;
-          reinterpret_cast<float4*>(oh)[q] = h;
-          reinterpret_cast<float4*>(ol)[q] = l;
+          h.x = tf32_round(acc[4 * t + 0]); l.x = tf32_round(acc[4 * t + 0] - h.x);
+          h.y = tf32_round(acc[4 * t + 1]); l.y = tf32_round(acc[4 * t + 1] - h.y);
+          h.z = tf32_round(acc[4 * t + 2]); l.z = tf32_round(acc[4 * t + 2] - h.z);
+          h.w = tf32_round(acc[4 * t + 3]); l.w = tf32_round(acc[4 * t + 3] - h.w);
+          reinterpret_cast<float4*>(oh)[t] = h;
+          reinterpret_cast<float4*>(ol)[t] = l;
         }
       } else {
         // atomic: propagations of different recursion depths may update the
         // same tile concurrently (they run on different streams)
         float4* w = reinterpret_cast<float4*>(p.wt + ((int64_t)it.r * BM + row) * p.ldw +
-                                              (int64_t)it.c * BN + ch * 32);
+                                              (int64_t)it.c * BN);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          atomicAdd(w + q, make_float4(-v[4 * q + 0], -v[4 * q + 1], -v[4 * q + 2], -v[4 * q + 3]));
+        for (int t = 0; t < BN / 4; ++t)
+          atomicAdd(w + t, make_float4(-acc[4 * t + 0], -acc[4 * t + 1], -acc[4 * t + 2],
+                                       -acc[4 * t + 3]));
       }
     }
+  }
+  __syncwarp();
+
+  // all MMAs must have completed before TMEM is freed (bounded wait)
+  if (warp == 2) {
+    const long long t0 = clock64();
+    bool done = true;
+    while (!mbar_try_wait(smem_u32(&bar_done), 0u)) {
+      if (clock64() - t0 > kBudget) { done = false; break; }
+    }
+    if (!__all_sync(0xffffffffu, done) && lane == 0) set_status(st, BAKRON_ERR_TIMEOUT);
   }
   fence_before_sync();
   __syncthreads();
@@ -352,7 +410,7 @@ cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s) {
       !make_map(&bhi, p.B_hi, p.b_rows, p.ldb) || !make_map(&blo, p.B_lo, p.b_rows, p.ldb))
     return cudaErrorInvalidValue;
   count_launch();
-  prop_tc_kernel<<<p.n_items, 128, kSmem, s>>>(ahi, alo, bhi, blo, p, p.st);
+  prop_tc_kernel<<<p.n_items, NTHREADS, kSmem, s>>>(ahi, alo, bhi, blo, p, p.st);
   return cudaGetLastError();
 }
 

@@ -84,7 +84,7 @@ def check_parity(W, UA32, UB32, s32, qmin, qmax, V, codes, pre=None, variant="an
     return out
 
 
-def corner_check(W, UA32, UB32, s32, qmin, qmax, codes, a, b):
+def corner_check(W, UA32, UB32, s32, qmin, qmax, codes, a, b, variant="antidiag"):
     """Exact oracle on the top-left a x b corner: its GPTQ output depends only
     on W[:a, :b] and the leading blocks of the factors (updates only move to
     the bottom-right), so it must match the full-size GPU result there."""
@@ -92,7 +92,8 @@ def corner_check(W, UA32, UB32, s32, qmin, qmax, codes, a, b):
     Wc = W[:a, :b]
     UA = UA32[:b, :b].astype(np.float64)
     UB = UB32[:a, :a].astype(np.float64)
-    g = O.antidiag(Wc, UA, UB, s32[:a], *oq, guide=codes[:a, :b], guide_tol=TOL)
+    solve = {"antidiag": O.antidiag, "bakron": O.bakron}[variant]
+    g = solve(Wc, UA, UB, s32[:a], *oq, guide=codes[:a, :b], guide_tol=TOL)
     diff = int(np.count_nonzero(g.codes != codes[:a, :b]))
     assert diff == 0, "corner %dx%d: %d codes differ from the guided oracle" % (a, b, diff)
     assert g.overrides <= MAX_FRAC * a * b
