@@ -18,6 +18,14 @@
 // Both stages are dense 128-tile products (the triangular diagonal blocks of
 // the factors carry their zeros), listed as work items built here once per
 // (M, N) and uploaded into the workspace.
+//
+// Lookahead: both stages are split by the target tile anti-diagonal they
+// serve into chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...  The first
+// chunk is what the very next leaf needs and runs on the critical stream;
+// the others run on a side stream while the next leaves proceed, and every
+// leaf waits for the chunks covering its diagonal.  A stage-1 item Y^T[J',I]
+// is first read by targets on diagonal max(Dm, I + J'), so it belongs to the
+// chunk holding that diagonal.
 #include <algorithm>
 #include <climits>
 #include <cstring>
@@ -36,18 +44,17 @@ constexpr int T = kTile;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Chunk {
+  int off1, n1, maxk1;  // stage-1 items
   int off, n, maxk;     // stage-2 items
   int dlo, dhi;         // target tile anti-diagonals [dlo, dhi)
-  double flops;
+  double flops1, flops;
 };
 
 struct Op {
   int kind;                // 0 = leaf, 1 = propagation
   int D, I0, ntiles;       // leaf
-  int off1, n1, maxk1;     // propagation stage 1
   int depth;               // recursion depth (selects the Y buffer and side stream)
-  int chunk0, nchunks;     // stage-2 chunks (first one is urgent)
-  double flops1;
+  int chunk0, nchunks;     // chunks (the first one is urgent)
 };
 
 struct Schedule {
@@ -64,19 +71,29 @@ void sort_items(std::vector<WorkItem>& v, size_t from) {
   });
 }
 
-// Stage 2 of a propagation into band [Dm, D1) is split by target tile
-// anti-diagonal into chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...: the
-// first is needed by the very next leaf, the others only later, so they run
-// on a side stream while the next leaves proceed.
 void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
   const int M = s.M, N = s.N;
   Op op{};
   op.kind = 1;
   op.depth = depth;
   s.max_depth = std::max(s.max_depth, depth);
-  op.off1 = (int)s.items.size();
-  double f1 = 0;
-  int mk1 = 0;
+  op.chunk0 = (int)s.chunks.size();
+  // chunk boundaries over the target band [Dm, D1)
+  std::vector<std::pair<int, int>> bounds;
+  for (int lo = Dm, width = 1; lo < D1;) {
+    const int hi = std::min(D1, lo + width);
+    bounds.emplace_back(lo, hi);
+    lo = hi;
+    if (lo > Dm + 1) width *= 2;
+  }
+  auto chunk_of = [&](int d) {
+    int c = 0;
+    while (bounds[c].second <= d) ++c;
+    return c;
+  };
+  // stage 1 items, bucketed by the first target diagonal that reads them
+  std::vector<std::vector<WorkItem>> s1(bounds.size());
+  std::vector<double> f1(bounds.size(), 0.0);
   for (int I = 0; I < M; ++I) {
     const int jlo = std::max(D0 - I, 0), jhi = std::min(Dm - I, N);
     if (jlo >= jhi) continue;
@@ -84,25 +101,26 @@ void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
       const int lo = std::max(I, Dm - Jp), hi = std::min(M - 1, D1 - 1 - Jp);
       if (lo > hi) continue;  // no tile of Q in column Jp at or below row I
       const int k1 = std::min(jhi, Jp + 1);
-      s.items.push_back(WorkItem{Jp, I, jlo, k1});
-      f1 += 2.0 * T * T * T * (k1 - jlo);
-      mk1 = std::max(mk1, k1 - jlo);
+      const int c = chunk_of(std::max(Dm, I + Jp));
+      s1[c].push_back(WorkItem{Jp, I, jlo, k1});
+      f1[c] += 2.0 * T * T * T * (k1 - jlo);
     }
   }
-  sort_items(s.items, op.off1);
-  op.n1 = (int)s.items.size() - op.off1;
-  op.flops1 = f1;
-  op.maxk1 = mk1;
-  op.chunk0 = (int)s.chunks.size();
-  int lo = Dm, width = 1;
-  while (lo < D1) {
-    const int hi = std::min(D1, lo + width);
+  for (size_t ci = 0; ci < bounds.size(); ++ci) {
     Chunk c{};
+    c.dlo = bounds[ci].first;
+    c.dhi = bounds[ci].second;
+    c.off1 = (int)s.items.size();
+    for (const WorkItem& w : s1[ci]) {
+      s.items.push_back(w);
+      c.maxk1 = std::max(c.maxk1, w.k1 - w.k0);
+    }
+    sort_items(s.items, c.off1);
+    c.n1 = (int)s.items.size() - c.off1;
+    c.flops1 = f1[ci];
     c.off = (int)s.items.size();
-    c.dlo = lo;
-    c.dhi = hi;
     for (int Ip = 0; Ip < M; ++Ip) {
-      for (int Jp = std::max(lo - Ip, 0); Jp < std::min(hi - Ip, N); ++Jp) {
+      for (int Jp = std::max(c.dlo - Ip, 0); Jp < std::min(c.dhi - Ip, N); ++Jp) {
         const int ilo = std::max(std::max(0, D0 - Jp), D0 - N + 1);
         const int ihi = std::min(Ip, Dm - 1);
         if (ilo > ihi) continue;
@@ -114,8 +132,6 @@ void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
     sort_items(s.items, c.off);
     c.n = (int)s.items.size() - c.off;
     s.chunks.push_back(c);
-    lo = hi;
-    if (lo > Dm + 1) width *= 2;
   }
   op.nchunks = (int)s.chunks.size() - op.chunk0;
   s.ops.push_back(op);
@@ -579,38 +595,41 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
     p1.out_hi = yhi; p1.out_lo = ylo; p1.ldo = L.Mp;
     p1.stage = 1;
     p1.st = st;
-    p1.items = items + op.off1; p1.n_items = op.n1; p1.max_k = op.maxk1;
     PropArgs p2{};
     p2.A_hi = lbthi; p2.A_lo = lbtlo; p2.lda = L.Mp; p2.a_rows = L.Mp;
     p2.B_hi = yhi; p2.B_lo = ylo; p2.ldb = L.Mp; p2.b_rows = L.Np;
     p2.wt = wt; p2.ldw = L.Np;
     p2.stage = 2;
     p2.st = st;
-    {
-      cudaEvent_t ev = pt.begin();
-      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p1, cs) : launch_prop_simt(p1, cs));
-      pt.end(1, ev);
-    }
+    auto launch = [&](PropArgs& pa, int off, int nit, int maxk, cudaStream_t str) {
+      pa.items = items + off; pa.n_items = nit; pa.max_k = maxk;
+      return o.use_3xtf32 ? launch_prop_tc(pa, str) : launch_prop_simt(pa, str);
+    };
     cudaEvent_t ev_s1 = nullptr;
-    if (op.nchunks > 1) {
-      TRY_CUDA(next_event(&ev_s1));
-      TRY_CUDA(cudaEventRecord(ev_s1, cs));
-    }
     for (int c = 0; c < op.nchunks; ++c) {
       const Chunk& ch = sch.chunks[op.chunk0 + c];
-      if (o.times) o.times->prop_flops += ch.flops;
-      if (ch.n == 0) continue;
-      p2.items = items + ch.off; p2.n_items = ch.n; p2.max_k = ch.maxk;
-      cudaStream_t cstr = c == 0 ? cs : ss->side[op.depth];
-      if (c > 0) TRY_CUDA(cudaStreamWaitEvent(cstr, ev_s1, 0));
-      PhaseTimer* tm = &pt;
+      if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
+      const bool urgent = c == 0;
+      cudaStream_t cstr = urgent ? cs : ss->side[op.depth];
+      if (c == 1) TRY_CUDA(cudaStreamWaitEvent(cstr, ev_s1, 0));
       PhaseTimer side_pt(o.times, cstr);
-      if (c > 0) tm = &side_pt;
-      cudaEvent_t ev = tm->begin();
-      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p2, cstr) : launch_prop_simt(p2, cstr));
-      tm->end(2, ev);
-      if (c > 0) {
-        side_pt.s = cstr;
+      PhaseTimer* tm = urgent ? &pt : &side_pt;
+      if (ch.n1 > 0) {
+        cudaEvent_t ev = tm->begin();
+        TRY_CUDA(launch(p1, ch.off1, ch.n1, ch.maxk1, cstr));
+        tm->end(1, ev);
+      }
+      if (urgent && op.nchunks > 1) {
+        // the deferred chunks read the urgent stage-1 tiles too
+        TRY_CUDA(next_event(&ev_s1));
+        TRY_CUDA(cudaEventRecord(ev_s1, cs));
+      }
+      if (ch.n > 0) {
+        cudaEvent_t ev = tm->begin();
+        TRY_CUDA(launch(p2, ch.off, ch.n, ch.maxk, cstr));
+        tm->end(2, ev);
+      }
+      if (!urgent) {
         pt.adopt(side_pt);
         cudaEvent_t done;
         TRY_CUDA(next_event(&done));
@@ -618,7 +637,6 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
         for (int d = ch.dlo; d < ch.dhi; ++d) waits[d].push_back(done);
       }
     }
-    if (o.times) o.times->prop_flops += op.flops1;
   }
   // join back onto the caller's stream (every deferred chunk was waited for
   // by the leaf of its diagonals, so the critical stream is last)

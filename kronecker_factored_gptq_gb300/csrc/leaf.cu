@@ -234,12 +234,16 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
 #pragma unroll
       for (int c = 0; c < S / 4; ++c) {
         const float4 v = *reinterpret_cast<const float4*>(Ubd + row * PU + 4 * c);
-        ub[4 * c + 0] = (4 * c + 0 < row) ? v.x : 0.f;
-        ub[4 * c + 1] = (4 * c + 1 < row) ? v.y : 0.f;
-        ub[4 * c + 2] = (4 * c + 2 < row) ? v.z : 0.f;
-        ub[4 * c + 3] = (4 * c + 3 < row) ? v.w : 0.f;
+        ub[4 * c + 0] = (4 * c + 0 < row - 1) ? v.x : 0.f;
+        ub[4 * c + 1] = (4 * c + 1 < row - 1) ? v.y : 0.f;
+        ub[4 * c + 2] = (4 * c + 2 < row - 1) ? v.z : 0.f;
+        ub[4 * c + 3] = (4 * c + 3 < row - 1) ? v.w : 0.f;
       }
-      ub[S - 1] = 0.f;   // a' < a <= 31
+      ub[S - 1] = 0.f;   // a' < a - 1 <= 30
+      // Ub(a-1, a): the row directly above, whose accumulator completes one
+      // step before this row needs it, is kept out of the look-ahead sum
+      const float ub1 = row > 0 ? Ubd[row * PU + row - 1] : 0.f;
+      const int rowm1 = row > 0 ? row - 1 : 0;
       const float ubaa = Ubd[row * PU + row];
       const float lB = 1.f / ubaa;
       const int64_t gi = i0 + S * I + row;
@@ -255,6 +259,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       float FR[NF];
 #pragma unroll
       for (int j = 0; j < NF; ++j) FR[j] = 0.f;
+      float pp = 0.f;   // column sum over rows a' < a - 1 for this step's column
 
       for (int kb = 0; kb * 4 < NSTEP; ++kb) {
 #pragma unroll
@@ -268,8 +273,13 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           const int bb = act ? b : 0;
           const float xin = Xrow[bb];
           const float la = lAj[bb];
-          // column sum over the rows above (ub = 0 for rows at or below)
-          const float* rc = rs + (act ? b : S) * PR;
+          // completed r(a-1, b) of the row above (previous step)
+          const float rprev = rs[(act ? b : S) * PR + rowm1];
+          // look-ahead: the column sum of the NEXT step (column b + 1) over
+          // rows a' < a - 1, all completed by the previous step; it is off
+          // this step's dependency chain
+          const int bn = b + 1;
+          const float* rc = rs + ((unsigned)bn < (unsigned)S ? bn : S) * PR;
           float p0 = 0.f, p1 = 0.f;
 #pragma unroll
           for (int c = 0; c < S / 4; ++c) {
@@ -281,10 +291,11 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           }
           // row b of the diagonal-major Ua, read before this step's stores
           const float4* dr = reinterpret_cast<const float4*>(Dj + bb * PD);
-          float4 dv[5];
+          float4 dv[4];
 #pragma unroll
-          for (int c = 0; c < 5; ++c) dv[c] = dr[c];
-          const float x = xin - (p0 + p1) - ubaa * FR[sg];
+          for (int c = 0; c < 4; ++c) dv[c] = dr[c];
+          const float x = xin - fmaf(ub1, rprev, pp) - ubaa * FR[sg];
+          pp = p0 + p1;
           // rounding decision on x * fl(1/s): within 2^-23 relative of x / s,
           // so it can differ from the correctly rounded quotient only within
           // 2e-5 grid units of a rounding boundary
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           // first with the values loaded before the stores, then the rest
 #pragma unroll
           for (int c = 0; c < PD / 4; ++c) {
-            const float4 v = c < 5 ? dv[c] : dr[c];
+            const float4 v = c < 4 ? dv[c] : dr[c];
             if (4 * c + 0 >= 1 && sg + 4 * c + 0 < NF) FR[sg + 4 * c + 0] = fmaf(e, v.x, FR[sg + 4 * c + 0]);
             if (4 * c + 1 >= 1 && sg + 4 * c + 1 < NF) FR[sg + 4 * c + 1] = fmaf(e, v.y, FR[sg + 4 * c + 1]);
             if (4 * c + 2 >= 1 && sg + 4 * c + 2 < NF) FR[sg + 4 * c + 2] = fmaf(e, v.z, FR[sg + 4 * c + 2]);
