@@ -52,6 +52,8 @@ constexpr size_t kSmem = (size_t)STAGES * STAGE_BYTES + 1024;
 constexpr uint32_t TMEM_COLS = 512;             // main[2] at 0, 128; corr[2] at 256, 384
 constexpr int SPC = kTile / BKF;                 // K slices per accumulation chunk
 constexpr int NTHREADS = 256;
+constexpr int SPITCH = BN + 4;                   // epilogue staging pitch (floats)
+static_assert(4 * 32 * SPITCH * 4 <= STAGES * STAGE_BYTES, "epilogue staging fits the ring");
 constexpr long long kBudget = 400000000LL;       // ~0.2 s of SM clock per wait
 
 // instruction descriptor, kind::tf32: D fp32, A/B tf32, both K-major, M=N=128
@@ -304,27 +306,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             p.tr_lo[trow * p.ldt + tcol] = tf32_round(acc[t] - h);
           }
         }
-        float* oh = p.out_hi + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN;
-        float* ol = p.out_lo + ((int64_t)it.r * BM + row) * p.ldo + (int64_t)it.c * BN;
+      }
+      // Coalesced write-out: each warp stages its 32 rows in the (now idle)
+      // TMA ring, then writes whole 512-byte rows, so a store or atomic
+      // instruction covers four 128-byte lines instead of 32 rows.  Every
+      // MMA has completed (the last accumulator chunk was consumed), so no
+      // copy or MMA touches the ring any more.
+      float* stg = reinterpret_cast<float*>(dsm + (sbase - base_raw)) + q * 32 * SPITCH;
 #pragma unroll
-        for (int t = 0; t < BN / 4; ++t) {
+      for (int t = 0; t < BN / 4; ++t)
+        *reinterpret_cast<float4*>(stg + lane * SPITCH + 4 * t) =
+            make_float4(acc[4 * t + 0], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+      __syncwarp();
+      const int64_t grow0 = (int64_t)it.r * BM + q * 32;
+      const int64_t gcol = (int64_t)it.c * BN + 4 * lane;
+      if (p.stage == 1) {
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * SPITCH + 4 * lane);
           float4 h, l;
-          h.x = tf32_round(acc[4 * t + 0]); l.x = tf32_round(acc[4 * t + 0] - h.x);
-          h.y = tf32_round(acc[4 * t + 1]); l.y = tf32_round(acc[4 * t + 1] - h.y);
-          h.z = tf32_round(acc[4 * t + 2]); l.z = tf32_round(acc[4 * t + 2] - h.z);
-          h.w = tf32_round(acc[4 * t + 3]); l.w = tf32_round(acc[4 * t + 3] - h.w);
-          reinterpret_cast<float4*>(oh)[t] = h;
-          reinterpret_cast<float4*>(ol)[t] = l;
+          h.x = tf32_round(v.x); l.x = tf32_round(v.x - h.x);
+          h.y = tf32_round(v.y); l.y = tf32_round(v.y - h.y);
+          h.z = tf32_round(v.z); l.z = tf32_round(v.z - h.z);
+          h.w = tf32_round(v.w); l.w = tf32_round(v.w - h.w);
+          *reinterpret_cast<float4*>(p.out_hi + (grow0 + rr) * p.ldo + gcol) = h;
+          *reinterpret_cast<float4*>(p.out_lo + (grow0 + rr) * p.ldo + gcol) = l;
         }
       } else {
         // atomic: propagations of different recursion depths may update the
         // same tile concurrently (they run on different streams)
-        float4* w = reinterpret_cast<float4*>(p.wt + ((int64_t)it.r * BM + row) * p.ldw +
-                                              (int64_t)it.c * BN);
-#pragma unroll
-        for (int t = 0; t < BN / 4; ++t)
-          atomicAdd(w + t, make_float4(-acc[4 * t + 0], -acc[4 * t + 1], -acc[4 * t + 2],
-                                       -acc[4 * t + 3]));
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * SPITCH + 4 * lane);
+          atomicAdd(reinterpret_cast<float4*>(p.wt + (grow0 + rr) * p.ldw + gcol),
+                    make_float4(-v.x, -v.y, -v.z, -v.w));
+        }
       }
     }
   }
