@@ -256,26 +256,49 @@ PLayout prepare_layout(int64_t n, int64_t m) {
 
 // A second stream (and fork/join events) per device, created once, on which
 // the B factor is prepared while A runs on the caller's stream.
-struct AuxStream {
-  cudaStream_t s = nullptr;
+// Streams of the factor preparation, per device, created once: the second
+// factor's main stream and one lookahead stream per factor, plus a pool of
+// reusable events.  Held under a lock for the whole (synchronous) call.
+struct PrepStreams {
+  cudaStream_t main[2] = {};       // high priority: the diagonal-block chains
+  cudaStream_t side[2] = {};       // low priority: lookahead panels and updates
   cudaEvent_t fork = nullptr, join = nullptr;
+  std::vector<cudaEvent_t> events;
+  std::mutex mu;
 };
 
-cudaError_t aux_stream(AuxStream** out) {
+cudaError_t prep_streams(PrepStreams** out) {
   static std::mutex mu;
-  static AuxStream per_dev[64];
+  static PrepStreams per_dev[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(mu);
-  AuxStream& a = per_dev[dev];
-  if (!a.s) {
-    if ((e = cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  PrepStreams& a = per_dev[dev];
+  if (!a.main[0]) {
+    int lo = 0, hi = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+    for (int w = 0; w < 2; ++w) {
+      if ((e = cudaStreamCreateWithPriority(&a.main[w], cudaStreamNonBlocking, hi)) != cudaSuccess)
+        return e;
+      if ((e = cudaStreamCreateWithPriority(&a.side[w], cudaStreamNonBlocking, lo)) != cudaSuccess)
+        return e;
+    }
     if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming)) != cudaSuccess) return e;
   }
   *out = &a;
+  return cudaSuccess;
+}
+
+cudaError_t prep_events(PrepStreams* ps, size_t n) {
+  while (ps->events.size() < n) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (r != cudaSuccess) return r;
+    ps->events.push_back(e);
+  }
   return cudaSuccess;
 }
 
@@ -464,16 +487,22 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   DevStatus* st = (DevStatus*)(base + L.status);
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
   TRY_CUDA(cudaMemsetAsync(st->info, 0x7f, sizeof(st->info), s));
-  AuxStream* aux = nullptr;
-  if (B) {
-    TRY_CUDA(aux_stream(&aux));
-    TRY_CUDA(cudaEventRecord(aux->fork, s));
-    TRY_CUDA(cudaStreamWaitEvent(aux->s, aux->fork, 0));
-  }
+  PrepStreams* ps = nullptr;
+  TRY_CUDA(prep_streams(&ps));
+  std::lock_guard<std::mutex> plk(ps->mu);
+  const size_t ev_per = 3 * (size_t)(std::max(L.kp[0], L.kp[1]) / T + 1);
+  TRY_CUDA(prep_events(ps, 2 * ev_per));
+  TRY_CUDA(cudaEventRecord(ps->fork, s));
   for (int which = 0; which < 2; ++which) {
     const float* X = which == 0 ? A : B;
     const int64_t k = which == 0 ? n : m;
     if (!X || k == 0) continue;
+    cudaStream_t fs = ps->main[which];
+    TRY_CUDA(cudaStreamWaitEvent(fs, ps->fork, 0));
+    // the lookahead stream starts after the factor's stream reaches this point
+    cudaEvent_t start = ps->events[which * ev_per + ev_per - 1];
+    TRY_CUDA(cudaEventRecord(start, fs));
+    TRY_CUDA(cudaStreamWaitEvent(ps->side[which], start, 0));
     PrepareFactorArgs pa{};
     pa.X = X; pa.k = k; pa.damp = which == 0 ? damp_A : damp_B;
     pa.U = which == 0 ? UA : UB;
@@ -492,11 +521,13 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
     pa.kp = L.kp[which];
     pa.which = which;
     pa.st = st;
-    TRY_CUDA(run_prepare_factor(pa, which == 0 ? s : aux->s));
-  }
-  if (aux) {
-    TRY_CUDA(cudaEventRecord(aux->join, aux->s));
-    TRY_CUDA(cudaStreamWaitEvent(s, aux->join, 0));
+    pa.side = ps->side[which];
+    pa.ev = ps->events.data() + which * ev_per;
+    TRY_CUDA(run_prepare_factor(pa, fs));
+    // join the factor's chain back onto the caller's stream
+    cudaEvent_t done = ps->events[which * ev_per + ev_per - 2];
+    TRY_CUDA(cudaEventRecord(done, fs));
+    TRY_CUDA(cudaStreamWaitEvent(s, done, 0));
   }
   DevStatus h{};
   bakron_status r = finish(s, st, &h);

@@ -458,36 +458,73 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   count_launch();
   flip_damp_kernel<<<grid_for(kp * kp), 256, 0, s>>>(a.X, k, a.scal, a.C, kp);
   BK_TRY(cudaGetLastError());
-  float* inv_plain = a.Tlo;   // 128 x 128 scratch during the Cholesky sweep
+  // Right-looking blocked Cholesky with one block column of lookahead.  On
+  // the factor's stream: the diagonal block kb, then the part of step kb
+  // that block kb+1 needs (panel row block kb+1, its split, and the update
+  // of tile (kb+1, kb+1)).  On the side stream: the rest of the panel and of
+  // the trailing update.  Step kb's urgent part waits for the side work of
+  // step kb-1 (it updated the column kb tiles).  Each factor uses three
+  // events per block column.  The 128 x 128 inverse of the diagonal block
+  // alternates between two scratch buffers, because the side stream may
+  // still be reading block kb's while block kb+1 is factored.
+  float* invbuf[2] = {a.Tlo, a.Tlo + NB * NB};
+  const PrepItems& PI = P;
+  bool side_used = false;
   for (int64_t kb = 0; kb < nblk; ++kb) {
+    float* inv_plain = invbuf[kb & 1];
     count_launch();
     potrf_block_kernel<<<1, 512, kPotrfSmem, s>>>(a.C, a.Gihi, a.Gilo, a.GiThi, a.GiTlo, inv_plain,
                                                   kp, kb, k, a.st, a.which);
     BK_TRY(cudaGetLastError());
     const int64_t rest = kp - (kb + 1) * NB;
     if (rest <= 0) break;
+    cudaEvent_t ev_pot = a.ev[3 * kb], ev_urg = a.ev[3 * kb + 1], ev_def = a.ev[3 * kb + 2];
+    BK_TRY(cudaEventRecord(ev_pot, s));
+    if (kb >= 1) BK_TRY(cudaStreamWaitEvent(s, a.ev[3 * (kb - 1) + 2], 0));
     float* panel = a.C + (kb + 1) * NB * kp + kb * NB;
-    // P = panel * inv(G_kk)^T  (rest x 128, ld = NB) in Thi
-    GemmArgs g{};
-    g.A = panel; g.lda = kp;
-    g.B = inv_plain; g.ldb = NB; g.transB = 1;
-    g.C = a.Thi; g.ldc = NB;
-    g.M = rest; g.N = NB; g.K = NB; g.alpha = 1.f; g.beta = 0.f;
-    BK_TRY(gemm(g, 1, s));
     const int64_t off = (kb + 1) * NB * kp + kb * NB;
-    count_launch();
-    copy_split_kernel<<<grid_for(rest * NB), 256, 0, s>>>(a.Thi, NB, a.C + off, a.Chi + off, a.Clo + off,
-                                                          kp, rest, NB);
-    BK_TRY(cudaGetLastError());
-    // trailing: C22 -= P P^T on the lower tiles (tensor cores)
-    PropArgs q{};
-    q.A_hi = a.Chi; q.A_lo = a.Clo; q.lda = kp; q.a_rows = kp;
-    q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
-    q.wt = a.C; q.ldw = kp;
-    q.items = a.items + P.syrk_off[kb]; q.n_items = P.syrk_n[kb]; q.max_k = 1;
-    q.stage = 2;
-    q.st = a.st;
-    BK_TRY(launch_prop_tc(q, s));
+    // P = panel * inv(G_kk)^T (rows x 128, ld = NB) in Thi; rows [r0, r0 + rows)
+    auto panel_rows = [&](int64_t r0, int64_t rows, cudaStream_t str) -> cudaError_t {
+      GemmArgs g{};
+      g.A = panel + r0 * kp; g.lda = kp;
+      g.B = inv_plain; g.ldb = NB; g.transB = 1;
+      g.C = a.Thi + r0 * NB; g.ldc = NB;
+      g.M = rows; g.N = NB; g.K = NB; g.alpha = 1.f; g.beta = 0.f;
+      BK_TRY(gemm(g, 1, str));
+      count_launch();
+      copy_split_kernel<<<grid_for(rows * NB), 256, 0, str>>>(
+          a.Thi + r0 * NB, NB, a.C + off + r0 * kp, a.Chi + off + r0 * kp, a.Clo + off + r0 * kp, kp,
+          rows, NB);
+      return cudaGetLastError();
+    };
+    // trailing update C22 -= P P^T over syrk items [i0, i0 + n) (tensor cores)
+    auto syrk = [&](int i0, int n, cudaStream_t str) -> cudaError_t {
+      if (n <= 0) return cudaSuccess;
+      PropArgs q{};
+      q.A_hi = a.Chi; q.A_lo = a.Clo; q.lda = kp; q.a_rows = kp;
+      q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
+      q.wt = a.C; q.ldw = kp;
+      q.items = a.items + i0; q.n_items = n; q.max_k = 1;
+      q.stage = 2;
+      q.st = a.st;
+      return launch_prop_tc(q, str);
+    };
+    // urgent: row block kb+1 and tile (kb+1, kb+1) (the first syrk item)
+    BK_TRY(panel_rows(0, NB, s));
+    BK_TRY(cudaEventRecord(ev_urg, s));
+    BK_TRY(syrk(PI.syrk_off[kb], 1, s));
+    // deferred: the other panel rows and trailing tiles
+    side_used = true;
+    BK_TRY(cudaStreamWaitEvent(a.side, ev_pot, 0));
+    if (rest > NB) BK_TRY(panel_rows(NB, rest - NB, a.side));
+    BK_TRY(cudaStreamWaitEvent(a.side, ev_urg, 0));
+    BK_TRY(syrk(PI.syrk_off[kb] + 1, PI.syrk_n[kb] - 1, a.side));
+    BK_TRY(cudaEventRecord(ev_def, a.side));
+  }
+  if (side_used) {
+    // the last deferred step joins the factor's stream before the inverse
+    const int64_t last = (nblk >= 2 ? nblk - 2 : 0);
+    BK_TRY(cudaStreamWaitEvent(s, a.ev[3 * last + 2], 0));
   }
   // G^{-1} by recursive doubling (tensor cores)
   for (size_t lvl = 0; lvl < P.t_off.size(); ++lvl) {
