@@ -385,11 +385,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    world, rank, local = dist_setup()
     if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; the other ranks exit at
+        # once, so no process group is needed
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
         run_reference(args, world, rank)
-    else:
-        run_ours(args, world, rank, local)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
