@@ -41,7 +41,8 @@ namespace {
 constexpr int T = kTile;          // 128
 constexpr int S = 32;             // block edge
 constexpr int NB = T / S;         // 4 blocks per tile edge
-constexpr int NTHR = 512;
+constexpr int NTHR = 384;
+constexpr int NPAIR = NTHR / 64;   // warp pairs for the block products
 constexpr int NF = S + 3;         // row-accumulator window: columns b0 .. b0 + 34, b0 >= -3 once active
 constexpr int PX = T + 4;         // tile pitch
 constexpr int PP = S + 1;         // P^T block pitch
@@ -78,7 +79,6 @@ __constant__ int kRow[20] = {0,  32, 64, 96,  32, 64, 96, 64, 96, 96,
                              0,  32, 64, 96,  32, 64, 96, 64, 96, 96};
 __constant__ int kCol[20] = {0,  32, 64, 96,  0,  0,  0,  32, 32, 64,
                              0,  0,  0,  0,   32, 32, 32, 64, 64, 96};
-static_assert(20 * S * S / 4 % NTHR == 0, "load items");
 
 // C(r, c) += sign * sum_k A(r, k) B(k, c) for one 32 x 32 block, 64 threads
 // (lt in [0, 64)), each a 4 x 4 tile: rows 4 tr .. 4 tr + 3, columns
@@ -163,11 +163,12 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   // before the first store.
   float* stage = Pt;
   {
-    constexpr int kIt = 20 * S * S / 4 / NTHR;   // 10 items per thread
+    constexpr int kItems = 20 * S * S / 4;
+    constexpr int kIt = (kItems + NTHR - 1) / NTHR;   // items per thread
     float4 hv[kIt], lv[kIt];
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
-      const int idx = tid + it * NTHR;
+      const int idx = min(tid + it * NTHR, kItems - 1);   // the tail repeats the last item
       const int blk = idx >> 8, w = idx & 255;
       const int r = w >> 3, q = (w & 7) * 4;
       const bool isA = blk < 10;
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
       const int idx = tid + it * NTHR;
+      if (idx >= kItems) break;
       const int blk = idx >> 8, w = idx & 255;
       const int r = w >> 3, q = (w & 7) * 4;
       float* dst = blk < 4 ? stage + blk * S * PU
@@ -280,22 +282,22 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           // this step's dependency chain
           const int bn = b + 1;
           const float* rc = rs + ((unsigned)bn < (unsigned)S ? bn : S) * PR;
-          float p0 = 0.f, p1 = 0.f;
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
           for (int c = 0; c < S / 4; ++c) {
             const float4 v = *reinterpret_cast<const float4*>(rc + 4 * c);
             p0 = fmaf(ub[4 * c + 0], v.x, p0);
             p1 = fmaf(ub[4 * c + 1], v.y, p1);
-            p0 = fmaf(ub[4 * c + 2], v.z, p0);
-            if (c < S / 4 - 1) p1 = fmaf(ub[4 * c + 3], v.w, p1);
+            p2 = fmaf(ub[4 * c + 2], v.z, p2);
+            if (c < S / 4 - 1) p3 = fmaf(ub[4 * c + 3], v.w, p3);
           }
           // row b of the diagonal-major Ua, read before this step's stores
           const float4* dr = reinterpret_cast<const float4*>(Dj + bb * PD);
-          float4 dv[4];
+          float4 dv[PD / 4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) dv[c] = dr[c];
+          for (int c = 0; c < PD / 4; ++c) dv[c] = dr[c];
           const float x = xin - fmaf(ub1, rprev, pp) - ubaa * FR[sg];
-          pp = p0 + p1;
+          pp = (p0 + p1) + (p2 + p3);
           // rounding decision on x * fl(1/s): within 2^-23 relative of x / s,
           // so it can differ from the correctly rounded quotient only within
           // 2e-5 grid units of a rounding boundary
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           // first with the values loaded before the stores, then the rest
 #pragma unroll
           for (int c = 0; c < PD / 4; ++c) {
-            const float4 v = c < 4 ? dv[c] : dr[c];
+            const float4 v = dv[c];
             if (4 * c + 0 >= 1 && sg + 4 * c + 0 < NF) FR[sg + 4 * c + 0] = fmaf(e, v.x, FR[sg + 4 * c + 0]);
             if (4 * c + 1 >= 1 && sg + 4 * c + 1 < NF) FR[sg + 4 * c + 1] = fmaf(e, v.y, FR[sg + 4 * c + 1]);
             if (4 * c + 2 >= 1 && sg + 4 * c + 2 < NF) FR[sg + 4 * c + 2] = fmaf(e, v.z, FR[sg + 4 * c + 2]);
@@ -370,11 +372,11 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       for (int I = Imin; I <= Imax; ++I) {
         const int J = k - I, slot = I - Imin;
         for (int J2 = J + 1; J2 < NB; ++J2, ++pidx)
-          if ((pidx & 7) == pair)
+          if (pidx % NPAIR == pair)
             block_product<false>(UaO + ua_idx(J, J2) * S * PU, X + (S * I) * PX + S * J, PX,
                                  Pt + p_idx(I, J2) * S * PP, PP, 1.f, lt);
         for (int I2 = I + 1; I2 < NB; ++I2, ++pidx)
-          if ((pidx & 7) == pair)
+          if (pidx % NPAIR == pair)
             block_product<false>(UbB + ub_idx(I, I2) * S * PU, rT + slot * RT_SLOT, PR,
                                  X + (S * I2) * PX + S * J, PX, -1.f, lt);
       }
