@@ -1,36 +1,43 @@
 // Leaf sweep: one tile anti-diagonal D of 128 x 128 tiles, one CTA per tile.
 //
-// A tile is solved as a 4 x 4 grid of 32 x 32 blocks, block anti-diagonal by
-// block anti-diagonal; inside a block the entries are rounded anti-diagonal
-// by anti-diagonal (the anti-diagonal variant of the summary page "FastKron:
-// Efficient Quantization with Kronecker-Factored Hessians", section 3), one
-// warp per block and one lane per block row, so a step needs no CTA barrier.
-// Any order that respects the entry partial order (an entry after every
-// entry to its top-left) gives the GPTQ result, and this one does.
+// A tile is solved as an NB x NB grid of S x S blocks (S = 16), block
+// anti-diagonal ("level") by level; inside a block the entries are rounded
+// anti-diagonal by anti-diagonal (the anti-diagonal variant of the summary
+// page "FastKron: Efficient Quantization with Kronecker-Factored Hessians",
+// section 3), one lane per block row and 32 / S blocks per warp, so a step
+// needs no CTA barrier.  Any order that respects the entry partial order (an
+// entry after every entry to its top-left) gives the GPTQ result, and this
+// one does.
 //
 // Notation (tile-local): Ua, Ub the diagonal 128-blocks of U_A, U_B; E the
 // scaled errors.  For blocks (I, J):
 //   P[I,J] = sum_{J'' < J} E[I,J''] Ua[J'',J]        (row accumulator, left part)
 //   R[I,J] = P[I,J] + E[I,J] Ua[J,J]                 (complete row accumulator)
 //   x0[I,J] = W~[I,J] - sum_{I' < I} Ub[I',I]^T R[I',J] - Ub[I,I]^T P[I,J]
-// where W~ already holds every update from earlier tile anti-diagonals and
-// Ub[I,I]^T P includes the diagonal.  x0 is what the block sweep starts from;
-// the sweep then applies the updates between entries of the block itself
-// with the same row-accumulator form at entry level:
+// where W~ already holds every update from earlier tile anti-diagonals.  x0
+// is what the block sweep starts from; the sweep applies the updates between
+// entries of the block itself in the same row-accumulator form:
 //   x(a,b) = x0(a,b) - sum_{a' < a} Ub(a',a) r(a',b) - Ub(a,a) r_part(a,b),
 //   r(a,b) = sum_{b' <= b} e(a,b') Ua(b',b),  r_part: the sum over b' < b.
-// Level k of the block sweep (blocks with I + J = k):
-//   A. x0 for its blocks: W~ -= Ub[I,I]^T P[I,J]  (triangular block product);
-//   B. block sweeps, 63 steps each, one warp per block;
-//   C. R = P + r; pushes to later blocks: P[I,J'] += E[I,J] Ua[J,J'] (J' > J)
-//      and W~[I',J] -= Ub[I,I']^T R[I,J] (I' > I).
-// Phases are separated by CTA barriers (21 per tile).
 //
-// Block sweep, lane a = block row: Ub(a', a) for a' < a lives in registers;
-// the completed r(a', b) of the rows above are read from shared memory
-// (rT[b][a'], 16-byte loads); the pending r(a, b'') of the lane's own row
-// live in a register window FR[j] = r(a, b0 + j), b0 = 4 kb - a, shifted by
-// four registers every four steps (the step loop is unrolled by four, so
+// Schedule, level k (blocks with I + J = k), two CTA barriers per level:
+//   B(k):   the sweep warps run the block sweeps of level k (then R = P + r,
+//           codes and V); four other warps meanwhile apply the pushes of
+//           level k-1 that later levels need but level k+1 does not:
+//           P[I,J'] += E[I,J] Ua[J,J'] for J' >= J + 2 and
+//           W~[I',J] -= Ub[I,I']^T R[I,J] for I' >= I + 2;
+//   prep(k+1): one warp per block (I,J) of level k+1 completes its x0 with
+//           the pushes from its two neighbours on level k, then
+//           W~[I,J] -= Ub[I,I]^T P[I,J] (triangular).
+// R of level k lives in one of two slot sets (level parity), because the
+// deferred pushes read it while level k+1 writes its own.
+//
+// Block sweep, lane = (block, row a): Ub(a', a) for a' < a lives in
+// registers; r(a-1, b), completed by the row above in the previous step,
+// arrives by a warp shuffle; the older r(a', b) of the rows above are read
+// from shared memory (rT[b][a'], 16-byte loads); the pending r(a, b'') of the lane's own
+// row live in a register window FR[j] = r(a, b0 + j), b0 = 4 kb - a, shifted
+// by four registers every four steps (the step loop is unrolled by four, so
 // every register index is static); the diagonal-major copy
 // Dg[b][t] = Ua(b, b + t) makes the row update a run of 16-byte loads.
 #include "internal.cuh"
@@ -39,77 +46,110 @@ namespace bakron {
 
 namespace {
 constexpr int T = kTile;          // 128
-constexpr int S = 32;             // block edge
-constexpr int NB = T / S;         // 4 blocks per tile edge
 constexpr int NTHR = 384;
-constexpr int NPAIR = NTHR / 64;   // warp pairs for the block products
-constexpr int NF = S + 3;         // row-accumulator window: columns b0 .. b0 + 34, b0 >= -3 once active
-constexpr int PX = T + 4;         // tile pitch
-constexpr int PP = S + 1;         // P^T block pitch
-constexpr int PR = S + 4;         // rT pitch (16-byte rows)
-constexpr int PU = S;             // U block pitch (rows read whole, columns written lane by lane)
-constexpr int PC = S + 4;         // code block pitch (bytes)
-constexpr int PD = S + 4;         // diagonal-major pitch (16-byte rows)
-constexpr int RT_SLOT = (S + 1) * PR;   // + one all-zero row
-constexpr int NSTEP = 2 * S - 1;
+constexpr int NWARP = NTHR / 32;
+constexpr int NDEF = 4;           // warps of the deferred pushes during a sweep
+constexpr size_t kSmemLimit = 232448;
 
-constexpr int OFF_X = 0;
-constexpr int OFF_P = OFF_X + T * PX;                  // 12 blocks (J >= 1)
-constexpr int OFF_RT = OFF_P + NB * (NB - 1) * S * PP; // 4 slots
-constexpr int OFF_D = OFF_RT + NB * RT_SLOT;           // 4 diagonal blocks of Ua
-constexpr int OFF_UA = OFF_D + NB * S * PD;            // 6 upper off-diagonal blocks of Ua
-constexpr int OFF_UB = OFF_UA + 6 * S * PU;            // 10 upper blocks of Ub (with diagonal)
-constexpr int OFF_LA = OFF_UB + 10 * S * PU;
-constexpr int OFF_CS = OFF_LA + T;                     // 4 x [S][PC] int8 codes
-constexpr int SMEM_FLOATS = OFF_CS + NB * S * PC / 4;
-constexpr size_t kLeafSmem = sizeof(float) * (size_t)SMEM_FLOATS;
-static_assert(kLeafSmem <= 232448, "leaf shared memory");
-static_assert(NB * S * PU <= NB * (NB - 1) * S * PP, "staging area");
+template <int S>
+struct Cfg {
+  static constexpr int NB = T / S;          // blocks per tile edge
+  static constexpr int BPW = 32 / S;        // blocks per warp in a sweep
+  static constexpr int NF = S + 3;          // row-accumulator window
+  static constexpr int PX = T + 4;          // tile pitch
+  static constexpr int PP = S + 1;          // P^T block pitch
+  static constexpr int PR = S + 4;          // rT pitch (16-byte rows)
+  static constexpr int PU = S;              // U block pitch
+  static constexpr int PC = S + 4;          // code block pitch (bytes)
+  static constexpr int PD = S + 4;          // diagonal-major pitch (16-byte rows)
+  static constexpr int RT_SLOT = (S + 1) * PR;   // + one all-zero row
+  static constexpr int NSTEP = 2 * S - 1;
+  static constexpr int NUA = NB * (NB - 1) / 2;  // upper off-diagonal Ua blocks
+  static constexpr int NUB = NB * (NB + 1) / 2;  // upper Ub blocks (with diagonal)
+  static constexpr int OFF_X = 0;
+  static constexpr int OFF_P = OFF_X + T * PX;               // NB (NB-1) blocks (J >= 1)
+  static constexpr int OFF_RT = OFF_P + NB * (NB - 1) * S * PP;   // 2 sets of NB slots
+  static constexpr int OFF_D = OFF_RT + 2 * NB * RT_SLOT;    // NB diagonal blocks of Ua
+  static constexpr int OFF_UA = OFF_D + NB * S * PD;
+  static constexpr int OFF_UB = OFF_UA + NUA * S * PU;
+  static constexpr int OFF_LA = OFF_UB + NUB * S * PU;
+  static constexpr int OFF_CS = OFF_LA + T;                  // NB x [S][PC] int8 codes
+  static constexpr int SMEM_FLOATS = OFF_CS + NB * S * PC / 4;
+  static constexpr size_t SMEM = sizeof(float) * (size_t)SMEM_FLOATS;
+  // block products: one warp, OPT outputs per lane (RPT rows x CPT columns)
+  static constexpr int OPT = S * S / 32;
+  static constexpr int CPT = OPT < 4 ? OPT : 4;
+  static constexpr int RPT = OPT / CPT;
+  static constexpr int TC = S / CPT;         // lanes along the columns
+  static_assert(SMEM <= kSmemLimit, "leaf shared memory");
+  static_assert(NB * S * PU <= NB * (NB - 1) * S * PP, "staging area");
+  static_assert(RPT * CPT == OPT && (32 / TC) * RPT == S, "product tiling");
+  static_assert(NB / BPW + NDEF <= NWARP, "a level leaves warps for the deferred pushes");
 
-// upper off-diagonal Ua block (J < J2) and upper Ub block (I <= I2)
-__device__ __forceinline__ int ua_idx(int J, int J2) { return J * (7 - J) / 2 + (J2 - J - 1); }
-__device__ __forceinline__ int ub_idx(int I, int I2) { return I * (9 - I) / 2 + (I2 - I); }
-__device__ __forceinline__ int p_idx(int I, int J) { return I * (NB - 1) + (J - 1); }
+  // upper off-diagonal Ua block (J < J2) and upper Ub block (I <= I2)
+  __device__ static __forceinline__ int ua_idx(int J, int J2) {
+    return J * (2 * NB - J - 1) / 2 + (J2 - J - 1);
+  }
+  __device__ static __forceinline__ int ub_idx(int I, int I2) {
+    return I * (2 * NB - I + 1) / 2 + (I2 - I);
+  }
+  __device__ static __forceinline__ int p_idx(int I, int J) { return I * (NB - 1) + (J - 1); }
+};
 
-// tile offsets (row of U^T, column of U^T) of the 20 loaded blocks:
-// Ua diagonal (J, J) for J = 0..3; Ua (J, J2), J < J2, in ua_idx order;
-// Ub (I, I2), I <= I2, in ub_idx order.  Row offset 32 * (J2 or I2),
-// column offset 32 * (J or I).
-__constant__ int kRow[20] = {0,  32, 64, 96,  32, 64, 96, 64, 96, 96,
-                             0,  32, 64, 96,  32, 64, 96, 64, 96, 96};
-__constant__ int kCol[20] = {0,  32, 64, 96,  0,  0,  0,  32, 32, 64,
-                             0,  0,  0,  0,   32, 32, 32, 64, 64, 96};
+// p-th pair (r, c) of the row-major enumeration of {r < c} (strict) or
+// {r <= c} of an nb x nb grid.
+__device__ __forceinline__ void decode_pair(int p, int nb, int strict, int& r, int& c) {
+  int row = 0, cnt = nb - strict;
+  while (p >= cnt) {
+    p -= cnt;
+    ++row;
+    cnt = nb - row - strict;
+  }
+  r = row;
+  c = row + strict + p;
+}
 
-// C(r, c) += sign * sum_k A(r, k) B(k, c) for one 32 x 32 block, 64 threads
-// (lt in [0, 64)), each a 4 x 4 tile: rows 4 tr .. 4 tr + 3, columns
-// tc + 8 u.  A row-major [r][k] with pitch PU (16-byte loads along k),
-// B(k, c) at B[k + c * ldbc], C(r, c) at C[r * ldcr + c].  TRI: A(r, k) = 0
-// for k > r, so the k loop stops at the warp's last row.
-template <bool TRI>
+// C(r, c) += sign * sum_k A(r, k) B(k, c) for one S x S block, one warp.
+// Lane: rows tr + TR i (i < RPT), columns tc + TC u (u < CPT), so the eight
+// lanes of a quarter warp read distinct 16-byte bank groups of A.  A
+// row-major [r][k] with pitch S (16-byte loads along k), B(k, c) at
+// B[k + c * ldbc] (VB: 16-byte loads along k, ldbc a multiple of 4), C(r, c)
+// at C[r * ldcr + c].  TRI: A(r, k) = 0 for k > r.
+template <int S, bool TRI, bool VB>
 __device__ __forceinline__ void block_product(const float* __restrict__ A, const float* __restrict__ B,
                                               int ldbc, float* __restrict__ C, int ldcr, float sign,
-                                              int lt) {
-  const int tr = lt >> 3, tc = lt & 7, r0 = 4 * tr;
-  float acc[4][4];
+                                              int lane) {
+  using K = Cfg<S>;
+  constexpr int RPT = K::RPT, CPT = K::CPT, TC = K::TC, TR = 32 / TC;
+  const int tr = lane / TC, tc = lane % TC;
+  float acc[RPT][CPT];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < RPT; ++i)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[i][u] = 0.f;
-  const int kend = TRI ? ((lt >> 5) + 1) * 16 : S;   // warp-uniform bound
+    for (int u = 0; u < CPT; ++u) acc[i][u] = 0.f;
+  const int kend = TRI ? min(S, (tr + TR * (RPT - 1) + 4) & ~3) : S;
 #pragma unroll 2
   for (int k0 = 0; k0 < kend; k0 += 4) {
-    float4 a4[4];
+    float4 a4[RPT];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a4[i] = *reinterpret_cast<const float4*>(A + (r0 + i) * PU + k0);
-    float bv[4][4];
+    for (int i = 0; i < RPT; ++i) a4[i] = *reinterpret_cast<const float4*>(A + (tr + TR * i) * S + k0);
+    float bv[4][CPT];
+    if constexpr (VB) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
+      for (int u = 0; u < CPT; ++u) {
+        const float4 b4 = *reinterpret_cast<const float4*>(B + (tc + TC * u) * ldbc + k0);
+        bv[0][u] = b4.x; bv[1][u] = b4.y; bv[2][u] = b4.z; bv[3][u] = b4.w;
+      }
+    } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) bv[kk][u] = B[k0 + kk + (tc + 8 * u) * ldbc];
+      for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int u = 0; u < CPT; ++u) bv[kk][u] = B[k0 + kk + (tc + TC * u) * ldbc];
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+    for (int i = 0; i < RPT; ++i)
+#pragma unroll
+      for (int u = 0; u < CPT; ++u) {
         acc[i][u] = fmaf(a4[i].x, bv[0][u], acc[i][u]);
         acc[i][u] = fmaf(a4[i].y, bv[1][u], acc[i][u]);
         acc[i][u] = fmaf(a4[i].z, bv[2][u], acc[i][u]);
@@ -117,28 +157,63 @@ __device__ __forceinline__ void block_product(const float* __restrict__ A, const
       }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < RPT; ++i)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float* c = C + (r0 + i) * ldcr + tc + 8 * u;
+    for (int u = 0; u < CPT; ++u) {
+      float* c = C + (tr + TR * i) * ldcr + tc + TC * u;
       *c = fmaf(sign, acc[i][u], *c);
     }
+}
+
+__device__ __forceinline__ int level_imin(int k, int nb) { return k < nb ? 0 : k - nb + 1; }
+__device__ __forceinline__ int level_imax(int k, int nb) { return k < nb ? k : nb - 1; }
+
+// The pushes of the blocks of level kp that level kp+1 does not need:
+// P[I,J'] += E[I,J] Ua[J,J'] for J' >= J + 2 and W~[I',J] -= Ub[I,I']^T R[I,J]
+// for I' >= I + 2.  Products are dealt to nwork warps in turn; this warp is
+// worker wk.  rTp: the R^T slots of level kp.
+template <int S>
+__device__ __forceinline__ void deferred_pushes(int kp, int wk, int nwork, float* X, float* Pt,
+                                                const float* rTp, const float* UaO, const float* UbB,
+                                                int lane) {
+  using K = Cfg<S>;
+  constexpr int NB = K::NB;
+  const int Ipmin = level_imin(kp, NB), Ipmax = level_imax(kp, NB);
+  int pidx = 0, mine = wk;
+  for (int I = Ipmin; I <= Ipmax; ++I) {
+    const int J = kp - I, slot = I - Ipmin;
+    for (int J2 = J + 2; J2 < NB; ++J2, ++pidx)
+      if (pidx == mine) {
+        block_product<S, false, true>(UaO + K::ua_idx(J, J2) * S * K::PU, X + (S * I) * K::PX + S * J, K::PX,
+                                Pt + K::p_idx(I, J2) * S * K::PP, K::PP, 1.f, lane);
+        mine += nwork;
+      }
+    for (int I2 = I + 2; I2 < NB; ++I2, ++pidx)
+      if (pidx == mine) {
+        block_product<S, false, true>(UbB + K::ub_idx(I, I2) * S * K::PU, rTp + slot * K::RT_SLOT, K::PR,
+                                X + (S * I2) * K::PX + S * J, K::PX, -1.f, lane);
+        mine += nwork;
+      }
+  }
 }
 }  // namespace
 
 // PRE: also write the pre-rounding values (a.preround), a debug output kept
 // out of the default instantiation for its register cost
-template <bool PRE>
+template <int S, bool PRE>
 __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
+  using K = Cfg<S>;
+  constexpr int NB = K::NB, BPW = K::BPW, NF = K::NF, PX = K::PX, PP = K::PP, PR = K::PR,
+                PU = K::PU, PC = K::PC, PD = K::PD, RT_SLOT = K::RT_SLOT, NSTEP = K::NSTEP;
   extern __shared__ __align__(16) float smem[];
-  float* X = smem + OFF_X;     // [T][PX]: W~, then E block by block
-  float* Pt = smem + OFF_P;    // 12 x [S][PP]: P^T[I,J] (b, a), J >= 1
-  float* rT = smem + OFF_RT;   // 4 x [S+1][PR]: completed r(a, b) at [b][a]; then R^T
-  float* Dg = smem + OFF_D;    // 4 x [S][PD]: Dg[J][b][t] = Ua(32J+b, 32J+b+t), 0 past the block
-  float* UaO = smem + OFF_UA;  // 6 x [S][PU]: Ua(32J+b, 32J2+b2) at [b2][b]
-  float* UbB = smem + OFF_UB;  // 10 x [S][PU]: Ub(32I+a, 32I2+a2) at [a2][a]
-  float* lA = smem + OFF_LA;   // [T]: 1 / Ua(b, b)
-  signed char* CS = reinterpret_cast<signed char*>(smem + OFF_CS);  // 4 x [S][PC] codes
+  float* X = smem + K::OFF_X;     // [T][PX]: W~, then E block by block
+  float* Pt = smem + K::OFF_P;    // NB (NB-1) x [S][PP]: P^T[I,J] (b, a), J >= 1
+  float* rT0 = smem + K::OFF_RT;  // 2 x NB x [S+1][PR]: completed r(a, b) at [b][a]; then R^T
+  float* Dg = smem + K::OFF_D;    // NB x [S][PD]: Dg[J][b][t] = Ua(SJ+b, SJ+b+t), 0 past the block
+  float* UaO = smem + K::OFF_UA;  // NUA x [S][PU]: Ua(SJ+b, SJ2+b2) at [b2][b]
+  float* UbB = smem + K::OFF_UB;  // NUB x [S][PU]: Ub(SI+a, SI2+a2) at [a2][a]
+  float* lA = smem + K::OFF_LA;   // [T]: 1 / Ua(b, b)
+  signed char* CS = reinterpret_cast<signed char*>(smem + K::OFF_CS);  // NB x [S][PC] codes
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -146,35 +221,37 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   const int Jtile = a.D - Itile;
   const int64_t i0 = (int64_t)Itile * T, j0 = (int64_t)Jtile * T;
 
-  // ---- load: W~ tile, the upper blocks of Ua and Ub (16-byte loads, several
-  // in flight per thread).  The global arrays hold U^T: lane = row of the
-  // shared block, so the transposing shared stores are conflict-free.
+  // ---- load: W~ tile, the upper blocks of Ua and Ub (16-byte loads, all of
+  // a thread's issued before its first store).  The global arrays hold U^T:
+  // a block is copied as it is stored (rows of U^T = columns of U).
 #pragma unroll 4
   for (int idx = tid; idx < T * T / 4; idx += NTHR) {
     const int r = idx >> 5, c = (idx & 31) * 4;
     *reinterpret_cast<float4*>(X + r * PX + c) =
         *reinterpret_cast<const float4*>(a.wt + (i0 + r) * a.ldw + j0 + c);
   }
-  // 20 blocks of U^T copied as they are (rows of U^T = columns of U):
-  // Ua diagonal blocks 0-3 (staged in the P area), Ua upper off-diagonal
-  // blocks 4-9, Ub upper blocks 10-19.  Block u is the 32 x 32 block of U^T
-  // at tile offsets (row kRow[u], column kCol[u]); a warp reads four whole
-  // 128-byte rows per instruction, and all loads of a thread are issued
-  // before the first store.
+  // blocks u < NB: Ua diagonal (staged in the P area); NB <= u < NB + NUA:
+  // Ua upper off-diagonal; then Ub upper with diagonal.  Block of U^T at
+  // (row S * c, column S * r) for the pair (r, c).
   float* stage = Pt;
   {
-    constexpr int kItems = 20 * S * S / 4;
-    constexpr int kIt = (kItems + NTHR - 1) / NTHR;   // items per thread
+    constexpr int QPB = S * S / 4;   // 16-byte items per block
+    constexpr int kItems = (NB + K::NUA + K::NUB) * QPB;
+    constexpr int kIt = (kItems + NTHR - 1) / NTHR;
     float4 hv[kIt], lv[kIt];
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
       const int idx = min(tid + it * NTHR, kItems - 1);   // the tail repeats the last item
-      const int blk = idx >> 8, w = idx & 255;
-      const int r = w >> 3, q = (w & 7) * 4;
-      const bool isA = blk < 10;
+      const int blk = idx / QPB, w = idx % QPB;
+      const int r = w / (S / 4), q = (w % (S / 4)) * 4;
+      int br, bc;
+      const bool isA = blk < NB + K::NUA;
+      if (blk < NB) { br = blk; bc = blk; }
+      else if (isA) decode_pair(blk - NB, NB, 1, br, bc);
+      else decode_pair(blk - NB - K::NUA, NB, 0, br, bc);
       const int64_t base = isA ? j0 : i0;
       const int64_t ld = isA ? a.lda : a.ldb;
-      const int64_t g = (base + kRow[blk] + r) * ld + base + kCol[blk] + q;
+      const int64_t g = (base + S * bc + r) * ld + base + S * br + q;
       hv[it] = *reinterpret_cast<const float4*>((isA ? a.lat_hi : a.lbt_hi) + g);
       lv[it] = *reinterpret_cast<const float4*>((isA ? a.lat_lo : a.lbt_lo) + g);
     }
@@ -182,10 +259,11 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
     for (int it = 0; it < kIt; ++it) {
       const int idx = tid + it * NTHR;
       if (idx >= kItems) break;
-      const int blk = idx >> 8, w = idx & 255;
-      const int r = w >> 3, q = (w & 7) * 4;
-      float* dst = blk < 4 ? stage + blk * S * PU
-                           : (blk < 10 ? UaO + (blk - 4) * S * PU : UbB + (blk - 10) * S * PU);
+      const int blk = idx / QPB, w = idx % QPB;
+      const int r = w / (S / 4), q = (w % (S / 4)) * 4;
+      float* dst = blk < NB ? stage + blk * S * PU
+                            : (blk < NB + K::NUA ? UaO + (blk - NB) * S * PU
+                                                 : UbB + (blk - NB - K::NUA) * S * PU);
       float4 v;
       v.x = hv[it].x + lv[it].x;
       v.y = hv[it].y + lv[it].y;
@@ -194,15 +272,15 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       *reinterpret_cast<float4*>(dst + r * PU + q) = v;
     }
   }
-  for (int idx = tid; idx < NB * RT_SLOT; idx += NTHR) rT[idx] = 0.f;
+  for (int idx = tid; idx < 2 * NB * RT_SLOT; idx += NTHR) rT0[idx] = 0.f;
   __syncthreads();
   for (int idx = tid; idx < NB * S * PD; idx += NTHR) {
     const int J = idx / (S * PD), rem = idx - J * S * PD;
-    const int t = rem >> 5, b = rem & (S - 1);
-    Dg[J * S * PD + b * PD + t] = (b + t < S) ? stage[J * S * PU + (b + t) * PU + b] : 0.f;
+    const int b = rem / PD, t = rem % PD;
+    Dg[idx] = (t < S && b + t < S) ? stage[J * S * PU + (b + t) * PU + b] : 0.f;
   }
   if (tid < T) {
-    const int J = tid >> 5, b = tid & (S - 1);
+    const int J = tid / S, b = tid % S;
     lA[tid] = 1.f / stage[J * S * PU + b * PU + b];
   }
   __syncthreads();
@@ -211,27 +289,20 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
 
   const float fqmin = (float)a.qmin, fqmax = (float)a.qmax;
   bool nonfinite = false, out_of_range = false;
-  const int pair = warp >> 1, lt = (warp & 1) * 32 + lane;
 
   for (int k = 0; k < 2 * NB - 1; ++k) {
-    const int Imin = k < NB ? 0 : k - NB + 1;
-    const int Imax = k < NB ? k : NB - 1;
+    const int Imin = level_imin(k, NB), Imax = level_imax(k, NB);
     const int nblk = Imax - Imin + 1;
+    const int nsw = (nblk + BPW - 1) / BPW;    // sweep warps of this level
+    float* rTk = rT0 + (k & 1) * NB * RT_SLOT;
 
-    // ---- A. x0 = W~ - Ub[I,I]^T P[I,J] for the blocks of this level with J >= 1
-    if (pair < nblk) {
-      const int I = Imin + pair, J = k - I;
-      if (J >= 1)
-        block_product<true>(UbB + ub_idx(I, I) * S * PU, Pt + p_idx(I, J) * S * PP, PP,
-                            X + (S * I) * PX + S * J, PX, -1.f, lt);
-    }
-    __syncthreads();
-
-    // ---- B. block sweeps
-    if (warp < nblk) {
-      const int I = Imin + warp, J = k - I;
-      const int row = lane;
-      const float* Ubd = UbB + ub_idx(I, I) * S * PU;
+    if (warp < nsw) {
+      // ---- B. block sweeps: lane = (sub, row), block Imin + BPW warp + sub
+      const int sub = lane / S, row = lane % S;
+      const int slot = warp * BPW + sub;
+      const bool live = slot < nblk;
+      const int I = Imin + (live ? slot : 0), J = k - I;
+      const float* Ubd = UbB + K::ub_idx(I, I) * S * PU;
       float ub[S];
 #pragma unroll
       for (int c = 0; c < S / 4; ++c) {
@@ -241,27 +312,27 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         ub[4 * c + 2] = (4 * c + 2 < row - 1) ? v.z : 0.f;
         ub[4 * c + 3] = (4 * c + 3 < row - 1) ? v.w : 0.f;
       }
-      ub[S - 1] = 0.f;   // a' < a - 1 <= 30
+      ub[S - 1] = 0.f;   // a' < a - 1 <= S - 2
       // Ub(a-1, a): the row directly above, whose accumulator completes one
       // step before this row needs it, is kept out of the look-ahead sum
       const float ub1 = row > 0 ? Ubd[row * PU + row - 1] : 0.f;
-      const int rowm1 = row > 0 ? row - 1 : 0;
       const float ubaa = Ubd[row * PU + row];
       const float lB = 1.f / ubaa;
       const int64_t gi = i0 + S * I + row;
       const float sc = a.scale[gi];
-      const bool row_real = gi < a.m;
-      float* rs = rT + warp * RT_SLOT;
+      const bool row_real = live && gi < a.m;
+      float* rs = rTk + slot * RT_SLOT;
       const float* Dj = Dg + J * S * PD;
       const float* lAj = lA + S * J;
       float* Xrow = X + (S * I + row) * PX + S * J;
       const int64_t jb0 = j0 + S * J;
       const float rinv = 1.f / sc;
-      signed char* csr = CS + warp * S * PC + row * PC;
+      signed char* csr = CS + slot * S * PC + row * PC;
       float FR[NF];
 #pragma unroll
       for (int j = 0; j < NF; ++j) FR[j] = 0.f;
       float pp = 0.f;   // column sum over rows a' < a - 1 for this step's column
+      float rlast = 0.f;  // r(a, .) completed by this lane in the previous step
 
       for (int kb = 0; kb * 4 < NSTEP; ++kb) {
 #pragma unroll
@@ -271,12 +342,13 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           // straight-line step: inactive lanes compute on safe addresses and
           // their results are masked (e = 0, stores predicated)
           const int b = d - row;
-          const bool act = (unsigned)b < (unsigned)S;
+          const bool act = live && (unsigned)b < (unsigned)S;
           const int bb = act ? b : 0;
           const float xin = Xrow[bb];
           const float la = lAj[bb];
-          // completed r(a-1, b) of the row above (previous step)
-          const float rprev = rs[(act ? b : S) * PR + rowm1];
+          // r(a-1, b): the row above completed column b in the previous step
+          // (lane 0 of a block multiplies it by ub1 = 0)
+          const float rprev = __shfl_up_sync(0xffffffffu, rlast, 1);
           // look-ahead: the column sum of the NEXT step (column b + 1) over
           // rows a' < a - 1, all completed by the previous step; it is off
           // this step's dependency chain
@@ -307,14 +379,14 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           nonfinite |= act && !isfinite(x);
           out_of_range |= act && ((c < -128.f) || (c > 127.f));
           FR[sg] = fmaf(e, dv[0].x, FR[sg]);
+          rlast = FR[sg];
           if (act) {
             Xrow[b] = e;
             csr[b] = (signed char)(int)fminf(fmaxf(c, -128.f), 127.f);
             rs[b * PR + row] = FR[sg];
           }
           if (PRE && act && row_real && jb0 + b < a.n) a.preround[gi * a.n + jb0 + b] = x;
-          // pending accumulators of this row: FR[sg + t] += e Ua(b, b + t),
-          // first with the values loaded before the stores, then the rest
+          // pending accumulators of this row: FR[sg + t] += e Ua(b, b + t)
 #pragma unroll
           for (int c = 0; c < PD / 4; ++c) {
             const float4 v = dv[c];
@@ -335,14 +407,27 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         const int64_t base = gi * a.n + jb0;
         const int nb = a.n - jb0 < S ? (int)(a.n - jb0) : S;
         if (nb == S && (a.n & 15) == 0) {
-          uint4 w[2];
-          unsigned* wu = reinterpret_cast<unsigned*>(w);
+          if constexpr (S % 16 == 0) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) wu[q] = *reinterpret_cast<const unsigned*>(csr + 4 * q);
-          reinterpret_cast<uint4*>(a.codes + base)[0] = w[0];
-          reinterpret_cast<uint4*>(a.codes + base)[1] = w[1];
+            for (int q = 0; q < S / 16; ++q) {
+              uint4 w;
+              w.x = *reinterpret_cast<const unsigned*>(csr + 16 * q + 0);
+              w.y = *reinterpret_cast<const unsigned*>(csr + 16 * q + 4);
+              w.z = *reinterpret_cast<const unsigned*>(csr + 16 * q + 8);
+              w.w = *reinterpret_cast<const unsigned*>(csr + 16 * q + 12);
+              reinterpret_cast<uint4*>(a.codes + base)[q] = w;
+            }
+          } else {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < S / 8; ++q) {
+              uint2 w;
+              w.x = *reinterpret_cast<const unsigned*>(csr + 8 * q + 0);
+              w.y = *reinterpret_cast<const unsigned*>(csr + 8 * q + 4);
+              reinterpret_cast<uint2*>(a.codes + base)[q] = w;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < S / 4; ++q) {
             float4 v;
             v.x = sc * (float)csr[4 * q + 0];
             v.y = sc * (float)csr[4 * q + 1];
@@ -358,62 +443,84 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         }
       }
       // R^T = P^T + r^T in place (lane = block row a owns column a)
-      if (J >= 1) {
-        const float* pb = Pt + p_idx(I, J) * S * PP;
+      if (live && J >= 1) {
+        const float* pb = Pt + K::p_idx(I, J) * S * PP;
 #pragma unroll 8
         for (int b = 0; b < S; ++b) rs[b * PR + row] += pb[b * PP + row];
       }
+    } else if (k >= 1 && warp < nsw + NDEF) {
+      // ---- deferred pushes of level k-1 into levels >= k+1, on NDEF of the
+      // other warps (more would take issue and shared-memory bandwidth from
+      // the latency-bound sweeps)
+      deferred_pushes<S>(k - 1, warp - nsw, NDEF, X, Pt, rT0 + ((k - 1) & 1) * NB * RT_SLOT,
+                         UaO, UbB, lane);
     }
     __syncthreads();
 
-    // ---- C. pushes from the blocks of this level, one block product per warp pair
-    {
-      int pidx = 0;
-      for (int I = Imin; I <= Imax; ++I) {
-        const int J = k - I, slot = I - Imin;
-        for (int J2 = J + 1; J2 < NB; ++J2, ++pidx)
-          if (pidx % NPAIR == pair)
-            block_product<false>(UaO + ua_idx(J, J2) * S * PU, X + (S * I) * PX + S * J, PX,
-                                 Pt + p_idx(I, J2) * S * PP, PP, 1.f, lt);
-        for (int I2 = I + 1; I2 < NB; ++I2, ++pidx)
-          if (pidx % NPAIR == pair)
-            block_product<false>(UbB + ub_idx(I, I2) * S * PU, rT + slot * RT_SLOT, PR,
-                                 X + (S * I2) * PX + S * J, PX, -1.f, lt);
+    // ---- prep(k+1): x0 of the blocks of level k+1, one warp per block
+    if (k + 1 < 2 * NB - 1) {
+      const int kn = k + 1;
+      const int Inmin = level_imin(kn, NB), Inmax = level_imax(kn, NB);
+      const int nn = Inmax - Inmin + 1;
+      for (int w = warp; w < nn; w += NWARP) {
+        const int I = Inmin + w, J = kn - I;
+        float* Xb = X + (S * I) * PX + S * J;
+        if (J >= 1)   // P[I,J] += E[I,J-1] Ua[J-1,J]  (the left neighbour, level k)
+          block_product<S, false, true>(UaO + K::ua_idx(J - 1, J) * S * PU, X + (S * I) * PX + S * (J - 1),
+                                  PX, Pt + K::p_idx(I, J) * S * PP, PP, 1.f, lane);
+        if (I >= 1)   // W~[I,J] -= Ub[I-1,I]^T R[I-1,J]  (the upper neighbour, level k)
+          block_product<S, false, true>(UbB + K::ub_idx(I - 1, I) * S * PU,
+                                  rTk + (I - 1 - Imin) * RT_SLOT, PR, Xb, PX, -1.f, lane);
+        __syncwarp();
+        if (J >= 1)   // W~[I,J] -= Ub[I,I]^T P[I,J]
+          block_product<S, true, false>(UbB + K::ub_idx(I, I) * S * PU, Pt + K::p_idx(I, J) * S * PP, PP,
+                                 Xb, PX, -1.f, lane);
       }
+      __syncthreads();
     }
-    __syncthreads();
   }
 
   if (nonfinite) set_status(a.st, BAKRON_ERR_NONFINITE);
   if (out_of_range) set_status(a.st, BAKRON_ERR_CODE_RANGE);
 
   // write-out: scaled errors (split) for the propagation
-  for (int idx = tid; idx < T * T; idx += NTHR) {
-    const int r = idx >> 7, cc = idx & (T - 1);
-    const float e = X[r * PX + cc];
-    const float h = tf32_round(e);
+  for (int idx = tid; idx < T * T / 4; idx += NTHR) {
+    const int r = idx >> 5, cc = (idx & 31) * 4;
+    const float4 e = *reinterpret_cast<const float4*>(X + r * PX + cc);
+    float4 h, l;
+    h.x = tf32_round(e.x); h.y = tf32_round(e.y); h.z = tf32_round(e.z); h.w = tf32_round(e.w);
+    l.x = e.x - h.x; l.y = e.y - h.y; l.z = e.z - h.z; l.w = e.w - h.w;
+    if (a.round_lo) {
+      l.x = tf32_round(l.x); l.y = tf32_round(l.y); l.z = tf32_round(l.z); l.w = tf32_round(l.w);
+    }
     const int64_t g = (i0 + r) * a.ldw + j0 + cc;
-    a.e_hi[g] = h;
-    a.e_lo[g] = a.round_lo ? tf32_round(e - h) : e - h;
+    *reinterpret_cast<float4*>(a.e_hi + g) = h;
+    *reinterpret_cast<float4*>(a.e_lo + g) = l;
   }
 }
 
+namespace {
+constexpr int kLeafBlock = 16;
+}  // namespace
+
 cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s) {
+  constexpr int S = kLeafBlock;
   static bool attr_set = false;
+  constexpr size_t smem = Cfg<S>::SMEM;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(leaf_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLeafSmem);
+    cudaError_t e = cudaFuncSetAttribute(leaf_kernel<S, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(leaf_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kLeafSmem);
+      e = cudaFuncSetAttribute(leaf_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   count_launch();
   if (a.preround)
-    leaf_kernel<true><<<n_tiles, NTHR, kLeafSmem, s>>>(a);
+    leaf_kernel<S, true><<<n_tiles, NTHR, smem, s>>>(a);
   else
-    leaf_kernel<false><<<n_tiles, NTHR, kLeafSmem, s>>>(a);
+    leaf_kernel<S, false><<<n_tiles, NTHR, smem, s>>>(a);
   return cudaGetLastError();
 }
 
