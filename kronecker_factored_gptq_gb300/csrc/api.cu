@@ -613,6 +613,10 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
       for (cudaEvent_t ev : waits[op.D]) TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
       la.D = op.D;
       la.I0 = op.I0;
+      // the first leaf reads the factors the kernel directly before it wrote;
+      // a leaf also waiting on deferred chunks (events) still waits for them
+      // in full, the relaxation covers only the previous kernel on this stream
+      la.pdl = op.D > 0;
       cudaEvent_t ev = pt.begin();
       TRY_CUDA(launch_leaf(la, op.ntiles, cs));
       pt.end(0, ev);
@@ -634,6 +638,7 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
     p2.st = st;
     auto launch = [&](PropArgs& pa, int off, int nit, int maxk, cudaStream_t str) {
       pa.items = items + off; pa.n_items = nit; pa.max_k = maxk;
+      pa.pdl = str == cs;
       return o.use_3xtf32 ? launch_prop_tc(pa, str) : launch_prop_simt(pa, str);
     };
     cudaEvent_t ev_s1 = nullptr;

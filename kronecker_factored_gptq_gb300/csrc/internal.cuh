@@ -26,6 +26,19 @@ __device__ __forceinline__ void set_status(DevStatus* st, int code) {
   atomicCAS(&st->status, 0, code);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialisation attribute may start before the previous kernel in
+// its stream has finished; grid_dep_wait() blocks until that kernel has
+// completed and its memory is visible (a no-op for a normal launch).
+// grid_dep_launch() lets the next such kernel start; every kernel here
+// issues it only after its own grid_dep_wait(), so work a kernel does
+// before its wait may read what launches two or more back wrote, never
+// what the launch directly before it writes.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Round an fp32 value to the nearest TF32 value (10 explicit mantissa bits),
 // ties away from zero on the magnitude; Inf/NaN pass through.  The 3xTF32
 // split keeps hi = tf32(x) and lo = x - hi (exact in fp32).
@@ -55,6 +68,7 @@ struct PropArgs {
   float alpha;                       // stage 1 scale (0 means 1)
   float* tr_hi; float* tr_lo; int64_t ldt;  // stage 1, nullable: transposed split store
   DevStatus* st;
+  int pdl;    // launch as a programmatic dependent of the previous kernel
 };
 
 struct LeafArgs {
@@ -69,7 +83,26 @@ struct LeafArgs {
   int qmin, qmax;
   int D, I0;                         // tile anti-diagonal; first row tile
   DevStatus* st;
+  int pdl;    // launch as a programmatic dependent of the previous kernel
 };
+
+// Launch `k` on `s`, as a programmatic dependent of the previous kernel in
+// the stream when `pdl` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
 
 // Process-wide count of kernel launches made by the library.
 void count_launch(int k = 1);

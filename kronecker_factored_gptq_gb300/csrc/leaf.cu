@@ -221,15 +221,11 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   const int Jtile = a.D - Itile;
   const int64_t i0 = (int64_t)Itile * T, j0 = (int64_t)Jtile * T;
 
-  // ---- load: W~ tile, the upper blocks of Ua and Ub (16-byte loads, all of
-  // a thread's issued before its first store).  The global arrays hold U^T:
-  // a block is copied as it is stored (rows of U^T = columns of U).
-#pragma unroll 4
-  for (int idx = tid; idx < T * T / 4; idx += NTHR) {
-    const int r = idx >> 5, c = (idx & 31) * 4;
-    *reinterpret_cast<float4*>(X + r * PX + c) =
-        *reinterpret_cast<const float4*>(a.wt + (i0 + r) * a.ldw + j0 + c);
-  }
+  // ---- load: the upper blocks of Ua and Ub (16-byte loads, all of a
+  // thread's issued before its first store), then the W~ tile.  The global
+  // arrays hold U^T: a block is copied as it is stored (rows of U^T =
+  // columns of U).  The factors were written at the start of the solve, so
+  // they are read before waiting for the previous kernel (which writes W~).
   // blocks u < NB: Ua diagonal (staged in the P area); NB <= u < NB + NUA:
   // Ua upper off-diagonal; then Ub upper with diagonal.  Block of U^T at
   // (row S * c, column S * r) for the pair (r, c).
@@ -285,12 +281,20 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   }
   __syncthreads();
   for (int idx = tid; idx < NB * (NB - 1) * S * PP; idx += NTHR) Pt[idx] = 0.f;
+  grid_dep_wait();
+#pragma unroll 4
+  for (int idx = tid; idx < T * T / 4; idx += NTHR) {
+    const int r = idx >> 5, c = (idx & 31) * 4;
+    *reinterpret_cast<float4*>(X + r * PX + c) =
+        *reinterpret_cast<const float4*>(a.wt + (i0 + r) * a.ldw + j0 + c);
+  }
   __syncthreads();
 
   const float fqmin = (float)a.qmin, fqmax = (float)a.qmax;
   bool nonfinite = false, out_of_range = false;
 
   for (int k = 0; k < 2 * NB - 1; ++k) {
+    if (k == 2 * NB - 2) grid_dep_launch();   // the next kernel may start setting up
     const int Imin = level_imin(k, NB), Imax = level_imax(k, NB);
     const int nblk = Imax - Imin + 1;
     const int nsw = (nblk + BPW - 1) / BPW;    // sweep warps of this level
@@ -518,10 +522,8 @@ cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s) {
   }
   count_launch();
   if (a.preround)
-    leaf_kernel<S, true><<<n_tiles, NTHR, smem, s>>>(a);
-  else
-    leaf_kernel<S, false><<<n_tiles, NTHR, smem, s>>>(a);
-  return cudaGetLastError();
+    return launch_kernel(leaf_kernel<S, true>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
+  return launch_kernel(leaf_kernel<S, false>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
 }
 
 }  // namespace bakron

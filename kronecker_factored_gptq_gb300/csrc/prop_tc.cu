@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t sbase = (base_raw + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_ahi) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_alo) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_bhi) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_blo) : "memory");
     abort_flag = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
@@ -185,6 +189,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   fence_after_sync();
   const uint32_t tmem = tmem_slot;
   volatile int* abortp = &abort_flag;
+  // the operands (and, for stage 2, W~) come from the previous kernels
+  grid_dep_wait();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -254,6 +260,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if ((i % SPC) == SPC - 1) mma_commit(smem_u32(&acc_full[b]));
     }
     mma_commit(smem_u32(&bar_done));
+    grid_dep_launch();   // every MMA of this CTA is issued
   } else if (warp >= 4) {
     // ---------------- epilogue: running fp32 sums of the K-tile chunks
     const int q = warp - 4;                 // TMEM lane quarter (warp % 4)
@@ -426,8 +433,8 @@ cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s) {
       !make_map(&bhi, p.B_hi, p.b_rows, p.ldb) || !make_map(&blo, p.B_lo, p.b_rows, p.ldb))
     return cudaErrorInvalidValue;
   count_launch();
-  prop_tc_kernel<<<p.n_items, NTHREADS, kSmem, s>>>(ahi, alo, bhi, blo, p, p.st);
-  return cudaGetLastError();
+  return launch_kernel(prop_tc_kernel, dim3(p.n_items), dim3(NTHREADS), kSmem, s, p.pdl != 0, ahi, alo,
+                       bhi, blo, p, p.st);
 }
 
 }  // namespace bakron
