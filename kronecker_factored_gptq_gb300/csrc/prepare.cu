@@ -160,36 +160,43 @@ __global__ void flip_damp_kernel(const float* __restrict__ X, int64_t k, const f
 // G_kk (lower, zero upper) back, inv(G_kk) split into Ginv's and (transposed)
 // into Ginv^T's diagonal block, and plainly into inv_plain (128 x 128).
 //
-// Blocked by 32: for each 32-wide column panel, one warp factors the 32 x 32
-// diagonal sub-block in registers (lane = row, shuffles), the rows below
-// solve against it (one thread per row), and all threads apply the trailing
-// update with 2-D register blocks.  The inverse starts from the four 32 x 32
-// diagonal inverses (one warp each, lane = column) and doubles twice,
-// X21 = -inv(G22) G21 inv(G11), with shared-memory products.
-constexpr size_t kPotrfSmem = sizeof(float) * 3 * NB * (NB + 1);
-constexpr int PP = NB + 1;
+// Right-looking with 16-wide column panels: warp 0 factors the 16 x 16
+// diagonal block in registers (lane = row, shuffles), one thread per row
+// below solves against it column by column (each step of its chain is one
+// multiply and one fused multiply-add), and every thread updates 4 x 4 tiles
+// of the trailing lower triangle.  The inverse starts from the eight 16 x 16
+// diagonal inverses (one warp each, lane = column, column by column) and
+// doubles three times, X21 = -inv(G22) (G21 inv(G11)), with 4 x 4 register
+// tiles over both triangular operands.
+constexpr int PB = 16;                 // panel width
+constexpr int PP = NB + 1;             // shared pitch (odd: row and column walks are conflict-free)
+constexpr size_t kPotrfSmem = sizeof(float) * (3 * NB * PP + NB);
 
-// C = alpha * A * B over an M x N output (M, N multiples of 16, K <= 128),
-// A (M x K), B (K x N), C all row-major in shared memory with pitch PP.
-// kmax_row: A lower triangular (A[m][k] = 0 for k > m) -> K limited per row.
-__device__ __forceinline__ void smem_mm(float* C, const float* A, const float* B, int M, int N, int K, float alpha,
-                        bool a_lower) {
-  const int tid = threadIdx.x, nth = blockDim.x;
-  const int nbn = N / 2, nblocks = (M / 2) * nbn;
-  for (int blk = tid; blk < nblocks; blk += nth) {
-    const int m = (blk / nbn) * 2, n = (blk % nbn) * 2;
-    const int kend = a_lower ? min(K, m + 2) : K;
-    float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
+// One 4 x 4 tile (rows m0.., columns n0..) of C = alpha * A * B, all in
+// shared memory with pitch PP, K range [k0, k1).
+__device__ __forceinline__ void tile_mm(float* C, const float* A, const float* B, int m0, int n0,
+                                        int k0, int k1, float alpha) {
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 #pragma unroll 4
-    for (int k = 0; k < kend; ++k) {
-      const float a0 = A[m * PP + k], a1 = A[(m + 1) * PP + k];
-      const float b0 = B[k * PP + n], b1 = B[k * PP + n + 1];
-      c00 = fmaf(a0, b0, c00); c01 = fmaf(a0, b1, c01);
-      c10 = fmaf(a1, b0, c10); c11 = fmaf(a1, b1, c11);
-    }
-    C[m * PP + n] = alpha * c00; C[m * PP + n + 1] = alpha * c01;
-    C[(m + 1) * PP + n] = alpha * c10; C[(m + 1) * PP + n + 1] = alpha * c11;
+  for (int k = k0; k < k1; ++k) {
+    float a[4], b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = A[(m0 + i) * PP + k];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) b[j] = B[k * PP + n0 + j];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) C[(m0 + i) * PP + n0 + j] = alpha * acc[i][j];
 }
 
 __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi, float* Gilo,
@@ -200,134 +207,149 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
   float* G = psm;                  // [NB][PP] the block, then its factor
   float* X = G + NB * PP;          // [NB][PP] the inverse
   float* S = X + NB * PP;          // [NB][PP] scratch
+  float* dinv = S + NB * PP;       // [NB] 1 / G[j][j]
   const unsigned FULLM = 0xffffffffu;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NT = 512;
   const int64_t o = kb * NB;
 #pragma unroll 8
-  for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
+  for (int idx = tid; idx < NB * NB; idx += NT) {
     const int r = idx / NB, c = idx - r * NB;
     G[r * PP + c] = (c <= r) ? C[(o + r) * kp + o + c] : 0.f;
     X[r * PP + c] = 0.f;
   }
   __syncthreads();
-  for (int sb = 0; sb < NB / 32; ++sb) {
-    const int q = sb * 32;
-    // (1) diagonal 32 x 32 sub-block, warp 0, lane = row
+  for (int sb = 0; sb < NB / PB; ++sb) {
+    const int q = sb * PB;
+    // (1) diagonal 16 x 16 block: warp 0, lanes r and r + 16 hold row r
     if (warp == 0) {
-      float a[32];
+      const int r = lane & (PB - 1);
+      float a[PB];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) a[k] = (k <= lane) ? G[(q + lane) * PP + q + k] : 0.f;
+      for (int c = 0; c < PB; ++c) a[c] = (c <= r) ? G[(q + r) * PP + q + c] : 0.f;
+      int badj = -1;   // first non-positive or non-finite pivot (replaced by 1)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < PB; ++j) {
         float d = __shfl_sync(FULLM, a[j], j);
-        if (!(d > 0.f) || !isfinite(d)) {
-          if (lane == 0 && o + q + j < k_real) {
-            atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + j));
-            set_status(st, BAKRON_ERR_NOT_PD);
-          }
-          d = 1.f;
-        }
-        const float piv = sqrtf(d), inv = 1.f / piv;
+        const bool bad = !(d > 0.f) || !isfinite(d);
+        if (bad && badj < 0) badj = j;
+        d = bad ? 1.f : d;
+        const float inv = rsqrtf(d);
         const float l = a[j] * inv;
-        if (lane == j) a[j] = piv;
-        else if (lane > j) a[j] = l;
+        if (r == j) a[j] = d * inv;
+        else if (r > j) a[j] = l;
+        if (lane == 0) dinv[q + j] = inv;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < PB; ++k) {
           if (k > j) {
             const float lk = __shfl_sync(FULLM, l, k);
-            if (lane >= k) a[k] -= l * lk;
+            if (r >= k) a[k] = fmaf(-l, lk, a[k]);
           }
         }
       }
+      if (lane < PB) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        if (k <= lane) G[(q + lane) * PP + q + k] = a[k];
+        for (int c = 0; c < PB; ++c)
+          if (c <= r) G[(q + r) * PP + q + c] = a[c];
+      }
+      if (lane == 0 && badj >= 0 && o + q + badj < k_real) {
+        atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + badj));
+        set_status(st, BAKRON_ERR_NOT_PD);
+      }
     }
     __syncthreads();
-    const int base = q + 32, n2 = NB - base;
+    const int base = q + PB, n2 = NB - base;
     if (n2 <= 0) break;
-    // (2) rows below: l[c] = (G[r][q+c] - sum_{t<c} l[t] L11[c][t]) / L11[c][c]
+    // (2) rows below: l = g L11^{-T}, one thread per row, column by column
     if (tid < n2) {
       const int r = base + tid;
-      float l[32];
+      float l[PB];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) l[c] = G[r * PP + q + c];
+      for (int c = 0; c < PB; ++c) l[c] = G[r * PP + q + c];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float acc = l[c];
+      for (int c = 0; c < PB; ++c) {
+        l[c] *= dinv[q + c];
 #pragma unroll
-        for (int t = 0; t < c; ++t) acc = fmaf(-l[t], G[(q + c) * PP + q + t], acc);
-        l[c] = acc / G[(q + c) * PP + q + c];
+        for (int t = c + 1; t < PB; ++t) l[t] = fmaf(-l[c], G[(q + t) * PP + q + c], l[t]);
       }
 #pragma unroll
-      for (int c = 0; c < 32; ++c) G[r * PP + q + c] = l[c];
+      for (int c = 0; c < PB; ++c) G[r * PP + q + c] = l[c];
     }
     __syncthreads();
-    // (3) trailing lower triangle: G[r][c] -= sum_t L21[r][t] L21[c][t]
+    // (3) trailing lower triangle: G[i][j] -= sum_t L21[i][t] L21[j][t] over
+    // 4 x 4 tiles (ti, tj), tj <= ti; reads columns q.., writes columns >= base
     {
-      const int tx = tid & 31, ty = tid >> 5;    // rows base+ty+16i, cols base+tx+32l
-      float acc[6][3];
+      const int tn = n2 / 4, ntiles = tn * (tn + 1) / 2;
+      for (int t = tid; t < ntiles; t += NT) {
+        int ti = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
+        while ((ti + 1) * (ti + 2) / 2 <= t) ++ti;
+        while (ti * (ti + 1) / 2 > t) --ti;
+        const int tj = t - ti * (ti + 1) / 2;
+        const int i0 = base + 4 * ti, j0 = base + 4 * tj;
+        float acc[4][4];
 #pragma unroll
-      for (int i = 0; i < 6; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int l = 0; l < 3; ++l) acc[i][l] = 0.f;
-      for (int t = 0; t < 32; ++t) {
-        float ar[6], bc[3];
+          for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+        for (int tt = 0; tt < PB; ++tt) {
+          float av[4], bv[4];
 #pragma unroll
-        for (int i = 0; i < 6; ++i) {
-          const int r = base + ty + 16 * i;
-          ar[i] = r < NB ? G[r * PP + q + t] : 0.f;
+          for (int i = 0; i < 4; ++i) av[i] = G[(i0 + i) * PP + q + tt];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bv[j] = G[(j0 + j) * PP + q + tt];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
 #pragma unroll
-        for (int l = 0; l < 3; ++l) {
-          const int c = base + tx + 32 * l;
-          bc[l] = c < NB ? G[c * PP + q + t] : 0.f;
-        }
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int i = 0; i < 6; ++i)
-#pragma unroll
-          for (int l = 0; l < 3; ++l) acc[i][l] = fmaf(ar[i], bc[l], acc[i][l]);
+          for (int j = 0; j < 4; ++j)
+            if (j0 + j <= i0 + i) G[(i0 + i) * PP + j0 + j] -= acc[i][j];
       }
-      __syncthreads();   // every read of this panel precedes the writes below
-#pragma unroll
-      for (int i = 0; i < 6; ++i)
-#pragma unroll
-        for (int l = 0; l < 3; ++l) {
-          const int r = base + ty + 16 * i, c = base + tx + 32 * l;
-          if (r < NB && c <= r) G[r * PP + c] -= acc[i][l];
-        }
     }
     __syncthreads();
   }
-  // inverse: four 32 x 32 diagonal inverses, warp w < 4 for block w, lane = column
-  if (warp < NB / 32) {
-    const int q = warp * 32;
-    float x[32];
+  // inverse of the eight 16 x 16 diagonal blocks: warp w, lane = column
+  if (warp < NB / PB) {
+    const int q = warp * PB, c = lane & (PB - 1);
+    float x[PB];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      float acc = (r == lane) ? 1.f : 0.f;
+    for (int r = 0; r < PB; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int t = 0; t < r; ++t) acc = fmaf(-G[(q + r) * PP + q + t], x[t], acc);
-      x[r] = acc / G[(q + r) * PP + q + r];
+    for (int t = 0; t < PB; ++t) {
+      x[t] *= dinv[q + t];
+#pragma unroll
+      for (int r = t + 1; r < PB; ++r) x[r] = fmaf(-G[(q + r) * PP + q + t], x[t], x[r]);
     }
+    if (lane < PB) {
 #pragma unroll
-    for (int r = 0; r < 32; ++r) X[(q + r) * PP + q + lane] = x[r];
+      for (int r = 0; r < PB; ++r) X[(q + r) * PP + q + c] = x[r];
+    }
   }
   __syncthreads();
-  // doubling: b = 32, 64.  X21 = -inv(G22) (G21 inv(G11)) for pairs of blocks
-  for (int b = 32; b < NB; b *= 2) {
-    for (int p0 = 0; p0 < NB; p0 += 2 * b) {
-      // S = G21 * inv(G11)  (b x b), placed at S[p0+b.., p0..]
-      smem_mm(S + (p0 + b) * PP + p0, G + (p0 + b) * PP + p0, X + p0 * PP + p0, b, b, b, 1.f, false);
+  // doubling: b = 16, 32, 64.  For each pair of b-blocks at p0:
+  //   S21 = G21 inv(G11)   (inv(G11) lower: K starts at the tile's first column)
+  //   X21 = -inv(G22) S21  (inv(G22) lower: K ends after the tile's last row)
+  for (int b = PB; b < NB; b *= 2) {
+    const int tb = b / 4, tpp = tb * tb, total = (NB / (2 * b)) * tpp;
+    for (int t = tid; t < total; t += NT) {
+      const int p0 = (t / tpp) * 2 * b, w = t % tpp;
+      const int m0 = (w / tb) * 4, n0 = (w % tb) * 4;
+      tile_mm(S + (p0 + b) * PP + p0, G + (p0 + b) * PP + p0, X + p0 * PP + p0, m0, n0, n0, b, 1.f);
     }
     __syncthreads();
-    for (int p0 = 0; p0 < NB; p0 += 2 * b) {
-      smem_mm(X + (p0 + b) * PP + p0, X + (p0 + b) * PP + p0 + b, S + (p0 + b) * PP + p0, b, b, b,
-              -1.f, true);
+    for (int t = tid; t < total; t += NT) {
+      const int p0 = (t / tpp) * 2 * b, w = t % tpp;
+      const int m0 = (w / tb) * 4, n0 = (w % tb) * 4;
+      tile_mm(X + (p0 + b) * PP + p0, X + (p0 + b) * PP + p0 + b, S + (p0 + b) * PP + p0, m0, n0, 0,
+              min(b, m0 + 4), -1.f);
     }
     __syncthreads();
   }
-  for (int idx = tid; idx < NB * NB; idx += blockDim.x) {
+  for (int idx = tid; idx < NB * NB; idx += NT) {
     const int r = idx / NB, c = idx - r * NB;
     C[(o + r) * kp + o + c] = (c <= r) ? G[r * PP + c] : 0.f;
     const float x = (c <= r) ? X[r * PP + c] : 0.f;
