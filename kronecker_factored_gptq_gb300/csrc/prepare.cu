@@ -32,99 +32,67 @@ namespace bakron {
 namespace {
 constexpr int NB = 128;
 
-struct GemmArgs {
-  const float* A; int64_t lda, sA;
-  const float* B; int64_t ldb, sB;
-  float* C; int64_t ldc, sC;
-  int64_t M, N, K;   // M, N multiples of 128 (rows clipped per batch by mclip)
-  float alpha, beta;
-  int transB;        // 0: B is K x N row-major; 1: B is N x K row-major
-  int lower_only;    // skip output tiles strictly above the diagonal
-  int klo_from_col;  // B lower triangular (B[k][n] = 0 for k < n): start K at the tile's first column
-  int khi_to_row;    // A lower triangular (A[m][k] = 0 for k > m): stop K after the tile's last row
-  int64_t mclip_base, mclip_step, mclip_total;  // per-batch row limit:
-  // rows available = min(M, mclip_total - (mclip_base + batch * mclip_step))
-};
-
-constexpr int BM = 128, BN = 128, BK = 16, PAD = 4;
-
-__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
-  __shared__ __align__(16) float As[BK][BM + PAD];
-  __shared__ __align__(16) float Bs[BK][BN + PAD];
-  const int64_t bz = blockIdx.z;
-  int64_t Mlim = g.M;
-  if (g.mclip_total > 0) {
-    const int64_t avail = g.mclip_total - (g.mclip_base + bz * g.mclip_step);
-    if (avail < Mlim) Mlim = avail;
-  }
-  const int64_t r0 = (int64_t)blockIdx.y * BM, c0 = (int64_t)blockIdx.x * BN;
-  if (r0 >= Mlim || c0 >= g.N) return;
-  if (g.lower_only && blockIdx.x > blockIdx.y) return;
-  const float* A = g.A + bz * g.sA;
-  const float* B = g.B + bz * g.sB;
-  float* C = g.C + bz * g.sC;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[8][8];
+// Panel of one Cholesky step, in place: P = A inv(G_kk)^T for the rows
+// [r0, r0 + 32 * gridDim.x) of the block column A (leading dimension lda),
+// inv the 128 x 128 inverse of the diagonal factor (row-major).  P
+// replaces A and is also written split (hi = tf32(P), lo = P - hi, same
+// offsets) for the tensor-core products.  One CTA per 32-row slab over all
+// 128 columns: a CTA reads only its own rows, all of them before it writes.
+constexpr int PR_ROWS = 32, PK = 16;
+__global__ void __launch_bounds__(256) panel_kernel(float* A, int64_t lda, const float* __restrict__ inv,
+                                                    float* Phi, float* Plo) {
+  __shared__ __align__(16) float As[PK][PR_ROWS + 4];
+  __shared__ __align__(16) float Bs[PK][NB + 4];
+  grid_dep_wait();   // inv and A come from the previous kernels
+  const int64_t r0 = (int64_t)blockIdx.x * PR_ROWS;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;   // columns 8 tx.., rows 2 ty..
+  float acc[2][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  const int lrow = tid >> 1, lk = (tid & 1) * 8;
-  int64_t kbeg = 0, kend = g.K;
-  if (g.klo_from_col) kbeg = c0 < kend ? c0 : kend;
-  if (g.khi_to_row && r0 + BM < kend) kend = r0 + BM;
-  for (int64_t k = kbeg; k < kend; k += BK) {
-    {
-      const float* pa = A + (r0 + lrow) * g.lda + k + lk;
+  for (int k = 0; k < NB; k += PK) {
+    if (tid < PR_ROWS * PK / 4) {
+      const int r = tid >> 2, kq = (tid & 3) * 4;
+      const float4 v = *reinterpret_cast<const float4*>(A + (r0 + r) * lda + k + kq);
+      As[kq + 0][r] = v.x; As[kq + 1][r] = v.y; As[kq + 2][r] = v.z; As[kq + 3][r] = v.w;
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) As[lk + u][lrow] = pa[u];
-      if (g.transB) {
-        const float* pb = B + (c0 + lrow) * g.ldb + k + lk;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) Bs[lk + u][lrow] = pb[u];
-      } else {
-        // 16 x 128 tile of B (row-major K x N): thread loads 8 consecutive n
-        const int kr = tid >> 4, nc = (tid & 15) * 8;
-        const float* pb = B + (k + kr) * g.ldb + c0 + nc;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) Bs[kr][nc + u] = pb[u];
-      }
+    for (int h = 0; h < 2; ++h) {
+      const int idx = tid + 256 * h, c = idx >> 2, kq = (idx & 3) * 4;
+      const float4 v = *reinterpret_cast<const float4*>(inv + c * NB + k + kq);
+      Bs[kq + 0][c] = v.x; Bs[kq + 1][c] = v.y; Bs[kq + 2][c] = v.z; Bs[kq + 3][c] = v.w;
     }
     __syncthreads();
 #pragma unroll
-    for (int kk = 0; kk < BK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    for (int kk = 0; kk < PK; ++kk) {
+      const float2 a2 = *reinterpret_cast<const float2*>(&As[kk][2 * ty]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][8 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][8 * tx + 4]);
+      const float av[2] = {a2.x, a2.y};
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
+  grid_dep_launch();
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t r = r0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+  for (int i = 0; i < 2; ++i) {
+    const int64_t g = (r0 + 2 * ty + i) * lda + 8 * tx;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int64_t c = c0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-      float* pc = C + r * g.ldc + c;
-      const float v = g.alpha * acc[i][j];
-      *pc = (g.beta == 0.f) ? v : fmaf(g.beta, *pc, v);
+    for (int h = 0; h < 2; ++h) {
+      float4 v = make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+      float4 hi, lo;
+      hi.x = tf32_round(v.x); hi.y = tf32_round(v.y); hi.z = tf32_round(v.z); hi.w = tf32_round(v.w);
+      lo.x = v.x - hi.x; lo.y = v.y - hi.y; lo.z = v.z - hi.z; lo.w = v.w - hi.w;
+      *reinterpret_cast<float4*>(A + g + 4 * h) = v;
+      *reinterpret_cast<float4*>(Phi + g + 4 * h) = hi;
+      *reinterpret_cast<float4*>(Plo + g + 4 * h) = lo;
     }
   }
-}
-
-cudaError_t gemm(const GemmArgs& g, int64_t batch, cudaStream_t s) {
-  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || batch <= 0) return cudaSuccess;
-  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)batch);
-  count_launch();
-  gemm_simt_kernel<<<grid, 256, 0, s>>>(g);
-  return cudaGetLastError();
 }
 
 // lambda = damp * mean(diag X), fp64 accumulation.
@@ -212,6 +180,7 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NT = 512;
   const int64_t o = kb * NB;
+  grid_dep_wait();   // the block was last updated by the previous kernels
 #pragma unroll 8
   for (int idx = tid; idx < NB * NB; idx += NT) {
     const int r = idx / NB, c = idx - r * NB;
@@ -349,6 +318,7 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
     }
     __syncthreads();
   }
+  grid_dep_launch();
   for (int idx = tid; idx < NB * NB; idx += NT) {
     const int r = idx / NB, c = idx - r * NB;
     C[(o + r) * kp + o + c] = (c <= r) ? G[r * PP + c] : 0.f;
@@ -361,22 +331,6 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
     const float ht = tf32_round(xt);
     GiThi[(o + r) * kp + o + c] = ht;
     GiTlo[(o + r) * kp + o + c] = xt - ht;
-  }
-}
-
-// dst = src (plain) and (dhi, dlo) = split(src), rows x cols
-__global__ void copy_split_kernel(const float* __restrict__ src, int64_t lds, float* __restrict__ dst,
-                                  float* __restrict__ dhi, float* __restrict__ dlo, int64_t ldd,
-                                  int64_t rows, int64_t cols) {
-  const int64_t total = rows * cols;
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = t / cols, c = t - r * cols;
-    const float v = src[r * lds + c];
-    const float h = tf32_round(v);
-    dst[r * ldd + c] = v;
-    dhi[r * ldd + c] = h;
-    dlo[r * ldd + c] = v - h;
   }
 }
 
@@ -495,9 +449,8 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   for (int64_t kb = 0; kb < nblk; ++kb) {
     float* inv_plain = invbuf[kb & 1];
     count_launch();
-    potrf_block_kernel<<<1, 512, kPotrfSmem, s>>>(a.C, a.Gihi, a.Gilo, a.GiThi, a.GiTlo, inv_plain,
-                                                  kp, kb, k, a.st, a.which);
-    BK_TRY(cudaGetLastError());
+    BK_TRY(launch_kernel(potrf_block_kernel, dim3(1), dim3(512), kPotrfSmem, s, kb > 0, a.C, a.Gihi,
+                         a.Gilo, a.GiThi, a.GiTlo, inv_plain, kp, kb, k, a.st, a.which));
     const int64_t rest = kp - (kb + 1) * NB;
     if (rest <= 0) break;
     cudaEvent_t ev_pot = a.ev[3 * kb], ev_urg = a.ev[3 * kb + 1], ev_def = a.ev[3 * kb + 2];
@@ -505,24 +458,18 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     if (kb >= 1) BK_TRY(cudaStreamWaitEvent(s, a.ev[3 * (kb - 1) + 2], 0));
     float* panel = a.C + (kb + 1) * NB * kp + kb * NB;
     const int64_t off = (kb + 1) * NB * kp + kb * NB;
-    // P = panel * inv(G_kk)^T (rows x 128, ld = NB) in Thi; rows [r0, r0 + rows)
-    auto panel_rows = [&](int64_t r0, int64_t rows, cudaStream_t str) -> cudaError_t {
-      GemmArgs g{};
-      g.A = panel + r0 * kp; g.lda = kp;
-      g.B = inv_plain; g.ldb = NB; g.transB = 1;
-      g.C = a.Thi + r0 * NB; g.ldc = NB;
-      g.M = rows; g.N = NB; g.K = NB; g.alpha = 1.f; g.beta = 0.f;
-      BK_TRY(gemm(g, 1, str));
+    // P = panel inv(G_kk)^T in place, plus its split, for rows [r0, r0 + rows)
+    auto panel_rows = [&](int64_t r0, int64_t rows, cudaStream_t str, bool pdl) -> cudaError_t {
       count_launch();
-      copy_split_kernel<<<grid_for(rows * NB), 256, 0, str>>>(
-          a.Thi + r0 * NB, NB, a.C + off + r0 * kp, a.Chi + off + r0 * kp, a.Clo + off + r0 * kp, kp,
-          rows, NB);
-      return cudaGetLastError();
+      return launch_kernel(panel_kernel, dim3((unsigned)(rows / PR_ROWS)), dim3(256), 0, str, pdl,
+                           panel + r0 * kp, kp, (const float*)inv_plain, a.Chi + off + r0 * kp,
+                           a.Clo + off + r0 * kp);
     };
     // trailing update C22 -= P P^T over syrk items [i0, i0 + n) (tensor cores)
-    auto syrk = [&](int i0, int n, cudaStream_t str) -> cudaError_t {
+    auto syrk = [&](int i0, int n, cudaStream_t str, bool pdl) -> cudaError_t {
       if (n <= 0) return cudaSuccess;
       PropArgs q{};
+      q.pdl = pdl;
       q.A_hi = a.Chi; q.A_lo = a.Clo; q.lda = kp; q.a_rows = kp;
       q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
       q.wt = a.C; q.ldw = kp;
@@ -532,15 +479,15 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
       return launch_prop_tc(q, str);
     };
     // urgent: row block kb+1 and tile (kb+1, kb+1) (the first syrk item)
-    BK_TRY(panel_rows(0, NB, s));
+    BK_TRY(panel_rows(0, NB, s, true));
     BK_TRY(cudaEventRecord(ev_urg, s));
-    BK_TRY(syrk(PI.syrk_off[kb], 1, s));
+    BK_TRY(syrk(PI.syrk_off[kb], 1, s, false));
     // deferred: the other panel rows and trailing tiles
     side_used = true;
     BK_TRY(cudaStreamWaitEvent(a.side, ev_pot, 0));
-    if (rest > NB) BK_TRY(panel_rows(NB, rest - NB, a.side));
+    if (rest > NB) BK_TRY(panel_rows(NB, rest - NB, a.side, false));
     BK_TRY(cudaStreamWaitEvent(a.side, ev_urg, 0));
-    BK_TRY(syrk(PI.syrk_off[kb] + 1, PI.syrk_n[kb] - 1, a.side));
+    BK_TRY(syrk(PI.syrk_off[kb] + 1, PI.syrk_n[kb] - 1, a.side, false));
     BK_TRY(cudaEventRecord(ev_def, a.side));
   }
   if (side_used) {
