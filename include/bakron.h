@@ -127,7 +127,10 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A,
  *   W      m x n     weights
  *   UA     n x n     U_A = L(A)^{-T} as written by bakron_prepare (upper;
  *                    the strictly lower triangle is ignored)
- *   UB     m x m     U_B = L(B)^{-T} (upper; likewise)
+ *   UB     m x m     U_B = L(B)^{-T} (upper; likewise); NULL means B = I:
+ *                    one-sided GPTQ with Hessian A for every row (the case
+ *                    the pages compare against), solved by a row path that
+ *                    sweeps column tiles with every row in parallel
  *   scale  m         per-row grid step s_i > 0
  *   qmin, qmax       code clamp; INT32_MIN / INT32_MAX = no clamp
  *   V      m x n     out: V = s_i * code

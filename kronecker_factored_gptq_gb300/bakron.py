@@ -195,7 +195,8 @@ def bakron_prepare(A, damp_A, B=None, damp_B=0.0, want_L=False, workspace=None, 
 
 def bakron_quantize(W, UA, UB, scale, qmin, qmax, want_preround=False, opts=None, workspace=None,
                     stream=None, out=None):
-    """Returns (V, codes, preround-or-None)."""
+    """Returns (V, codes, preround-or-None).  UB=None means B = I: one-sided
+    GPTQ with Hessian A for every row, solved by the library's row path."""
     torch = _torch()
     m, n = W.shape
     if out is None:
@@ -208,7 +209,8 @@ def bakron_quantize(W, UA, UB, scale, qmin, qmax, want_preround=False, opts=None
     ws = _ws(nb, workspace)
     st = lib().bakron_quantize(
         _dev(W, torch.float32, (m, n), "W"), m, n,
-        _dev(UA, torch.float32, (n, n), "UA"), _dev(UB, torch.float32, (m, m), "UB"),
+        _dev(UA, torch.float32, (n, n), "UA"),
+        None if UB is None else _dev(UB, torch.float32, (m, m), "UB"),
         _dev(scale, torch.float32, (m,), "scale"), int(qmin), int(qmax),
         _dev(V, torch.float32, (m, n), "V"), _dev(codes, torch.int8, (m, n), "codes"),
         None if pre is None else _dev(pre, torch.float32, (m, n), "preround"),

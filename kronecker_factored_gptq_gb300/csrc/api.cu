@@ -167,6 +167,69 @@ const Schedule& get_schedule(int M, int N) {
   return cache.emplace(key, std::move(s)).first->second;
 }
 
+// Schedule of the one-sided (B = I) solve: divide and conquer over column
+// tiles.  rows_rec(J0, J1) is a leaf (column tile J0 of every row tile) if
+// J1 - J0 == 1; otherwise rows_rec(J0, Jm), the propagation
+// W~[I, J'] -= sum_{J in [J0, Jm)} E[I, J] U_A[J, J'] for J' in [Jm, J1),
+// rows_rec(Jm, J1).  The propagation is split by target column into chunks
+// [Jm, Jm+1), [Jm+1, Jm+2), [Jm+2, Jm+4), ...: the first (what the next
+// leaf needs) on the critical stream, the others deferred.
+struct RowsOp {
+  int kind;            // 0 = leaf, 1 = propagation
+  int J, depth;        // leaf column tile; recursion depth
+  int chunk0, nchunks;
+};
+
+struct RowsSchedule {
+  int M = 0, N = 0, max_depth = 0;
+  std::vector<WorkItem> items;
+  std::vector<RowsOp> ops;
+  std::vector<Chunk> chunks;   // stage-2 items only (off, n, maxk, dlo, dhi, flops)
+};
+
+void build_rows_rec(RowsSchedule& s, int J0, int J1, int depth) {
+  if (J1 - J0 <= 1) {
+    s.ops.push_back(RowsOp{0, J0, depth, 0, 0});
+    return;
+  }
+  const int Jm = (J0 + J1) / 2;
+  build_rows_rec(s, J0, Jm, depth + 1);
+  RowsOp op{1, 0, depth, (int)s.chunks.size(), 0};
+  s.max_depth = std::max(s.max_depth, depth);
+  for (int lo = Jm, width = 1; lo < J1;) {
+    const int hi = std::min(J1, lo + width);
+    Chunk c{};
+    c.dlo = lo;
+    c.dhi = hi;
+    c.off = (int)s.items.size();
+    for (int Jp = lo; Jp < hi; ++Jp)
+      for (int I = 0; I < s.M; ++I) s.items.push_back(WorkItem{I, Jp, J0, Jm});
+    c.n = (int)s.items.size() - c.off;
+    c.maxk = Jm - J0;
+    c.flops = 2.0 * T * T * T * (double)(Jm - J0) * c.n;
+    s.chunks.push_back(c);
+    lo = hi;
+    if (lo > Jm + 1) width *= 2;
+  }
+  op.nchunks = (int)s.chunks.size() - op.chunk0;
+  s.ops.push_back(op);
+  build_rows_rec(s, Jm, J1, depth + 1);
+}
+
+const RowsSchedule& get_rows_schedule(int M, int N) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, RowsSchedule> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_pair(M, N);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  RowsSchedule s;
+  s.M = M;
+  s.N = N;
+  build_rows_rec(s, 0, N, 0);
+  return cache.emplace(key, std::move(s)).first->second;
+}
+
 constexpr int kMaxDepth = 24;
 
 struct QLayout {
@@ -188,7 +251,8 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
   const size_t f = sizeof(float);
   L.status = take(256);
-  L.sched = take(sizeof(WorkItem) * (s.items.size() + 1));
+  const RowsSchedule& rs = get_rows_schedule((int)L.M, (int)L.N);
+  L.sched = take(sizeof(WorkItem) * (std::max(s.items.size(), rs.items.size()) + 1));
   L.scale = take(f * L.Mp);
   L.wt = take(f * L.Mp * L.Np);
   L.ehi = take(f * L.Mp * L.Np);
@@ -410,6 +474,116 @@ struct PhaseTimer {
 
 bool sizes_ok(int64_t m, int64_t n) { return m >= 1 && n >= 1 && m <= (1 << 20) && n <= (1 << 20); }
 
+// The one-sided solve (U_B = I): see RowsSchedule.  Arguments validated by
+// bakron_quantize; the workspace layout is the two-sided one (its Y^T and
+// U_B^T regions stay unused).
+bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* UA, const float* scale,
+                            int qmin, int qmax, float* V, int8_t* codes, float* preround,
+                            const bakron_opts& o, void* ws, cudaStream_t s) {
+  const QLayout L = quantize_layout(m, n);
+  const RowsSchedule& sch = get_rows_schedule((int)L.M, (int)L.N);
+  SolveStreams* ss = nullptr;
+  TRY_CUDA(solve_streams(&ss));
+  std::lock_guard<std::mutex> slk(ss->mu);
+  size_t nev = 0;
+  auto next_event = [&](cudaEvent_t* ev) { return pool_event(ss, nev++, ev); };
+  char* base = (char*)ws;
+  DevStatus* st = (DevStatus*)(base + L.status);
+  WorkItem* items = (WorkItem*)(base + L.sched);
+  float* sp = (float*)(base + L.scale);
+  float* wt = (float*)(base + L.wt);
+  float* ehi = (float*)(base + L.ehi);
+  float* elo = (float*)(base + L.elo);
+  float* lathi = (float*)(base + L.lathi);
+  float* latlo = (float*)(base + L.latlo);
+  if (o.times) std::memset(o.times, 0, sizeof(*o.times));
+  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+  if (!sch.items.empty())
+    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
+                                  cudaMemcpyHostToDevice, s));
+  cudaStream_t cs = ss->crit;
+  {
+    cudaEvent_t ev;
+    TRY_CUDA(next_event(&ev));
+    TRY_CUDA(cudaEventRecord(ev, s));
+    TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+  }
+  PhaseTimer pt(o.times, cs);
+  {
+    cudaEvent_t ev = pt.begin();
+    TRY_CUDA(launch_check_finite(scale, m, st, cs));
+    TRY_CUDA(launch_pad_scale(scale, m, sp, L.Mp, cs));
+    TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
+    TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
+    pt.end(3, ev);
+  }
+  LeafArgs la{};
+  la.wt = wt; la.ldw = L.Np;
+  la.lat_hi = lathi; la.lat_lo = latlo; la.lda = L.Np;
+  la.scale = sp;
+  la.e_hi = ehi; la.e_lo = elo;
+  la.round_lo = 1;
+  la.V = V; la.codes = codes; la.preround = preround;
+  la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
+  la.st = st;
+  std::vector<std::vector<cudaEvent_t>> waits((size_t)L.N + 1);
+  for (const RowsOp& op : sch.ops) {
+    if (op.kind == 0) {
+      for (cudaEvent_t ev : waits[op.J]) TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+      la.D = op.J;
+      la.I0 = 0;
+      la.pdl = op.J > 0;   // the first leaf reads the factor the kernel before it wrote
+      cudaEvent_t ev = pt.begin();
+      TRY_CUDA(launch_rows_leaf(la, (int)L.M, cs));
+      pt.end(0, ev);
+      continue;
+    }
+    PropArgs p2{};
+    p2.A_hi = ehi; p2.A_lo = elo; p2.lda = L.Np; p2.a_rows = L.Mp;
+    p2.B_hi = lathi; p2.B_lo = latlo; p2.ldb = L.Np; p2.b_rows = L.Np;
+    p2.wt = wt; p2.ldw = L.Np;
+    p2.stage = 2;
+    p2.st = st;
+    for (int c = 0; c < op.nchunks; ++c) {
+      const Chunk& ch = sch.chunks[op.chunk0 + c];
+      if (o.times) o.times->prop_flops += ch.flops;
+      const bool urgent = c == 0;
+      cudaStream_t cstr = urgent ? cs : ss->side[op.depth];
+      if (c == 1) {
+        // the deferred chunks start once the leaves they read have finished
+        cudaEvent_t ev;
+        TRY_CUDA(next_event(&ev));
+        TRY_CUDA(cudaEventRecord(ev, cs));
+        TRY_CUDA(cudaStreamWaitEvent(cstr, ev, 0));
+      }
+      PhaseTimer side_pt(o.times, cstr);
+      PhaseTimer* tm = urgent ? &pt : &side_pt;
+      p2.items = items + ch.off; p2.n_items = ch.n; p2.max_k = ch.maxk;
+      p2.pdl = urgent;
+      cudaEvent_t ev = tm->begin();
+      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p2, cstr) : launch_prop_simt(p2, cstr));
+      tm->end(2, ev);
+      if (!urgent) {
+        pt.adopt(side_pt);
+        cudaEvent_t done;
+        TRY_CUDA(next_event(&done));
+        TRY_CUDA(cudaEventRecord(done, cstr));
+        for (int d = ch.dlo; d < ch.dhi; ++d) waits[d].push_back(done);
+      }
+    }
+  }
+  {
+    cudaEvent_t ev;
+    TRY_CUDA(next_event(&ev));
+    TRY_CUDA(cudaEventRecord(ev, cs));
+    TRY_CUDA(cudaStreamWaitEvent(s, ev, 0));
+  }
+  DevStatus h{};
+  bakron_status r = finish(s, st, &h);
+  pt.collect();
+  return r;
+}
+
 }  // namespace
 }  // namespace bakron
 
@@ -549,11 +723,14 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   bakron_default_opts(&o);
   if (opts_in) o = *opts_in;
   if (!valid_opts(o)) return BAKRON_ERR_INVALID_ARG;
-  if (!W || !UA || !UB || !scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
+  if (!W || !UA || !scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
   if (!sizes_ok(m, n) || qmin > qmax) return BAKRON_ERR_INVALID_ARG;
   const QLayout L = quantize_layout(m, n);
   if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
   if (o.use_3xtf32 && !prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
+  if (!UB)
+    return quantize_rows(W, m, n, UA, scale, qmin, qmax, V, codes, preround, o, ws,
+                         (cudaStream_t)stream);
   const Schedule& sch = get_schedule((int)L.M, (int)L.N);
   cudaStream_t s = (cudaStream_t)stream;
   SolveStreams* ss = nullptr;

@@ -119,6 +119,8 @@ cudaError_t launch_pad_scale(const float* scale, int64_t m, float* sp, int64_t m
                              cudaStream_t s);
 cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cudaStream_t s);
 cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s);
+// one-sided (B = I) leaf: column tile a.D of every row tile
+cudaError_t launch_rows_leaf(const LeafArgs& a, int n_row_tiles, cudaStream_t s);
 cudaError_t launch_prop_simt(const PropArgs& p, cudaStream_t s);
 cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s);
 bool prop_tc_supported();

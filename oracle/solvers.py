@@ -58,7 +58,7 @@ def _as64(*arrs):
     return [np.array(a, dtype=np.float64, copy=True) for a in arrs]
 
 
-def gptq_rows(W, UA, s, qmin=None, qmax=None):
+def gptq_rows(W, UA, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
     """Textbook one-sided GPTQ (Hessian A (x) I_m): every row independently.
 
     ``UA`` is the upper Cholesky factor of ``A^{-1}``.  Columns are processed
@@ -73,15 +73,17 @@ def gptq_rows(W, UA, s, qmin=None, qmax=None):
     C = np.zeros((m, n))
     P = np.zeros((m, n))
     E = np.zeros((m, n))
+    n_over = 0
     for j in range(n):
         x = X[:, j].copy()
         P[:, j] = x
-        c = quantize_codes(x, s, qmin, qmax)
+        c, o = _decide(x, s, qmin, qmax, None if guide is None else guide[:, j], guide_tol)
+        n_over += o
         C[:, j] = c
         err = (x - s * c) / UA[j, j]
         E[:, j] = err
         X[:, j + 1:] -= np.outer(err, UA[j, j + 1:])
-    return SolveResult(C, P, s[:, None] * C, E)
+    return SolveResult(C, P, s[:, None] * C, E, n_over)
 
 
 def naive_vec_gptq(W, s, qmin=None, qmax=None, A=None, B=None, UA=None, UB=None,

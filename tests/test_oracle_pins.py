@@ -201,6 +201,35 @@ def test_b_identity_is_rowwise_gptq(m, n):
     np.testing.assert_array_equal(full.codes, one.codes)
 
 
+def test_gptq_rows_guided_by_its_own_codes_is_unchanged():
+    # the guide only decides near ties, and agrees with the decision there
+    p = problem(9, 13, seed=12)
+    one = O.gptq_rows(p["W"], p["UA"], p["s"], p["qmin"], p["qmax"])
+    g = O.gptq_rows(p["W"], p["UA"], p["s"], p["qmin"], p["qmax"], guide=one.codes)
+    np.testing.assert_array_equal(g.codes, one.codes)
+    np.testing.assert_array_equal(g.preround, one.preround)
+    assert g.overrides == 0
+
+
+def test_gptq_rows_guide_takes_a_near_tie():
+    # one entry placed exactly on a rounding boundary (x / s = k + 1/2 in
+    # column 0, which no update reaches): round half to even takes one side,
+    # a guide with the other code is followed there, and the changed error
+    # then moves every later entry of that row only
+    p = problem(4, 6, seed=13)
+    W = p["W"].copy()
+    s = p["s"]
+    W[2, 0] = 0.5 * s[2]
+    one = O.gptq_rows(W, p["UA"], s, p["qmin"], p["qmax"])
+    assert one.codes[2, 0] == 0.0
+    guide = one.codes.copy()
+    guide[2, 0] = 1.0
+    g = O.gptq_rows(W, p["UA"], s, p["qmin"], p["qmax"], guide=guide)
+    assert g.codes[2, 0] == 1.0 and g.overrides >= 1
+    np.testing.assert_array_equal(np.delete(g.codes, 2, axis=0), np.delete(one.codes, 2, axis=0))
+    assert not np.allclose(g.preround[2, 1:], one.preround[2, 1:])
+
+
 def test_diagonal_factors_give_rtn():
     rng = np.random.default_rng(3)
     m, n = 9, 11
