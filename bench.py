@@ -408,7 +408,7 @@ def run_ours(args, world, rank, local):
     # One-sided GPTQ (B = I) on the same W and A: the comparison the pages
     # quote (0.059 s for 8192 x 8192 on their GPU); context, not the metric.
     one_sided = None
-    if not args.no_one_sided:
+    if not args.no_context:
         UA1 = torch.empty((n, n), dtype=torch.float32, device=dev)
         ws_p1 = torch.empty(kb.prepare_workspace_size(n, 0), dtype=torch.uint8, device=dev)
         ts = []
@@ -429,6 +429,33 @@ def run_ours(args, world, rank, local):
         one_sided = {"solve_s": solve1 / 1e3, "prepare_A_s": prep1 / 1e3,
                      "solve_tflops_mn2": float(m) * n * n / (solve1 / 1e3) / 1e12,
                      "pages_rtx_pro_6000_s": 0.059, "steps": len(ts)}
+
+    # Kronecker-factor accumulation (K-FAC and one-step Shampoo) from a stream
+    # of 16384 samples of both sides: the step before the solver; context.
+    factors = None
+    if not args.no_context:
+        Ns = 16384
+        Xs, Gs = WL.sample_stream(Ns, n, m, seed=args.seed)
+        dXs, dGs = torch.from_numpy(Xs).to(dev), torch.from_numpy(Gs).to(dev)
+        del Xs, Gs
+        fws = torch.empty(kb.factors_workspace_size(Ns, n, m), dtype=torch.uint8, device=dev)
+        factors = {"samples": Ns}
+        for name, md in (("kfac", kb.FACTORS_KFAC), ("shampoo", kb.FACTORS_SHAMPOO)):
+            ts = []
+            for k in range(args.warmup + 3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                kb.bakron_factors(dXs, dGs, mode=md, workspace=fws)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if k >= args.warmup:
+                    ts.append(e0.elapsed_time(e1))
+            t = statistics.median(ts) / 1e3
+            # lower 128-tiles of both Gram matrices, 2 flops per multiply-add
+            fl_f = 2.0 * Ns * (n * (n + 128) / 2 + m * (m + 128) / 2)
+            factors[name + "_s"] = t
+            factors[name + "_tflops"] = fl_f / t / 1e12
+        del dXs, dGs, fws
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -464,6 +491,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "one_sided_gptq": one_sided,
+        "factor_accumulation": factors,
         "context": {"pages_rtx_pro_6000_solve_s": 1.839, "pages_yaqa_solve_s": 110.379,
                     "pages_gptq_solve_s": 0.059},
     }
@@ -483,8 +511,8 @@ def main():
     ap.add_argument("--simt", action="store_true", help="fp32 FMA propagation instead of tcgen05")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-one-sided", action="store_true",
-                    help="skip the one-sided (B = I) timing reported as context")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the context timings (one-sided GPTQ, factor accumulation)")
     args = ap.parse_args()
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; the other ranks exit at

@@ -166,6 +166,28 @@ bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n,
                                        const bakron_opts* opts, void* ws, size_t ws_bytes,
                                        void* stream);
 
+/* Kronecker factors of a linear layer's Hessian from N samples (the
+ * Hessians section of the summary page: the layer Hessian E[a a^T (x) g g^T]
+ * factorised either with a K-FAC-style independence assumption or with one
+ * Shampoo-style power-iteration step of the best Kronecker approximation,
+ * started from the identity).  Row t of X (N x n) is the input activation
+ * a_t, row t of G (N x m) the gradient g_t of the loss at the layer output.
+ *   BAKRON_FACTORS_KFAC:    A = (1/N) sum_t a_t a_t^T,
+ *                           B = (1/N) sum_t g_t g_t^T;
+ *   BAKRON_FACTORS_SHAMPOO: A = (1/N) sum_t |g_t|^2 a_t a_t^T,
+ *                           B = (1/N) sum_t |a_t|^2 g_t g_t^T.
+ * A (n x n) and B (m x m) are full symmetric matrices, the undamped inputs
+ * of bakron_prepare.  Either output may be NULL (then its side's samples may
+ * be NULL too, except that Shampoo weights need both X and G).  The sums run
+ * on the tensor cores with a 3xTF32 split and fp32 accumulation.  ws: device
+ * workspace of bakron_factors_workspace_size(N, n, m) bytes (n or m may be 0
+ * when that side is not used). */
+enum { BAKRON_FACTORS_KFAC = 0, BAKRON_FACTORS_SHAMPOO = 1 };
+bakron_status bakron_factors_workspace_size(int64_t N, int64_t n, int64_t m, size_t* bytes);
+bakron_status bakron_factors(const float* X, int64_t N, int64_t n, const float* G, int64_t m,
+                             int mode, float* A, float* B, void* ws, size_t ws_bytes,
+                             void* stream);
+
 /* bakron_quantize for callers that cannot allocate device memory, such as
  * code embedded in a host application that owns all device memory through
  * its own pool and forbids cudaMalloc/cudaFree (they synchronise the device

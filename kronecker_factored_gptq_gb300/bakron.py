@@ -24,7 +24,9 @@ INT32_MAX = (1 << 31) - 1
 EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bakron_kernel_launches",
            "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
            "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
-           "bakron_quantize_noalloc"]
+           "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors"]
+FACTORS_KFAC = 0
+FACTORS_SHAMPOO = 1
 
 
 class PhaseTimes(ctypes.Structure):
@@ -77,9 +79,11 @@ def lib():
                                            ctypes.POINTER(Opts), vp, sz, vp]
     L.bakron_quantize_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                           vp, vp, vp]
+    L.bakron_factors_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
+    L.bakron_factors.argtypes = [vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, sz, vp]
     for f in ("bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
               "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
-              "bakron_quantize_noalloc"):
+              "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors"):
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
@@ -268,6 +272,39 @@ def bakron_quantize_noalloc(W, UA, UB, scale, qmin, qmax, out=None, stream=None)
         _stream(stream))
     _check(st, "bakron_quantize_noalloc")
     return V, codes
+
+
+def factors_workspace_size(N, n, m):
+    size = ctypes.c_size_t(0)
+    _check(lib().bakron_factors_workspace_size(N, n, m, ctypes.byref(size)),
+           "bakron_factors_workspace_size")
+    return size.value
+
+
+def bakron_factors(X=None, G=None, mode=FACTORS_KFAC, want_A=True, want_B=True, workspace=None,
+                   stream=None):
+    """Kronecker factors (A, B) from samples: rows of X (N x n) are input
+    activations, rows of G (N x m) output gradients.  mode FACTORS_KFAC or
+    FACTORS_SHAMPOO; an unwanted factor comes back as None."""
+    torch = _torch()
+    ref = X if X is not None else G
+    N = ref.shape[0]
+    n = 0 if X is None else X.shape[1]
+    m = 0 if G is None else G.shape[1]
+    A = torch.empty((n, n), dtype=torch.float32, device=ref.device) if (want_A and X is not None) else None
+    B = torch.empty((m, m), dtype=torch.float32, device=ref.device) if (want_B and G is not None) else None
+    size = ctypes.c_size_t(0)
+    _check(lib().bakron_factors_workspace_size(N, n, m, ctypes.byref(size)),
+           "bakron_factors_workspace_size")
+    ws = _ws(size.value, workspace)
+    st = lib().bakron_factors(
+        None if X is None else _dev(X, torch.float32, (N, n), "X"), N, n,
+        None if G is None else _dev(G, torch.float32, (N, m), "G"), m, int(mode),
+        None if A is None else _dev(A, torch.float32, (n, n), "A"),
+        None if B is None else _dev(B, torch.float32, (m, m), "B"),
+        ctypes.c_void_p(ws.data_ptr()), size.value, _stream(stream))
+    _check(st, "bakron_factors")
+    return A, B
 
 
 class Solver:

@@ -63,7 +63,8 @@ struct PropArgs {
   float* out_hi; float* out_lo; int64_t ldo;   // stage 1: Y^T split
   float* wt; int64_t ldw;                      // stage 2: W~ -= C
   const WorkItem* items; int n_items;
-  int stage;  // 1: out = split(alpha C) [and tr = split(alpha C)^T]; 2: wt -= C
+  int stage;  // 1: out = split(alpha C) [and tr = split(alpha C)^T]; 2: wt -= C;
+              // 3: wt = alpha C (tensor cores only)
   int max_k;  // longest K range of the items, in tiles
   float alpha;                       // stage 1 scale (0 means 1)
   float* tr_hi; float* tr_lo; int64_t ldt;  // stage 1, nullable: transposed split store

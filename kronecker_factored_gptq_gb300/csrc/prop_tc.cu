@@ -31,7 +31,8 @@
 //     accumulators, two of each);
 //   warps 4-7: epilogue, TMEM -> registers (warp 4 + q owns TMEM lanes
 //     32q..32q+31, i.e. output rows) -> running fp32 sums -> global: stage 1
-//     writes C split into (hi, lo), stage 2 subtracts C from W~.
+//     writes C split into (hi, lo), stage 2 subtracts C from W~, stage 3
+//     writes alpha C plainly (the factor accumulation).
 // Every mbarrier wait is bounded (clock64 budget); on expiry the CTA records
 // BAKRON_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs (with a
 // bound again), frees TMEM and returns.
@@ -296,12 +297,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (ok) {
       const int row = q * 32 + lane;
-      if (p.stage == 1) {
+      if (p.stage != 2) {
         if (p.alpha != 0.f && p.alpha != 1.f) {
 #pragma unroll
           for (int t = 0; t < BN; ++t) acc[t] *= p.alpha;
         }
-        if (p.tr_hi) {
+        if (p.stage == 1 && p.tr_hi) {
           // transposed split store: lane = output row, so for each column the
           // 32 lanes of a warp write 32 consecutive floats
           const int64_t tcol = (int64_t)it.r * BM + row;
@@ -338,6 +339,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           h.w = tf32_round(v.w); l.w = tf32_round(v.w - h.w);
           *reinterpret_cast<float4*>(p.out_hi + (grow0 + rr) * p.ldo + gcol) = h;
           *reinterpret_cast<float4*>(p.out_lo + (grow0 + rr) * p.ldo + gcol) = l;
+        }
+      } else if (p.stage == 3) {
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * SPITCH + 4 * lane);
+          *reinterpret_cast<float4*>(p.wt + (grow0 + rr) * p.ldw + gcol) = v;
         }
       } else {
         // atomic: propagations of different recursion depths may update the

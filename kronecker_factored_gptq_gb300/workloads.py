@@ -175,3 +175,15 @@ CONFIGS = {
 
 def load(name, seed=0, device=None):
     return CONFIGS[name](seed=seed, device=device)
+
+
+def sample_stream(N, n, m, seed=0):
+    """N samples of a layer's input activations (N x n, channel scales drawn
+    log-normal(0, 1) as in the 1024 x 1024 workload) and output gradients
+    (N x m, standard normal), fp32: the inputs of the Kronecker-factor
+    accumulation."""
+    rng = _rng(seed, 20)
+    X = rng.standard_normal((N, n), dtype=np.float32)
+    X *= np.exp(_rng(seed, 21).standard_normal(n)).astype(np.float32)[None, :]
+    G = _rng(seed, 22).standard_normal((N, m), dtype=np.float32)
+    return X, G

@@ -21,6 +21,9 @@ Birnick & Saab):
   vec order) and BaKron (anti-diagonal parallelism + divide and conquer over
   the anti-diagonal dimension); plus textbook one-sided GPTQ (Hessian A (x) I).
   Theorem 3.2 on the summary page states the four give the same output.
+* ``hessians``  - K-FAC and one-step Shampoo Kronecker factors of a layer
+  Hessian from activation and gradient samples (summary page, section on the
+  Hessians).
 * ``checks``    - the output certificate, the proxy loss
   ||L(B)(V-W)L(A)^T||_F^2 and the Corollary 3.4 bound 1/4 tr(A) tr(B).
 
@@ -39,6 +42,7 @@ from .solvers import (SolveResult, gptq_rows, naive_vec_gptq, antidiag,
                       recursive_vec, bakron, bakron_tiled_order_check)
 from .checks import (certificate, proxy_loss, cor34_bound, cor34_tight_bound,
                      compare_codes)
+from .hessians import kfac_factors, shampoo_factors
 
 __all__ = [
     "damp", "rev_cholesky", "update_factor", "prepare", "lower_from_update",
@@ -46,5 +50,5 @@ __all__ = [
     "gptq_rows", "naive_vec_gptq", "antidiag", "recursive_vec", "bakron",
     "bakron_tiled_order_check",
     "certificate", "proxy_loss", "cor34_bound", "cor34_tight_bound",
-    "compare_codes", "SolveResult",
+    "compare_codes", "SolveResult", "kfac_factors", "shampoo_factors",
 ]

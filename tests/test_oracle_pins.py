@@ -339,3 +339,55 @@ def test_guide_only_acts_on_near_ties():
     # a guide that disagrees everywhere changes nothing away from near ties
     g2 = O.antidiag(*args, guide=r.codes + 1, guide_tol=1e-9)
     np.testing.assert_array_equal(g2.codes, r.codes)
+
+
+# ------------------------------------------------- Hessian factor accumulation
+
+def _fisher_terms(X, G):
+    """Per-sample Hessians vec(g a^T) vec(g a^T)^T with the column-major vec
+    (entry (i, j) of the m x n gradient at index i + m j), written out."""
+    N, n = X.shape
+    m = G.shape[1]
+    F = np.zeros((N, m * n, m * n))
+    for t in range(N):
+        v = np.outer(G[t], X[t]).reshape(-1, order="F")
+        F[t] = np.outer(v, v)
+    return F
+
+
+def test_kfac_factors_brute_force_and_single_sample_kronecker():
+    rng = np.random.default_rng(30)
+    X = rng.standard_normal((7, 4))
+    G = rng.standard_normal((7, 3))
+    A, B = O.kfac_factors(X, G)
+    A_bf = sum(np.outer(x, x) for x in X) / 7
+    B_bf = sum(np.outer(g, g) for g in G) / 7
+    np.testing.assert_allclose(A, A_bf, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(B, B_bf, rtol=1e-13, atol=1e-14)
+    # one sample: the Kronecker product is the exact per-sample Hessian
+    A1, B1 = O.kfac_factors(X[:1], G[:1])
+    np.testing.assert_allclose(np.kron(A1, B1), _fisher_terms(X[:1], G[:1])[0], atol=1e-13)
+    assert O.kfac_factors(X, None)[1] is None and O.kfac_factors(None, G)[0] is None
+
+
+def test_shampoo_factors_are_partial_traces_of_the_fisher():
+    # One power step from the identity: A = tr_B(E[F]) and B = tr_A(E[F]),
+    # the partial traces of the explicit mn x mn expected Hessian.
+    rng = np.random.default_rng(31)
+    X = rng.standard_normal((6, 3))
+    G = rng.standard_normal((6, 4))
+    A, B = O.shampoo_factors(X, G)
+    F = _fisher_terms(X, G).mean(axis=0).reshape(3, 4, 3, 4)   # [j, i, j', i']
+    np.testing.assert_allclose(A, np.einsum("jiki->jk", F), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(B, np.einsum("jijk->ik", F), rtol=1e-12, atol=1e-13)
+
+
+def test_shampoo_with_equal_norms_is_scaled_kfac():
+    rng = np.random.default_rng(32)
+    X = rng.standard_normal((9, 5))
+    G = rng.standard_normal((9, 4))
+    G /= np.linalg.norm(G, axis=1, keepdims=True) / 1.5   # every |g_t| = 1.5
+    A, _ = O.shampoo_factors(X, G)
+    Ak, _ = O.kfac_factors(X, G)
+    np.testing.assert_allclose(A, 2.25 * Ak, rtol=1e-12)
+    assert np.isclose(np.trace(Ak), np.mean(np.sum(X * X, axis=1)))
