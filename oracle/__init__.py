@@ -12,9 +12,9 @@ Birnick & Saab):
 * ``factors``   - damping, RevCholesky ``A = L^T L`` (L lower) and the update
   factor ``U = L^{-T}`` (summary page "FastKron: Efficient Quantization with
   Kronecker-Factored Hessians", Corollary 3.4 names ``L(A) = RevCholesky(A)``).
-* ``quantizer`` - the per-row symmetric b-bit base quantizer and the near-tie
-  rule used by every comparison (abstract: BaKron is modular in the base
-  quantizer).
+* ``quantizer`` - the base quantizers (per-row or per-column-group,
+  symmetric or asymmetric b-bit grids) and the near-tie rule used by every
+  comparison (abstract: BaKron is modular in the base quantizer).
 * ``solvers``   - GPTQ on vec(W) with Hessian A (x) B written out four ways, in
   the order the summary page derives them (section 3): naive (explicit
   mn x mn Hessian), anti-diagonal, recursive (divide and conquer over the
@@ -37,7 +37,8 @@ Corollary 3.4 inequality, cross-formulation equality).
 """
 
 from .factors import damp, rev_cholesky, update_factor, prepare, lower_from_update
-from .quantizer import row_scale, quantize_codes, near_tie
+from .quantizer import (row_scale, quantize_codes, near_tie, Grid, symmetric_grid,
+                        asymmetric_grid)
 from .solvers import (SolveResult, gptq_rows, naive_vec_gptq, antidiag,
                       recursive_vec, bakron, bakron_tiled_order_check)
 from .checks import (certificate, proxy_loss, cor34_bound, cor34_tight_bound,
@@ -46,7 +47,7 @@ from .hessians import kfac_factors, shampoo_factors
 
 __all__ = [
     "damp", "rev_cholesky", "update_factor", "prepare", "lower_from_update",
-    "row_scale", "quantize_codes", "near_tie",
+    "row_scale", "quantize_codes", "near_tie", "Grid", "symmetric_grid", "asymmetric_grid",
     "gptq_rows", "naive_vec_gptq", "antidiag", "recursive_vec", "bakron",
     "bakron_tiled_order_check",
     "certificate", "proxy_loss", "cor34_bound", "cor34_tight_bound",

@@ -23,7 +23,7 @@ unclamped unit-step round-to-nearest quantizer it is at most
 import numpy as np
 
 from .factors import lower_from_update
-from .quantizer import quantize_codes, near_tie
+from .quantizer import Grid, quantize_codes, near_tie
 
 
 def proxy_loss(W, V, LA, LB):
@@ -56,15 +56,15 @@ def certificate(W, V, codes, UA, UB, s, qmin=None, qmax=None, tol=1e-4,
     W = np.asarray(W, np.float64)
     V = np.asarray(V, np.float64)
     codes = np.asarray(codes, np.float64)
-    s = np.asarray(s, np.float64)
     m, n = W.shape
+    g = Grid.of(s, qmin, qmax, m, n)
     LA = lower_from_update(UA)
     LB = lower_from_update(UB)
     E = LB @ (W - V) @ LA.T
     wt = V + E / np.outer(np.diag(LB), np.diag(LA))
-    replay = quantize_codes(wt, s[:, None], qmin, qmax)
+    replay = quantize_codes(wt, g.S, g.qmin, g.qmax, g.Z)
     mism = replay != codes
-    nt = near_tie(wt, s[:, None], qmin, qmax, tol)
+    nt = near_tie(wt, g.S, g.qmin, g.qmax, tol, g.Z)
     n_m = int(np.count_nonzero(mism))
     bad = int(np.count_nonzero(mism & ~nt))
     return {
@@ -86,7 +86,8 @@ def compare_codes(codes_test, codes_ref, preround_ref, s, qmin=None, qmax=None,
     a = np.asarray(codes_test, np.float64)
     b = np.asarray(codes_ref, np.float64)
     diff = a != b
-    nt = near_tie(preround_ref, np.asarray(s, np.float64)[:, None], qmin, qmax, tol)
+    g = Grid.of(s, qmin, qmax, a.shape[0], a.shape[1])
+    nt = near_tie(preround_ref, g.S, g.qmin, g.qmax, tol, g.Z)
     n_d = int(np.count_nonzero(diff))
     bad = int(np.count_nonzero(diff & ~nt))
     return {"diff": n_d, "bad": bad,

@@ -21,14 +21,17 @@ Kronecker-Factored Hessians", problem set-up and section 3):
   updates the entries to its bottom-right).
 
 Every solver returns a :class:`SolveResult`; ``preround`` holds the value each
-entry had when it was rounded.  ``guide``/``guide_tol`` (optional, every
+entry had when it was rounded.  ``s`` is either a per-row scale vector (with
+``qmin``/``qmax``; the workloads' symmetric per-row grid) or a
+:class:`quantizer.Grid` (per-entry scale and zero point, e.g. column groups or
+an asymmetric grid; then ``qmin``/``qmax`` are ignored).  ``guide``/``guide_tol`` (optional, every
 solver): where the solver's own pre-rounding value is a near tie (see
 ``quantizer.near_tie``), take the guide's code instead of its own decision.
 """
 
 import numpy as np
 
-from .quantizer import quantize_codes, near_tie
+from .quantizer import Grid, quantize_codes, near_tie
 
 
 class SolveResult:
@@ -40,18 +43,6 @@ class SolveResult:
         self.V = V
         self.E = E
         self.overrides = overrides
-
-
-def _decide(x, s, qmin, qmax, guide, guide_tol):
-    c = quantize_codes(x, s, qmin, qmax)
-    n_over = 0
-    if guide is not None:
-        nt = near_tie(x, s, qmin, qmax, guide_tol)
-        g = np.asarray(guide, dtype=np.float64)
-        over = nt & (g != c)
-        n_over = int(np.count_nonzero(over))
-        c = np.where(nt, g, c)
-    return c, n_over
 
 
 def _as64(*arrs):
@@ -68,8 +59,9 @@ def gptq_rows(W, UA, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
     GPTQ uses a Hessian of the form A (x) I).
     """
     X, UA = _as64(W, UA)
-    s = np.asarray(s, dtype=np.float64)
     m, n = X.shape
+    grid = Grid.of(s, qmin, qmax, m, n)
+    rows = np.arange(m)
     C = np.zeros((m, n))
     P = np.zeros((m, n))
     E = np.zeros((m, n))
@@ -77,13 +69,13 @@ def gptq_rows(W, UA, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
     for j in range(n):
         x = X[:, j].copy()
         P[:, j] = x
-        c, o = _decide(x, s, qmin, qmax, None if guide is None else guide[:, j], guide_tol)
+        c, o = grid.decide(x, rows, j, None if guide is None else guide[:, j], guide_tol)
         n_over += o
         C[:, j] = c
-        err = (x - s * c) / UA[j, j]
+        err = (x - grid.value(c, rows, j)) / UA[j, j]
         E[:, j] = err
         X[:, j + 1:] -= np.outer(err, UA[j, j + 1:])
-    return SolveResult(C, P, s[:, None] * C, E, n_over)
+    return SolveResult(C, P, grid.values(C), E, n_over)
 
 
 def naive_vec_gptq(W, s, qmin=None, qmax=None, A=None, B=None, UA=None, UB=None,
@@ -99,8 +91,8 @@ def naive_vec_gptq(W, s, qmin=None, qmax=None, A=None, B=None, UA=None, UB=None,
     ``O(m^2 n^2)`` work per step set (section 3, BaKron-naive).
     """
     W = np.asarray(W, dtype=np.float64)
-    s = np.asarray(s, dtype=np.float64)
     m, n = W.shape
+    grid = Grid.of(s, qmin, qmax, m, n)
     if A is not None:
         H = np.kron(np.asarray(A, np.float64), np.asarray(B, np.float64))
         Hinv = np.linalg.inv(H)
@@ -112,6 +104,7 @@ def naive_vec_gptq(W, s, qmin=None, qmax=None, A=None, B=None, UA=None, UB=None,
     U = np.linalg.cholesky(Hinv).T
     x = W.reshape(-1, order="F").copy()
     rows = np.arange(m * n) % m
+    cols = np.arange(m * n) // m
     g = None if guide is None else np.asarray(guide, np.float64).reshape(-1, order="F")
     c = np.zeros(m * n)
     pre = np.zeros(m * n)
@@ -119,14 +112,14 @@ def naive_vec_gptq(W, s, qmin=None, qmax=None, A=None, B=None, UA=None, UB=None,
     n_over = 0
     for k in range(m * n):
         pre[k] = x[k]
-        ck, o = _decide(x[k:k + 1], s[rows[k]:rows[k] + 1], qmin, qmax,
-                        None if g is None else g[k:k + 1], guide_tol)
+        ri, cj = rows[k:k + 1], cols[k:k + 1]
+        ck, o = grid.decide(x[k:k + 1], ri, cj, None if g is None else g[k:k + 1], guide_tol)
         n_over += o
         c[k] = ck[0]
-        e[k] = (x[k] - s[rows[k]] * c[k]) / U[k, k]
+        e[k] = (x[k] - grid.value(ck, ri, cj)[0]) / U[k, k]
         x[k + 1:] -= e[k] * U[k, k + 1:]
     C = c.reshape((m, n), order="F")
-    return SolveResult(C, pre.reshape((m, n), order="F"), s[:, None] * C,
+    return SolveResult(C, pre.reshape((m, n), order="F"), grid.values(C),
                        e.reshape((m, n), order="F"), n_over)
 
 
@@ -146,8 +139,8 @@ def antidiag(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
     >= the smallest active row, columns >= the smallest active column).
     """
     X, UA, UB = _as64(W, UA, UB)
-    s = np.asarray(s, dtype=np.float64)
     m, n = X.shape
+    grid = Grid.of(s, qmin, qmax, m, n)
     lA = 1.0 / np.diag(UA)
     lB = 1.0 / np.diag(UB)
     S = np.add.outer(np.arange(m), np.arange(n))
@@ -160,17 +153,17 @@ def antidiag(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
         x = X[i, j].copy()
         P[i, j] = x
         gd = None if guide is None else np.asarray(guide)[i, j]
-        c, o = _decide(x, s[i], qmin, qmax, gd, guide_tol)
+        c, o = grid.decide(x, i, j, gd, guide_tol)
         n_over += o
         C[i, j] = c
-        e = (x - s[i] * c) * lB[i] * lA[j]
+        e = (x - grid.value(c, i, j)) * lB[i] * lA[j]
         E[i, j] = e
         i0, j0 = int(i[0]), int(j[-1])
         Z = e[:, None] * UA[j, j0:]           # row r: E_{i_r j_r} U_A[j_r, j0:]
         delta = UB[i, i0:].T @ Z              # sum_r U_B[i_r, i'] Z[r, j']
         later = S[i0:, j0:] > d
         X[i0:, j0:] -= np.where(later, delta, 0.0)
-    return SolveResult(C, P, s[:, None] * C, E, n_over)
+    return SolveResult(C, P, grid.values(C), E, n_over)
 
 
 def recursive_vec(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
@@ -183,8 +176,8 @@ def recursive_vec(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4
     intended for tiny shapes only.
     """
     X, UA, UB = _as64(W, UA, UB)
-    s = np.asarray(s, dtype=np.float64)
     m, n = X.shape
+    grid = Grid.of(s, qmin, qmax, m, n)
     lA = 1.0 / np.diag(UA)
     lB = 1.0 / np.diag(UB)
     K = np.arange(m)[:, None] + m * np.arange(n)[None, :]
@@ -198,11 +191,11 @@ def recursive_vec(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4
         i, j = k % m, k // m
         x = X[i:i + 1, j]
         P[i, j] = x[0]
-        c, o = _decide(x, s[i:i + 1], qmin, qmax,
-                       None if gd is None else gd[i:i + 1, j], guide_tol)
+        c, o = grid.decide(x, np.array([i]), np.array([j]),
+                           None if gd is None else gd[i:i + 1, j], guide_tol)
         n_over[0] += o
         C[i, j] = c[0]
-        E[i, j] = (x[0] - s[i] * c[0]) * lB[i] * lA[j]
+        E[i, j] = (x[0] - grid.value(c[0], i, j)) * lB[i] * lA[j]
 
     def rec(k0, k1):
         if k1 - k0 == 1:
@@ -218,7 +211,7 @@ def recursive_vec(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4
 
     if m * n:
         rec(0, m * n)
-    return SolveResult(C, P, s[:, None] * C, E, n_over[0])
+    return SolveResult(C, P, grid.values(C), E, n_over[0])
 
 
 def bakron(W, UA, UB, s, qmin=None, qmax=None, leaf_width=1, guide=None,
@@ -236,8 +229,8 @@ def bakron(W, UA, UB, s, qmin=None, qmax=None, leaf_width=1, guide=None,
     boxes of the two bands.
     """
     X, UA, UB = _as64(W, UA, UB)
-    s = np.asarray(s, dtype=np.float64)
     m, n = X.shape
+    grid = Grid.of(s, qmin, qmax, m, n)
     lA = 1.0 / np.diag(UA)
     lB = 1.0 / np.diag(UB)
     S = np.add.outer(np.arange(m), np.arange(n))
@@ -256,11 +249,10 @@ def bakron(W, UA, UB, s, qmin=None, qmax=None, leaf_width=1, guide=None,
             i, j = _diag_entries(d, m, n)
             x = X[i, j].copy()
             P[i, j] = x
-            c, o = _decide(x, s[i], qmin, qmax,
-                           None if gd is None else gd[i, j], guide_tol)
+            c, o = grid.decide(x, i, j, None if gd is None else gd[i, j], guide_tol)
             n_over[0] += o
             C[i, j] = c
-            e = (x - s[i] * c) * lB[i] * lA[j]
+            e = (x - grid.value(c, i, j)) * lB[i] * lA[j]
             E[i, j] = e
             if d + 1 < d1:
                 r0, r1, c0, c1 = box(d + 1, d1)
@@ -290,7 +282,7 @@ def bakron(W, UA, UB, s, qmin=None, qmax=None, leaf_width=1, guide=None,
 
     if m and n:
         rec(0, m + n - 1)
-    return SolveResult(C, P, s[:, None] * C, E, n_over[0])
+    return SolveResult(C, P, grid.values(C), E, n_over[0])
 
 
 def bakron_tiled_order_check(W, UA, UB, s, qmin=None, qmax=None, tile=4):
@@ -305,8 +297,8 @@ def bakron_tiled_order_check(W, UA, UB, s, qmin=None, qmax=None, tile=4):
     Raises ``ValueError`` if the order is not such an order.
     """
     X, UA, UB = _as64(W, UA, UB)
-    s = np.asarray(s, dtype=np.float64)
     m, n = X.shape
+    grid = Grid.of(s, qmin, qmax, m, n)
     lA = 1.0 / np.diag(UA)
     lB = 1.0 / np.diag(UB)
     order = []
@@ -328,12 +320,12 @@ def bakron_tiled_order_check(W, UA, UB, s, qmin=None, qmax=None, tile=4):
             raise ValueError("order rounds (%d,%d) before an entry to its top-left" % (i, j))
         x = X[i, j]
         P[i, j] = x
-        c = quantize_codes(np.array([x]), s[i:i + 1], qmin, qmax)[0]
+        c = grid.decide(np.array([x]), np.array([i]), np.array([j]))[0][0]
         C[i, j] = c
-        e = (x - s[i] * c) * lB[i] * lA[j]
+        e = (x - grid.value(c, i, j)) * lB[i] * lA[j]
         E[i, j] = e
         done[i, j] = True
         upd = np.outer(UB[i, i:], UA[j, j:]) * e
         upd[0, 0] = 0.0
         X[i:, j:] -= np.where(done[i:, j:], 0.0, upd)
-    return SolveResult(C, P, s[:, None] * C, E)
+    return SolveResult(C, P, grid.values(C), E)

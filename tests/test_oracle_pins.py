@@ -391,3 +391,71 @@ def test_shampoo_with_equal_norms_is_scaled_kfac():
     Ak, _ = O.kfac_factors(X, G)
     np.testing.assert_allclose(A, 2.25 * Ak, rtol=1e-12)
     assert np.isclose(np.trace(Ak), np.mean(np.sum(X * X, axis=1)))
+
+
+# ------------------------------------------------- base quantizers (grids)
+
+def test_symmetric_grid_per_row_is_row_scale():
+    rng = np.random.default_rng(40)
+    W = (0.02 * rng.standard_normal((5, 12))).astype(np.float32)
+    W[2] = 0.0
+    g, s, z = O.symmetric_grid(W, 4)
+    np.testing.assert_array_equal(s[:, 0], O.row_scale(W, 7))
+    assert np.all(z == 0) and g.qmin == -8 and g.qmax == 7
+    g2, s2, _ = O.symmetric_grid(W, 4, group=4)
+    assert s2.shape == (5, 3)
+    np.testing.assert_array_equal(s2[:, 1], O.row_scale(W[:, 4:8], 7))
+
+
+def test_asymmetric_grid_hand_example():
+    W = np.array([[-0.3, 0.1, 0.5]], dtype=np.float32)
+    g, s, z = O.asymmetric_grid(W, 2)
+    s_want = np.float32((np.float32(0.5) - np.float32(-0.3)) / np.float32(3.0))   # fp32 span / 3
+    assert s[0, 0] == s_want and z[0, 0] == 1.0
+    c = O.quantize_codes(W[0], g.S[0], g.qmin, g.qmax, g.Z[0])
+    np.testing.assert_array_equal(c, [0.0, 1.0, 3.0])
+    np.testing.assert_allclose(g.values(c[None, :])[0], s_want * np.array([-1.0, 0.0, 2.0]))
+
+
+@pytest.mark.parametrize("kind", ["sym", "asym"])
+@pytest.mark.parametrize("group", [None, 3])
+def test_grid_rtn_error_bounds(kind, group):
+    rng = np.random.default_rng(41)
+    W = (0.05 * rng.standard_normal((6, 10)) + 0.01).astype(np.float32)
+    g, s, z = (O.symmetric_grid if kind == "sym" else O.asymmetric_grid)(W, 3, group)
+    c = O.quantize_codes(W, g.S, g.qmin, g.qmax, g.Z)
+    err = np.abs(g.values(c) - W.astype(np.float64))
+    # symmetric: the data lie inside the representable range (error <= s/2);
+    # asymmetric: the zero point is rounded, so the range can miss by s/2
+    bound = (0.5 if kind == "sym" else 1.0) * g.S * (1 + 1e-6)
+    assert np.all(err <= bound)
+    assert np.all((c >= g.qmin) & (c <= g.qmax))
+
+
+def test_theorem32_with_grouped_asymmetric_grid():
+    p = problem(5, 7, seed=42)
+    g, _, _ = O.asymmetric_grid(p["W"], 3, group=2)
+    ref = O.naive_vec_gptq(p["W"], g, UA=p["UA"], UB=p["UB"])
+    for r in (O.antidiag(p["W"], p["UA"], p["UB"], g), O.bakron(p["W"], p["UA"], p["UB"], g),
+              O.recursive_vec(p["W"], p["UA"], p["UB"], g),
+              O.bakron_tiled_order_check(p["W"], p["UA"], p["UB"], g, tile=2)):
+        np.testing.assert_array_equal(r.codes, ref.codes)
+        np.testing.assert_allclose(r.preround, ref.preround, atol=1e-12)
+        np.testing.assert_allclose(r.V, ref.V, atol=1e-15)
+    # B = I: row-wise GPTQ with the same grid
+    one = O.gptq_rows(p["W"], p["UA"], g)
+    two = O.antidiag(p["W"], p["UA"], np.eye(5), g)
+    np.testing.assert_array_equal(one.codes, two.codes)
+    # the certificate accepts the output and rejects a flipped code
+    cert = O.certificate(p["W"], ref.V, ref.codes, p["UA"], p["UB"], g)
+    assert cert["ok"] and cert["mismatch"] == 0
+
+
+def test_grid_diagonal_factors_give_grid_rtn():
+    rng = np.random.default_rng(43)
+    W = 0.02 * rng.standard_normal((4, 9))
+    g, _, _ = O.asymmetric_grid(W, 4, group=3)
+    UA = np.diag(rng.uniform(0.5, 2.0, 9))
+    UB = np.diag(rng.uniform(0.5, 2.0, 4))
+    r = O.bakron(W, UA, UB, g)
+    np.testing.assert_array_equal(r.codes, O.quantize_codes(W, g.S, g.qmin, g.qmax, g.Z))
