@@ -148,6 +148,37 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n,
                               const bakron_opts* opts, void* ws, size_t ws_bytes,
                               void* stream);
 
+/* Base quantizer grids (the abstract calls BaKron modular in the base
+ * quantizer).  A grid gives row i and column group k (columns
+ * [group*k, group*k + group)) a scale s_ik > 0 and an integer zero point z_ik;
+ * an entry's code is c = clamp(rint(x / s) + z, qmin, qmax) and its value
+ * s (c - z).  bakron_grid_params fills scale and zero (m x groups, device,
+ * row-major) from the ORIGINAL W (device, m x n) and writes the code range to
+ * *qmin, *qmax (host, nullable):
+ *   asymmetric = 0: symmetric b-bit, s = max|W_G| / (2^(b-1) - 1) (1 for an
+ *                   all-zero group), z = 0, codes [-2^(b-1), 2^(b-1) - 1];
+ *   asymmetric = 1: min-max b-bit with zero in range, lo = min(min W_G, 0),
+ *                   hi = max(max W_G, 0), s = (hi - lo) / (2^b - 1),
+ *                   z = rint(-lo / s), codes [0, 2^b - 1] (b <= 7 keeps the
+ *                   codes inside int8; wider codes make bakron_quantize_grid
+ *                   return BAKRON_ERR_CODE_RANGE).
+ * group: 0 or >= n for one group per row, otherwise a multiple of 32.
+ * bits: 2..8.  All arithmetic in fp32 (IEEE division). */
+bakron_status bakron_grid_params(const float* W, int64_t m, int64_t n, int bits, int asymmetric,
+                                 int64_t group, float* scale, float* zero, int* qmin, int* qmax,
+                                 void* stream);
+
+/* bakron_quantize on a grid: scale and zero (zero nullable = all 0) are
+ * m x groups for the given group size (rules as above), qmin/qmax the code
+ * range.  UB may be NULL (B = I).  Everything else as bakron_quantize; the
+ * workspace size is the same.  A zero point that is not an integer inside
+ * [qmin, qmax] returns BAKRON_ERR_CODE_RANGE. */
+bakron_status bakron_quantize_grid(const float* W, int64_t m, int64_t n, const float* UA,
+                                   const float* UB, const float* scale, const float* zero,
+                                   int64_t group, int qmin, int qmax, float* V, int8_t* codes,
+                                   float* preround, const bakron_opts* opts, void* ws,
+                                   size_t ws_bytes, void* stream);
+
 /* BaKron-antidiagonal (section 3 of the summary page; equivalent to YAQA):
  * one persistent grid-synchronised kernel, m + n - 1 steps, each rounding
  * one anti-diagonal and applying U_B^T E_d U_A to the entries on later

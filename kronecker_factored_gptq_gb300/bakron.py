@@ -24,7 +24,8 @@ INT32_MAX = (1 << 31) - 1
 EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bakron_kernel_launches",
            "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
            "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
-           "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors"]
+           "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
+           "bakron_grid_params", "bakron_quantize_grid"]
 FACTORS_KFAC = 0
 FACTORS_SHAMPOO = 1
 
@@ -79,11 +80,16 @@ def lib():
                                            ctypes.POINTER(Opts), vp, sz, vp]
     L.bakron_quantize_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                           vp, vp, vp]
+    L.bakron_grid_params.argtypes = [vp, i64, i64, ctypes.c_int, ctypes.c_int, i64, vp, vp,
+                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), vp]
+    L.bakron_quantize_grid.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, ctypes.c_int, ctypes.c_int,
+                                       vp, vp, vp, ctypes.POINTER(Opts), vp, sz, vp]
     L.bakron_factors_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
     L.bakron_factors.argtypes = [vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, sz, vp]
     for f in ("bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
               "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
-              "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors"):
+              "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
+              "bakron_grid_params", "bakron_quantize_grid"):
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
@@ -221,6 +227,61 @@ def bakron_quantize(W, UA, UB, scale, qmin, qmax, want_preround=False, opts=None
         ctypes.byref(opts) if opts is not None else None,
         ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
     _check(st, "bakron_quantize")
+    return V, codes, pre
+
+
+def grid_groups(n, group):
+    """Number of column groups of a grid (group 0/None or >= n: one per row)."""
+    if not group or group >= n:
+        return 1
+    if group % 32:
+        raise ValueError("group must be a multiple of 32 (or cover the whole row)")
+    return -(-n // group)
+
+
+def bakron_grid_params(W, bits, asymmetric=False, group=None, stream=None):
+    """Grid of a b-bit base quantizer on the original W: returns
+    (scale, zero, qmin, qmax) with scale/zero of shape (m, groups)."""
+    torch = _torch()
+    m, n = W.shape
+    ng = grid_groups(n, group)
+    scale = torch.empty((m, ng), dtype=torch.float32, device=W.device)
+    zero = torch.empty((m, ng), dtype=torch.float32, device=W.device)
+    qmin, qmax = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().bakron_grid_params(_dev(W, torch.float32, (m, n), "W"), m, n, int(bits),
+                                  1 if asymmetric else 0, int(group or 0),
+                                  ctypes.c_void_p(scale.data_ptr()), ctypes.c_void_p(zero.data_ptr()),
+                                  ctypes.byref(qmin), ctypes.byref(qmax), _stream(stream))
+    _check(st, "bakron_grid_params")
+    return scale, zero, qmin.value, qmax.value
+
+
+def bakron_quantize_grid(W, UA, UB, scale, zero, group, qmin, qmax, want_preround=False, opts=None,
+                         workspace=None, stream=None, out=None):
+    """bakron_quantize on a grid (scale/zero of shape (m, groups)); UB=None
+    means B = I.  Returns (V, codes, preround-or-None)."""
+    torch = _torch()
+    m, n = W.shape
+    ng = grid_groups(n, group)
+    if out is None:
+        V = torch.empty((m, n), dtype=torch.float32, device=W.device)
+        codes = torch.empty((m, n), dtype=torch.int8, device=W.device)
+    else:
+        V, codes = out
+    pre = torch.empty((m, n), dtype=torch.float32, device=W.device) if want_preround else None
+    nb = workspace_size(m, n, opts)
+    ws = _ws(nb, workspace)
+    st = lib().bakron_quantize_grid(
+        _dev(W, torch.float32, (m, n), "W"), m, n, _dev(UA, torch.float32, (n, n), "UA"),
+        None if UB is None else _dev(UB, torch.float32, (m, m), "UB"),
+        _dev(scale, torch.float32, (m, ng), "scale"),
+        None if zero is None else _dev(zero, torch.float32, (m, ng), "zero"),
+        int(group or 0), int(qmin), int(qmax),
+        _dev(V, torch.float32, (m, n), "V"), _dev(codes, torch.int8, (m, n), "codes"),
+        None if pre is None else _dev(pre, torch.float32, (m, n), "preround"),
+        ctypes.byref(opts) if opts is not None else None,
+        ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
+    _check(st, "bakron_quantize_grid")
     return V, codes, pre
 
 

@@ -235,7 +235,7 @@ constexpr int kMaxDepth = 24;
 struct QLayout {
   int64_t M, N, Mp, Np;
   int ndepth;
-  size_t status, sched, scale, wt, ehi, elo, yhi[kMaxDepth], ylo[kMaxDepth], lathi, latlo, lbthi,
+  size_t status, sched, scale, zero, wt, ehi, elo, yhi[kMaxDepth], ylo[kMaxDepth], lathi, latlo, lbthi,
       lbtlo, total;
 };
 
@@ -253,7 +253,11 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   L.status = take(256);
   const RowsSchedule& rs = get_rows_schedule((int)L.M, (int)L.N);
   L.sched = take(sizeof(WorkItem) * (std::max(s.items.size(), rs.items.size()) + 1));
-  L.scale = take(f * L.Mp);
+  // grid scales and zero points, padded rows x groups (at most one group per
+  // 32 columns)
+  const size_t ngmax = (size_t)std::max<int64_t>(1, (n + 31) / 32);
+  L.scale = take(f * L.Mp * ngmax);
+  L.zero = take(f * L.Mp * ngmax);
   L.wt = take(f * L.Mp * L.Np);
   L.ehi = take(f * L.Mp * L.Np);
   L.elo = take(f * L.Mp * L.Np);
@@ -477,7 +481,14 @@ bool sizes_ok(int64_t m, int64_t n) { return m >= 1 && n >= 1 && m <= (1 << 20) 
 // The one-sided solve (U_B = I): see RowsSchedule.  Arguments validated by
 // bakron_quantize; the workspace layout is the two-sided one (its Y^T and
 // U_B^T regions stay unused).
-bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* UA, const float* scale,
+// A validated grid: scale / zero point per (row, group of `group` columns).
+struct GridIn {
+  const float* scale;
+  const float* zero;   // nullable: zero points of 0
+  int64_t group, ng;
+};
+
+bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* UA, const GridIn& gr,
                             int qmin, int qmax, float* V, int8_t* codes, float* preround,
                             const bakron_opts& o, void* ws, cudaStream_t s) {
   const QLayout L = quantize_layout(m, n);
@@ -491,6 +502,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   DevStatus* st = (DevStatus*)(base + L.status);
   WorkItem* items = (WorkItem*)(base + L.sched);
   float* sp = (float*)(base + L.scale);
+  float* zp = (float*)(base + L.zero);
   float* wt = (float*)(base + L.wt);
   float* ehi = (float*)(base + L.ehi);
   float* elo = (float*)(base + L.elo);
@@ -511,8 +523,9 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
-    TRY_CUDA(launch_check_finite(scale, m, st, cs));
-    TRY_CUDA(launch_pad_scale(scale, m, sp, L.Mp, cs));
+    TRY_CUDA(launch_check_finite(gr.scale, m * gr.ng, st, cs));
+    TRY_CUDA(launch_check_zero(gr.zero, m * gr.ng, qmin, qmax, st, cs));
+    TRY_CUDA(launch_pad_grid(gr.scale, gr.zero, m, gr.ng, sp, zp, L.Mp, cs));
     TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
     TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
     pt.end(3, ev);
@@ -521,6 +534,9 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   la.wt = wt; la.ldw = L.Np;
   la.lat_hi = lathi; la.lat_lo = latlo; la.lda = L.Np;
   la.scale = sp;
+  la.zero = zp;
+  la.group = gr.group;
+  la.ngroups = gr.ng;
   la.e_hi = ehi; la.e_lo = elo;
   la.round_lo = 1;
   la.V = V; la.codes = codes; la.preround = preround;
@@ -715,21 +731,25 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   return r;
 }
 
-bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float* UA, const float* UB,
-                              const float* scale, int qmin, int qmax, float* V, int8_t* codes,
-                              float* preround, const bakron_opts* opts_in, void* ws,
-                              size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace bakron {
+namespace {
+bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* UA, const float* UB,
+                            const GridIn& gr, int qmin, int qmax, float* V, int8_t* codes,
+                            float* preround, const bakron_opts* opts_in, void* ws, size_t ws_bytes,
+                            void* stream) {
   bakron_opts o;
   bakron_default_opts(&o);
   if (opts_in) o = *opts_in;
   if (!valid_opts(o)) return BAKRON_ERR_INVALID_ARG;
-  if (!W || !UA || !scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
+  if (!W || !UA || !gr.scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
   if (!sizes_ok(m, n) || qmin > qmax) return BAKRON_ERR_INVALID_ARG;
   const QLayout L = quantize_layout(m, n);
   if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
   if (o.use_3xtf32 && !prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
   if (!UB)
-    return quantize_rows(W, m, n, UA, scale, qmin, qmax, V, codes, preround, o, ws,
+    return quantize_rows(W, m, n, UA, gr, qmin, qmax, V, codes, preround, o, ws,
                          (cudaStream_t)stream);
   const Schedule& sch = get_schedule((int)L.M, (int)L.N);
   cudaStream_t s = (cudaStream_t)stream;
@@ -742,6 +762,7 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   DevStatus* st = (DevStatus*)(base + L.status);
   WorkItem* items = (WorkItem*)(base + L.sched);
   float* sp = (float*)(base + L.scale);
+  float* zp = (float*)(base + L.zero);
   float* wt = (float*)(base + L.wt);
   float* ehi = (float*)(base + L.ehi);
   float* elo = (float*)(base + L.elo);
@@ -766,8 +787,9 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
-    TRY_CUDA(launch_check_finite(scale, m, st, cs));
-    TRY_CUDA(launch_pad_scale(scale, m, sp, L.Mp, cs));
+    TRY_CUDA(launch_check_finite(gr.scale, m * gr.ng, st, cs));
+    TRY_CUDA(launch_check_zero(gr.zero, m * gr.ng, qmin, qmax, st, cs));
+    TRY_CUDA(launch_pad_grid(gr.scale, gr.zero, m, gr.ng, sp, zp, L.Mp, cs));
     TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
     TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
     TRY_CUDA(launch_transpose_split(UB, m, lbthi, lbtlo, L.Mp, cs));
@@ -778,6 +800,9 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   la.lat_hi = lathi; la.lat_lo = latlo; la.lda = L.Np;
   la.lbt_hi = lbthi; la.lbt_lo = lbtlo; la.ldb = L.Mp;
   la.scale = sp;
+  la.zero = zp;
+  la.group = gr.group;
+  la.ngroups = gr.ng;
   la.e_hi = ehi; la.e_lo = elo;
   la.round_lo = o.use_3xtf32;
   la.V = V; la.codes = codes; la.preround = preround;
@@ -863,6 +888,56 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
   bakron_status r = finish(s, st, &h);
   pt.collect();
   return r;
+}
+
+
+// The grid of a b-bit base quantizer: `group` columns per group (0 or >= n:
+// one group per row; otherwise a multiple of 32).  Returns the group count,
+// or -1 for an invalid group size.
+int64_t grid_groups(int64_t n, int64_t group) {
+  if (group <= 0 || group >= n) return 1;
+  if (group % 32 != 0) return -1;
+  return (n + group - 1) / group;
+}
+}  // namespace
+}  // namespace bakron
+
+extern "C" {
+
+bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float* UA, const float* UB,
+                              const float* scale, int qmin, int qmax, float* V, int8_t* codes,
+                              float* preround, const bakron_opts* opts, void* ws,
+                              size_t ws_bytes, void* stream) {
+  const GridIn gr{scale, nullptr, n, 1};
+  return quantize_impl(W, m, n, UA, UB, gr, qmin, qmax, V, codes, preround, opts, ws, ws_bytes,
+                       stream);
+}
+
+bakron_status bakron_quantize_grid(const float* W, int64_t m, int64_t n, const float* UA,
+                                   const float* UB, const float* scale, const float* zero,
+                                   int64_t group, int qmin, int qmax, float* V, int8_t* codes,
+                                   float* preround, const bakron_opts* opts, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  const int64_t ng = grid_groups(n, group);
+  if (ng < 1 || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
+  const GridIn gr{scale, zero, ng == 1 ? n : group, ng};
+  return quantize_impl(W, m, n, UA, UB, gr, qmin, qmax, V, codes, preround, opts, ws, ws_bytes,
+                       stream);
+}
+
+bakron_status bakron_grid_params(const float* W, int64_t m, int64_t n, int bits, int asymmetric,
+                                 int64_t group, float* scale, float* zero, int* qmin, int* qmax,
+                                 void* stream) {
+  const int64_t ng = grid_groups(n, group);
+  if (!W || !scale || !zero || !sizes_ok(m, n) || ng < 1 || bits < 2 || bits > 8 ||
+      (asymmetric != 0 && asymmetric != 1))
+    return BAKRON_ERR_INVALID_ARG;
+  if (qmin) *qmin = asymmetric ? 0 : -(1 << (bits - 1));
+  if (qmax) *qmax = asymmetric ? (1 << bits) - 1 : (1 << (bits - 1)) - 1;
+  cudaStream_t s = (cudaStream_t)stream;
+  TRY_CUDA(launch_grid_params(W, m, n, ng == 1 ? n : group, ng, bits, asymmetric, scale, zero, s));
+  TRY_CUDA(cudaStreamSynchronize(s));
+  return BAKRON_OK;
 }
 
 bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n, const float* UA,

@@ -76,7 +76,9 @@ struct LeafArgs {
   float* wt; int64_t ldw;            // padded working matrix W~ (Mp x Np)
   const float* lat_hi; const float* lat_lo; int64_t lda;  // U_A^T split (Np x Np)
   const float* lbt_hi; const float* lbt_lo; int64_t ldb;  // U_B^T split (Mp x Mp)
-  const float* scale;                // padded row scales (Mp)
+  const float* scale;                // padded grid scales (Mp x ngroups)
+  const float* zero;                 // padded grid zero points (Mp x ngroups)
+  int64_t group, ngroups;            // columns per group; groups per row
   float* e_hi; float* e_lo;          // scaled errors, split (Mp x Np, ld = ldw)
   int round_lo;                      // e_lo rounded to tf32 (read by the tensor cores)
   float* V; int8_t* codes; float* preround;  // outputs, m x n (preround nullable)
@@ -116,8 +118,12 @@ cudaError_t launch_pad_matrix(const float* src, int64_t rows, int64_t cols, floa
                               int64_t rows_p, int64_t cols_p, cudaStream_t s);
 cudaError_t launch_transpose_split(const float* U, int64_t k, float* hi, float* lo, int64_t kp,
                                    cudaStream_t s);
-cudaError_t launch_pad_scale(const float* scale, int64_t m, float* sp, int64_t mp,
-                             cudaStream_t s);
+cudaError_t launch_grid_params(const float* W, int64_t m, int64_t n, int64_t g, int64_t ng, int bits,
+                               int asym, float* scale, float* zero, cudaStream_t s);
+cudaError_t launch_pad_grid(const float* scale, const float* zero, int64_t m, int64_t ng, float* sp,
+                            float* zp, int64_t mp, cudaStream_t s);
+cudaError_t launch_check_zero(const float* z, int64_t count, int qmin, int qmax, DevStatus* st,
+                              cudaStream_t s);
 cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cudaStream_t s);
 cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s);
 // one-sided (B = I) leaf: column tile a.D of every row tile

@@ -323,13 +323,20 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       const float ubaa = Ubd[row * PU + row];
       const float lB = 1.f / ubaa;
       const int64_t gi = i0 + S * I + row;
-      const float sc = a.scale[gi];
       const bool row_real = live && gi < a.m;
       float* rs = rTk + slot * RT_SLOT;
       const float* Dj = Dg + J * S * PD;
       const float* lAj = lA + S * J;
       float* Xrow = X + (S * I + row) * PX + S * J;
       const int64_t jb0 = j0 + S * J;
+      // the block's columns lie in one group of the grid (groups are whole
+      // multiples of 32 columns, or the whole row)
+      int64_t grp = jb0 / a.group;
+      if (grp > a.ngroups - 1) grp = a.ngroups - 1;
+      const float sc = a.scale[gi * a.ngroups + grp];
+      const float zc = a.zero[gi * a.ngroups + grp];
+      // centred code c = clamp(rint(x / s), qmin - z, qmax - z); stored c + z
+      const float clo = fqmin - zc, chi = fqmax - zc;
       const float rinv = 1.f / sc;
       signed char* csr = CS + slot * S * PC + row * PC;
       float FR[NF];
@@ -378,15 +385,16 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           // so it can differ from the correctly rounded quotient only within
           // 2e-5 grid units of a rounding boundary
           float c = rintf(x * rinv);
-          c = fminf(fmaxf(c, fqmin), fqmax);
+          c = fminf(fmaxf(c, clo), chi);
           const float e = act ? (x - sc * c) * lB * la : 0.f;
+          const float code = c + zc;
           nonfinite |= act && !isfinite(x);
-          out_of_range |= act && ((c < -128.f) || (c > 127.f));
+          out_of_range |= act && ((code < -128.f) || (code > 127.f));
           FR[sg] = fmaf(e, dv[0].x, FR[sg]);
           rlast = FR[sg];
           if (act) {
             Xrow[b] = e;
-            csr[b] = (signed char)(int)fminf(fmaxf(c, -128.f), 127.f);
+            csr[b] = (signed char)(int)fminf(fmaxf(code, -128.f), 127.f);
             rs[b * PR + row] = FR[sg];
           }
           if (PRE && act && row_real && jb0 + b < a.n) a.preround[gi * a.n + jb0 + b] = x;
@@ -433,16 +441,16 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
 #pragma unroll
           for (int q = 0; q < S / 4; ++q) {
             float4 v;
-            v.x = sc * (float)csr[4 * q + 0];
-            v.y = sc * (float)csr[4 * q + 1];
-            v.z = sc * (float)csr[4 * q + 2];
-            v.w = sc * (float)csr[4 * q + 3];
+            v.x = sc * ((float)csr[4 * q + 0] - zc);
+            v.y = sc * ((float)csr[4 * q + 1] - zc);
+            v.z = sc * ((float)csr[4 * q + 2] - zc);
+            v.w = sc * ((float)csr[4 * q + 3] - zc);
             reinterpret_cast<float4*>(a.V + base)[q] = v;
           }
         } else {
           for (int t = 0; t < nb; ++t) {
             a.codes[base + t] = csr[t];
-            a.V[base + t] = sc * (float)csr[t];
+            a.V[base + t] = sc * ((float)csr[t] - zc);
           }
         }
       }

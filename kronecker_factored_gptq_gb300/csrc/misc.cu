@@ -113,16 +113,100 @@ cudaError_t launch_transpose_split(const float* U, int64_t k, float* hi, float* 
   return cudaGetLastError();
 }
 
-__global__ void pad_scale_kernel(const float* __restrict__ scale, int64_t m, float* __restrict__ sp,
-                                 int64_t mp) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < mp;
-       i += (int64_t)gridDim.x * blockDim.x)
-    sp[i] = (i < m) ? scale[i] : 1.f;
+// Grid of one (row, group) pair per warp: the b-bit grid of columns
+// [g k, g k + g) of row i.  Symmetric: s = max|W| / qmax (1 for a zero
+// group), z = 0.  Asymmetric (min-max with zero in range): lo = min(min W, 0),
+// hi = max(max W, 0), s = (hi - lo) / (2^b - 1) (1 for a zero group),
+// z = rint(-lo / s) in [0, 2^b - 1].  All in fp32 (IEEE division).
+__global__ void grid_params_kernel(const float* __restrict__ W, int64_t m, int64_t n, int64_t g,
+                                   int64_t ng, int bits, int asym, float* __restrict__ scale,
+                                   float* __restrict__ zero) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t p = w0; p < m * ng; p += nw) {
+    const int64_t i = p / ng, k = p - i * ng;
+    const int64_t j0 = k * g, j1 = j0 + g < n ? j0 + g : n;
+    float mn = 0.f, mx = 0.f, amax = 0.f;
+    for (int64_t j = j0 + lane; j < j1; j += 32) {
+      const float v = W[i * n + j];
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+      amax = fmaxf(amax, fabsf(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    }
+    if (lane == 0) {
+      float sc, z = 0.f;
+      if (!asym) {
+        const float qmax = (float)((1 << (bits - 1)) - 1);
+        sc = (amax == 0.f) ? 1.f : amax / qmax;
+      } else {
+        const float levels = (float)((1 << bits) - 1);
+        const float span = mx - mn;
+        if (span == 0.f) {
+          sc = 1.f;
+        } else {
+          sc = span / levels;
+          z = fminf(fmaxf(rintf(-mn / sc), 0.f), levels);
+        }
+      }
+      scale[p] = sc;
+      zero[p] = z;
+    }
+  }
 }
 
-cudaError_t launch_pad_scale(const float* scale, int64_t m, float* sp, int64_t mp, cudaStream_t s) {
+cudaError_t launch_grid_params(const float* W, int64_t m, int64_t n, int64_t g, int64_t ng, int bits,
+                               int asym, float* scale, float* zero, cudaStream_t s) {
   count_launch();
-  pad_scale_kernel<<<grid_for(mp, 256), 256, 0, s>>>(scale, m, sp, mp);
+  grid_params_kernel<<<grid_for(m * ng * 32, 256), 256, 0, s>>>(W, m, n, g, ng, bits, asym, scale,
+                                                                zero);
+  return cudaGetLastError();
+}
+
+// Padded grid (mp x ng): the real rows' scale / zero point, then scale 1 and
+// zero point 0 on the padding rows; zero = NULL means zero points of 0.
+__global__ void pad_grid_kernel(const float* __restrict__ scale, const float* __restrict__ zero,
+                                int64_t m, int64_t ng, float* __restrict__ sp,
+                                float* __restrict__ zp, int64_t mp) {
+  const int64_t total = mp * ng;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const bool real = t < m * ng;
+    sp[t] = real ? scale[t] : 1.f;
+    zp[t] = (real && zero) ? zero[t] : 0.f;
+  }
+}
+
+cudaError_t launch_pad_grid(const float* scale, const float* zero, int64_t m, int64_t ng, float* sp,
+                            float* zp, int64_t mp, cudaStream_t s) {
+  count_launch();
+  pad_grid_kernel<<<grid_for(mp * ng, 256), 256, 0, s>>>(scale, zero, m, ng, sp, zp, mp);
+  return cudaGetLastError();
+}
+
+// CODE_RANGE if a zero point is not an integer inside [qmin, qmax].
+__global__ void check_zero_kernel(const float* __restrict__ z, int64_t count, float qmin, float qmax,
+                                  DevStatus* st) {
+  bool bad = false;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = z[i];
+    bad |= !(v >= qmin && v <= qmax) || rintf(v) != v;
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) set_status(st, BAKRON_ERR_CODE_RANGE);
+}
+
+cudaError_t launch_check_zero(const float* z, int64_t count, int qmin, int qmax, DevStatus* st,
+                              cudaStream_t s) {
+  if (count == 0 || !z) return cudaSuccess;
+  count_launch();
+  check_zero_kernel<<<grid_for(count, 256), 256, 0, s>>>(z, count, (float)qmin, (float)qmax, st);
   return cudaGetLastError();
 }
 

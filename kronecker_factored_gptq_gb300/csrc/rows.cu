@@ -81,13 +81,19 @@ __global__ void __launch_bounds__(NTH, 1) rows_leaf_kernel(LeafArgs a) {
   const bool wide = a.qmin < -128 || a.qmax > 127;
   bool out_of_range = false;
   const int row = tid;                       // sweep: threads 0..127, one row each
-  const float sc = a.scale[i0 + (row & (T - 1))];
-  const float rinv = 1.f / sc;
 
   for (int cb = 0; cb < T / CB; ++cb) {
     const int q = cb * CB;
-    // ---- (a) sweep of columns q .. q + 31, one thread per row
+    // ---- (a) sweep of columns q .. q + 31, one thread per row; the block's
+    // columns lie in one group of the grid (groups are whole multiples of 32
+    // columns, or the whole row)
     if (tid < T) {
+      int64_t grp = (j0 + q) / a.group;
+      if (grp > a.ngroups - 1) grp = a.ngroups - 1;
+      const int64_t gidx = (i0 + row) * a.ngroups + grp;
+      const float sc = a.scale[gidx], zc = a.zero[gidx];
+      const float rinv = 1.f / sc;
+      const float clo = fqmin - zc, chi = fqmax - zc;   // centred code range
       float* Xr = X + row * PX + q;
       float FR[CB];
 #pragma unroll
@@ -107,12 +113,13 @@ __global__ void __launch_bounds__(NTH, 1) rows_leaf_kernel(LeafArgs a) {
           const int b = 4 * g + bb;
           const float x = xg[bb] - FR[b];
           float c = rintf(x * rinv);
-          c = fminf(fmaxf(c, fqmin), fqmax);
+          c = fminf(fmaxf(c, clo), chi);
           const float e = (x - sc * c) * lA[q + b];
-          if (wide) out_of_range |= (c < -128.f) || (c > 127.f);
+          const float code = c + zc;
+          if (wide) out_of_range |= (code < -128.f) || (code > 127.f);
           eg[bb] = e;
           short c8;   // saturating conversion to the int8 range
-          asm("cvt.rzi.sat.s8.f32 %0, %1;" : "=h"(c8) : "f"(c));
+          asm("cvt.rzi.sat.s8.f32 %0, %1;" : "=h"(c8) : "f"(code));
           cw |= ((unsigned)c8 & 0xffu) << (8 * bb);
           if (PRE) {
             const int64_t gi = i0 + row, gj = j0 + q + b;
@@ -202,19 +209,22 @@ __global__ void __launch_bounds__(NTH, 1) rows_leaf_kernel(LeafArgs a) {
   for (int r = warp; r < T; r += NTH / 32) {
     const int64_t gi = i0 + r;
     if (gi >= a.m) continue;
-    const float s = a.scale[gi];
     const int64_t jc = j0 + 4 * lane;
+    int64_t grp = jc / a.group;
+    if (grp > a.ngroups - 1) grp = a.ngroups - 1;
+    const float s = a.scale[gi * a.ngroups + grp], z = a.zero[gi * a.ngroups + grp];
     const signed char* cr = CS + r * PC + 4 * lane;
     if (jc + 3 < a.n && (a.n & 3) == 0) {
       const int64_t base = gi * a.n + jc;
       *reinterpret_cast<unsigned*>(a.codes + base) = *reinterpret_cast<const unsigned*>(cr);
       *reinterpret_cast<float4*>(a.V + base) =
-          make_float4(s * (float)cr[0], s * (float)cr[1], s * (float)cr[2], s * (float)cr[3]);
+          make_float4(s * ((float)cr[0] - z), s * ((float)cr[1] - z), s * ((float)cr[2] - z),
+                      s * ((float)cr[3] - z));
     } else {
       for (int t = 0; t < 4; ++t)
         if (jc + t < a.n) {
           a.codes[gi * a.n + jc + t] = cr[t];
-          a.V[gi * a.n + jc + t] = s * (float)cr[t];
+          a.V[gi * a.n + jc + t] = s * ((float)cr[t] - z);
         }
     }
   }
