@@ -457,6 +457,41 @@ def run_ours(args, world, rank, local):
             factors[name + "_tflops"] = fl_f / t / 1e12
         del dXs, dGs, fws
 
+    # Batched solves: the two MLP projection shapes (4096 x 14336 and its
+    # transpose), one after the other and then together in one batch call
+    # (each problem on its own stream set); context for throughput.
+    batch = None
+    if not args.no_context:
+        probs = []
+        for name in ("mlp4096x14336", "mlp14336x4096"):
+            wb = WL.load(name, seed=args.seed, device=dev)
+            bW, bA, bB = (torch.from_numpy(x).to(dev) for x in (wb.W, wb.A, wb.B))
+            sb = kb.bakron_rowscale(bW, wb.qmax)
+            UAb, UBb, _, _, _ = kb.bakron_prepare(bA, wb.damp_A, bB, wb.damp_B)
+            del bA, bB
+            probs.append(dict(W=bW, UA=UAb, UB=UBb, scale=sb, qmin=wb.qmin, qmax=wb.qmax))
+        wsb = [torch.empty(kb.workspace_size(p_["W"].shape[0], p_["W"].shape[1]), dtype=torch.uint8,
+                           device=dev) for p_ in probs]
+        seq, bat = [], []
+        for k in range(args.warmup + 3):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            for p_, wsp in zip(probs, wsb):
+                kb.bakron_quantize(p_["W"], p_["UA"], p_["UB"], p_["scale"], p_["qmin"], p_["qmax"],
+                                   workspace=wsp)
+            e[1].record(stream)
+            kb.bakron_quantize_batch(probs)
+            e[2].record(stream)
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                seq.append(e[0].elapsed_time(e[1]))
+                bat.append(e[1].elapsed_time(e[2]))
+        fl_b = sum(flops_model(*p_["W"].shape) for p_ in probs)
+        batch = {"problems": "4096x14336 + 14336x4096", "sequential_s": statistics.median(seq) / 1e3,
+                 "batched_s": statistics.median(bat) / 1e3,
+                 "batched_tflops": fl_b / (statistics.median(bat) / 1e3) / 1e12}
+        del probs, wsb
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, f = oracle_sample(w, args.sample)
@@ -492,6 +527,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "one_sided_gptq": one_sided,
         "factor_accumulation": factors,
+        "batched_solves": batch,
         "context": {"pages_rtx_pro_6000_solve_s": 1.839, "pages_yaqa_solve_s": 110.379,
                     "pages_gptq_solve_s": 0.059},
     }

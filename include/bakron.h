@@ -179,6 +179,35 @@ bakron_status bakron_quantize_grid(const float* W, int64_t m, int64_t n, const f
                                    float* preround, const bakron_opts* opts, void* ws,
                                    size_t ws_bytes, void* stream);
 
+/* Several independent solves in one call (e.g. the layers of a model): each
+ * problem runs the bakron_quantize_grid sequence on a stream set of its own,
+ * so their leaf chains and products overlap on the GPU (a single solve is a
+ * latency-bound chain that leaves most SMs idle).  Up to 8 problems run
+ * concurrently; further ones queue behind them.  Per problem: W (m x n), UA,
+ * UB (NULL = B = I), scale and zero (m x groups; zero nullable), group, the
+ * code range, and the outputs V and codes (no preround); `status` receives
+ * that problem's bakron_status.  The call returns BAKRON_OK when every
+ * problem succeeded, else the first failure.  Arguments are validated per
+ * problem as in bakron_quantize_grid.  ws: bakron_batch_workspace_size
+ * bytes (the problems' workspaces side by side). */
+typedef struct {
+  const float* W;
+  int64_t m, n;
+  const float* UA;
+  const float* UB;
+  const float* scale;
+  const float* zero;
+  int64_t group;
+  int qmin, qmax;
+  float* V;
+  int8_t* codes;
+  int status;
+} bakron_problem;
+bakron_status bakron_batch_workspace_size(int count, const bakron_problem* problems,
+                                          const bakron_opts* opts, size_t* bytes);
+bakron_status bakron_quantize_batch(int count, bakron_problem* problems, const bakron_opts* opts,
+                                    void* ws, size_t ws_bytes, void* stream);
+
 /* BaKron-antidiagonal (section 3 of the summary page; equivalent to YAQA):
  * one persistent grid-synchronised kernel, m + n - 1 steps, each rounding
  * one anti-diagonal and applying U_B^T E_d U_A to the entries on later

@@ -25,7 +25,8 @@ EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bak
            "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
            "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
            "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
-           "bakron_grid_params", "bakron_quantize_grid"]
+           "bakron_grid_params", "bakron_quantize_grid", "bakron_batch_workspace_size",
+           "bakron_quantize_batch"]
 FACTORS_KFAC = 0
 FACTORS_SHAMPOO = 1
 
@@ -44,6 +45,14 @@ class Opts(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int), ("leaf_width", ctypes.c_int), ("use_3xtf32", ctypes.c_int),
                 ("spin_budget_cycles", ctypes.c_longlong), ("fault_inject", ctypes.c_int),
                 ("times", ctypes.POINTER(PhaseTimes))]
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("m", ctypes.c_int64), ("n", ctypes.c_int64),
+                ("UA", ctypes.c_void_p), ("UB", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("zero", ctypes.c_void_p), ("group", ctypes.c_int64), ("qmin", ctypes.c_int),
+                ("qmax", ctypes.c_int), ("V", ctypes.c_void_p), ("codes", ctypes.c_void_p),
+                ("status", ctypes.c_int)]
 
 
 class BakronError(RuntimeError):
@@ -84,12 +93,17 @@ def lib():
                                      ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), vp]
     L.bakron_quantize_grid.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, ctypes.c_int, ctypes.c_int,
                                        vp, vp, vp, ctypes.POINTER(Opts), vp, sz, vp]
+    L.bakron_batch_workspace_size.argtypes = [ctypes.c_int, ctypes.POINTER(Problem),
+                                              ctypes.POINTER(Opts), ctypes.POINTER(sz)]
+    L.bakron_quantize_batch.argtypes = [ctypes.c_int, ctypes.POINTER(Problem), ctypes.POINTER(Opts),
+                                        vp, sz, vp]
     L.bakron_factors_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
     L.bakron_factors.argtypes = [vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, sz, vp]
     for f in ("bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
               "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
               "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
-              "bakron_grid_params", "bakron_quantize_grid"):
+              "bakron_grid_params", "bakron_quantize_grid", "bakron_batch_workspace_size",
+              "bakron_quantize_batch"):
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
@@ -283,6 +297,47 @@ def bakron_quantize_grid(W, UA, UB, scale, zero, group, qmin, qmax, want_preroun
         ctypes.c_void_p(ws.data_ptr()), nb, _stream(stream))
     _check(st, "bakron_quantize_grid")
     return V, codes, pre
+
+
+def bakron_quantize_batch(problems, opts=None, workspace=None, stream=None, outs=None):
+    """Several independent solves at once.  ``problems``: sequence of dicts
+    with W, UA, UB (None = B = I), scale, zero (None = 0), group (None = per
+    row), qmin, qmax.  Returns a list of (V, codes); raises BakronError with
+    ``statuses`` (one per problem) if any problem failed."""
+    torch = _torch()
+    arr = (Problem * len(problems))()
+    keep = []
+    for k, pr in enumerate(problems):
+        W = pr["W"]
+        m, n = W.shape
+        ng = grid_groups(n, pr.get("group"))
+        if outs is None:
+            V = torch.empty((m, n), dtype=torch.float32, device=W.device)
+            C = torch.empty((m, n), dtype=torch.int8, device=W.device)
+        else:
+            V, C = outs[k]
+        UB, zero = pr.get("UB"), pr.get("zero")
+        arr[k] = Problem(
+            _dev(W, torch.float32, (m, n), "W"), m, n, _dev(pr["UA"], torch.float32, (n, n), "UA"),
+            None if UB is None else _dev(UB, torch.float32, (m, m), "UB"),
+            _dev(pr["scale"], torch.float32, (m, ng) if ng > 1 or pr["scale"].dim() == 2 else (m,),
+                 "scale"),
+            None if zero is None else _dev(zero, torch.float32, (m, ng), "zero"),
+            int(pr.get("group") or 0), int(pr["qmin"]), int(pr["qmax"]),
+            _dev(V, torch.float32, (m, n), "V"), _dev(C, torch.int8, (m, n), "codes"), 0)
+        keep.append((V, C))
+    size = ctypes.c_size_t(0)
+    o = ctypes.byref(opts) if opts is not None else None
+    _check(lib().bakron_batch_workspace_size(len(problems), arr, o, ctypes.byref(size)),
+           "bakron_batch_workspace_size")
+    ws = _ws(size.value, workspace)
+    st = lib().bakron_quantize_batch(len(problems), arr, o, ctypes.c_void_p(ws.data_ptr()),
+                                     size.value, _stream(stream))
+    if st != OK:
+        err = BakronError(st, "bakron_quantize_batch")
+        err.statuses = [arr[k].status for k in range(len(problems))]
+        raise err
+    return keep
 
 
 def bakron_quantize_antidiag(W, UA, UB, scale, qmin, qmax, guide_codes=None, guide_tol=1e-4,

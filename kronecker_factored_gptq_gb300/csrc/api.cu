@@ -31,6 +31,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <thread>
 #include <utility>
 #include <vector>
 
@@ -381,15 +382,19 @@ struct SolveStreams {
   std::mutex mu;
 };
 
-cudaError_t solve_streams(SolveStreams** out) {
+// Stream sets per device: slot 0 serves the single-problem calls, slots
+// 0 .. kSlots-1 the problems of a batch (one set per concurrent problem).
+constexpr int kSlots = 8;
+
+cudaError_t solve_streams(SolveStreams** out, int slot = 0) {
   static std::mutex mu;
-  static SolveStreams per_dev[64];
+  static SolveStreams per_dev[64][kSlots];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64 || slot < 0 || slot >= kSlots) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(mu);
-  SolveStreams& ss = per_dev[dev];
+  SolveStreams& ss = per_dev[dev][slot];
   if (!ss.crit) {
     int lo = 0, hi = 0;
     if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
@@ -481,6 +486,16 @@ bool sizes_ok(int64_t m, int64_t n) { return m >= 1 && n >= 1 && m <= (1 << 20) 
 // The one-sided solve (U_B = I): see RowsSchedule.  Arguments validated by
 // bakron_quantize; the workspace layout is the two-sided one (its Y^T and
 // U_B^T regions stay unused).
+// One problem of a batch: the stream set it runs on (locked by the caller),
+// that set's event pool position, and what the call leaves for the caller:
+// the event recorded at its end on the critical stream and its status block.
+struct BatchCtx {
+  SolveStreams* ss;
+  size_t* nev;
+  cudaEvent_t done;
+  DevStatus* st;
+};
+
 // A validated grid: scale / zero point per (row, group of `group` columns).
 struct GridIn {
   const float* scale;
@@ -490,13 +505,15 @@ struct GridIn {
 
 bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* UA, const GridIn& gr,
                             int qmin, int qmax, float* V, int8_t* codes, float* preround,
-                            const bakron_opts& o, void* ws, cudaStream_t s) {
+                            const bakron_opts& o, void* ws, cudaStream_t s, BatchCtx* bctx) {
   const QLayout L = quantize_layout(m, n);
   const RowsSchedule& sch = get_rows_schedule((int)L.M, (int)L.N);
-  SolveStreams* ss = nullptr;
-  TRY_CUDA(solve_streams(&ss));
-  std::lock_guard<std::mutex> slk(ss->mu);
-  size_t nev = 0;
+  SolveStreams* ss = bctx ? bctx->ss : nullptr;
+  if (!ss) TRY_CUDA(solve_streams(&ss));
+  std::unique_lock<std::mutex> slk(ss->mu, std::defer_lock);
+  if (!bctx) slk.lock();
+  size_t nev_own = 0;
+  size_t& nev = bctx ? *bctx->nev : nev_own;
   auto next_event = [&](cudaEvent_t* ev) { return pool_event(ss, nev++, ev); };
   char* base = (char*)ws;
   DevStatus* st = (DevStatus*)(base + L.status);
@@ -509,10 +526,6 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   float* lathi = (float*)(base + L.lathi);
   float* latlo = (float*)(base + L.latlo);
   if (o.times) std::memset(o.times, 0, sizeof(*o.times));
-  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
-  if (!sch.items.empty())
-    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
-                                  cudaMemcpyHostToDevice, s));
   cudaStream_t cs = ss->crit;
   {
     cudaEvent_t ev;
@@ -520,6 +533,10 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     TRY_CUDA(cudaEventRecord(ev, s));
     TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
   }
+  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
+  if (!sch.items.empty())
+    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
+                             cudaMemcpyHostToDevice, cs));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
@@ -592,6 +609,11 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     cudaEvent_t ev;
     TRY_CUDA(next_event(&ev));
     TRY_CUDA(cudaEventRecord(ev, cs));
+    if (bctx) {
+      bctx->done = ev;
+      bctx->st = st;
+      return BAKRON_OK;
+    }
     TRY_CUDA(cudaStreamWaitEvent(s, ev, 0));
   }
   DevStatus h{};
@@ -738,10 +760,11 @@ namespace {
 bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* UA, const float* UB,
                             const GridIn& gr, int qmin, int qmax, float* V, int8_t* codes,
                             float* preround, const bakron_opts* opts_in, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            void* stream, BatchCtx* bctx = nullptr) {
   bakron_opts o;
   bakron_default_opts(&o);
   if (opts_in) o = *opts_in;
+  if (bctx) o.times = nullptr;
   if (!valid_opts(o)) return BAKRON_ERR_INVALID_ARG;
   if (!W || !UA || !gr.scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
   if (!sizes_ok(m, n) || qmin > qmax) return BAKRON_ERR_INVALID_ARG;
@@ -750,13 +773,15 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   if (o.use_3xtf32 && !prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
   if (!UB)
     return quantize_rows(W, m, n, UA, gr, qmin, qmax, V, codes, preround, o, ws,
-                         (cudaStream_t)stream);
+                         (cudaStream_t)stream, bctx);
   const Schedule& sch = get_schedule((int)L.M, (int)L.N);
   cudaStream_t s = (cudaStream_t)stream;
-  SolveStreams* ss = nullptr;
-  TRY_CUDA(solve_streams(&ss));
-  std::lock_guard<std::mutex> slk(ss->mu);
-  size_t nev = 0;
+  SolveStreams* ss = bctx ? bctx->ss : nullptr;
+  if (!ss) TRY_CUDA(solve_streams(&ss));
+  std::unique_lock<std::mutex> slk(ss->mu, std::defer_lock);
+  if (!bctx) slk.lock();
+  size_t nev_own = 0;
+  size_t& nev = bctx ? *bctx->nev : nev_own;
   auto next_event = [&](cudaEvent_t* ev) { return pool_event(ss, nev++, ev); };
   char* base = (char*)ws;
   DevStatus* st = (DevStatus*)(base + L.status);
@@ -772,10 +797,6 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   float* lbtlo = (float*)(base + L.lbtlo);
   if (o.times) std::memset(o.times, 0, sizeof(*o.times));
 
-  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
-  if (!sch.items.empty())
-    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
-                             cudaMemcpyHostToDevice, s));
   // fork onto the critical stream
   cudaStream_t cs = ss->crit;
   {
@@ -784,6 +805,10 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
     TRY_CUDA(cudaEventRecord(ev, s));
     TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
   }
+  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
+  if (!sch.items.empty())
+    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
+                             cudaMemcpyHostToDevice, cs));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
@@ -882,6 +907,11 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
     cudaEvent_t ev;
     TRY_CUDA(next_event(&ev));
     TRY_CUDA(cudaEventRecord(ev, cs));
+    if (bctx) {
+      bctx->done = ev;
+      bctx->st = st;
+      return BAKRON_OK;
+    }
     TRY_CUDA(cudaStreamWaitEvent(s, ev, 0));
   }
   DevStatus h{};
@@ -938,6 +968,95 @@ bakron_status bakron_grid_params(const float* W, int64_t m, int64_t n, int bits,
   TRY_CUDA(launch_grid_params(W, m, n, ng == 1 ? n : group, ng, bits, asymmetric, scale, zero, s));
   TRY_CUDA(cudaStreamSynchronize(s));
   return BAKRON_OK;
+}
+
+bakron_status bakron_batch_workspace_size(int count, const bakron_problem* p,
+                                          const bakron_opts* opts, size_t* bytes) {
+  if (count < 1 || !p || !bytes) return BAKRON_ERR_INVALID_ARG;
+  size_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    size_t b = 0;
+    bakron_status st = bakron_workspace_size(p[i].m, p[i].n, opts, &b);
+    if (st != BAKRON_OK) return st;
+    total += (b + 1023) / 1024 * 1024;
+  }
+  *bytes = total;
+  return BAKRON_OK;
+}
+
+bakron_status bakron_quantize_batch(int count, bakron_problem* p, const bakron_opts* opts, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  size_t need = 0;
+  bakron_status vs = bakron_batch_workspace_size(count, p, opts, &need);
+  if (vs != BAKRON_OK) return vs;
+  if (!ws || ws_bytes < need) return BAKRON_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    p[i].status = BAKRON_OK;
+    if (grid_groups(p[i].n, p[i].group) < 1) return BAKRON_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int nslots = std::min(count, kSlots);
+  std::vector<SolveStreams*> sets(nslots, nullptr);
+  std::vector<std::unique_lock<std::mutex>> locks;
+  std::vector<size_t> nev(nslots, 0);
+  for (int k = 0; k < nslots; ++k) {
+    TRY_CUDA(solve_streams(&sets[k], k));
+    locks.emplace_back(sets[k]->mu);
+  }
+  std::vector<BatchCtx> ctx(count);
+  std::vector<int> enq(count, 0);
+  std::vector<size_t> offs(count + 1, 0);
+  for (int i = 0; i < count; ++i) {
+    size_t b = 0;
+    bakron_workspace_size(p[i].m, p[i].n, opts, &b);
+    offs[i + 1] = offs[i] + (b + 1023) / 1024 * 1024;
+  }
+  (void)prop_tc_supported();   // cached before the enqueuing threads start
+  int dev = 0;
+  TRY_CUDA(cudaGetDevice(&dev));
+  // one host thread per stream set enqueues its problems, so a launch queue
+  // that fills up for one problem does not hold back the others
+  auto enqueue_slot = [&](int k) {
+    if (cudaSetDevice(dev) != cudaSuccess) {
+      for (int i = k; i < count; i += nslots) p[i].status = BAKRON_ERR_CUDA;
+      return;
+    }
+    for (int i = k; i < count; i += nslots) {
+      const int64_t ng = grid_groups(p[i].n, p[i].group);
+      const GridIn gr{p[i].scale, p[i].zero, ng == 1 ? p[i].n : p[i].group, ng};
+      ctx[i].ss = sets[k];
+      ctx[i].nev = &nev[k];
+      const bakron_status st = quantize_impl(
+          p[i].W, p[i].m, p[i].n, p[i].UA, p[i].UB, gr, p[i].qmin, p[i].qmax, p[i].V, p[i].codes,
+          nullptr, opts, (char*)ws + offs[i], offs[i + 1] - offs[i], stream, &ctx[i]);
+      p[i].status = st;
+      enq[i] = st == BAKRON_OK;
+    }
+  };
+  {
+    std::vector<std::thread> th;
+    for (int k = 1; k < nslots; ++k) th.emplace_back(enqueue_slot, k);
+    enqueue_slot(0);
+    for (auto& t : th) t.join();
+  }
+  bakron_status first = BAKRON_OK;
+  for (int i = 0; i < count; ++i)
+    if (!enq[i] && first == BAKRON_OK) first = (bakron_status)p[i].status;
+  // join every enqueued problem onto the caller's stream, then read the
+  // status blocks
+  std::vector<DevStatus> hs(count);
+  for (int i = 0; i < count; ++i)
+    if (enq[i]) TRY_CUDA(cudaStreamWaitEvent(s, ctx[i].done, 0));
+  for (int i = 0; i < count; ++i)
+    if (enq[i])
+      TRY_CUDA(cudaMemcpyAsync(&hs[i], ctx[i].st, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  TRY_CUDA(cudaStreamSynchronize(s));
+  for (int i = 0; i < count; ++i)
+    if (enq[i]) {
+      p[i].status = hs[i].status;
+      if (first == BAKRON_OK && hs[i].status != BAKRON_OK) first = (bakron_status)hs[i].status;
+    }
+  return first;
 }
 
 bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n, const float* UA,
