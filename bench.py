@@ -334,7 +334,7 @@ def run_ours(args, world, rank, local):
         bound = "alu"
     roofline = {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_src": peaks["src"] + (" (bf16 x 1.1/2.25, sustained)" if use_tc else
+                "peak_src": peaks["src"] + (" (bf16 x 1.1/2.25, sustained)" if bound == "tensor" else
                                              " (152 SMs x 128 FP32 lanes x 2 x max SM clock)"),
                 "traffic": (traffic_per_launch("kronecker_factored_gptq_gb300/csrc/prop_tc.cu",
                                                "profiles/prop_tc_kernel_c8192_traffic.md")

@@ -535,8 +535,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   }
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
   if (!sch.items.empty())
-    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
-                             cudaMemcpyHostToDevice, cs));
+    TRY_CUDA(upload_items(sch.items.data(), sch.items.size(), items, cs));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
@@ -807,8 +806,7 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   }
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
   if (!sch.items.empty())
-    TRY_CUDA(cudaMemcpyAsync(items, sch.items.data(), sizeof(WorkItem) * sch.items.size(),
-                             cudaMemcpyHostToDevice, cs));
+    TRY_CUDA(upload_items(sch.items.data(), sch.items.size(), items, cs));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();

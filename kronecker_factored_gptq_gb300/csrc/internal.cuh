@@ -107,6 +107,11 @@ cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
 }
 
+// Copy a cached host work list into the workspace (see misc.cu); the
+// no-allocation entry point sets the thread flag for the length of its call.
+cudaError_t upload_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s);
+void set_no_host_alloc(bool on);
+
 // Process-wide count of kernel launches made by the library.
 void count_launch(int k = 1);
 long long launches_so_far();

@@ -1,6 +1,10 @@
 // Small bandwidth-bound kernels: the row grid, padding, and the transposed
 // 3xTF32 split of the update factors.
 #include <atomic>
+#include <map>
+#include <mutex>
+
+#include <cstring>
 
 #include "internal.cuh"
 
@@ -226,6 +230,71 @@ cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cu
   if (count == 0) return cudaSuccess;
   count_launch();
   check_positive_finite_kernel<<<grid_for(count, 256), 256, 0, s>>>(x, count, st);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ work-item upload
+// The host-built work lists of a cached schedule are staged once in mapped
+// pinned host memory and copied into the workspace by a kernel that reads
+// them over the host link.  A DMA copy would queue on the host-to-device
+// copy engine behind any large transfer the caller has in flight (such as
+// the next problem's inputs) and stall the solve.  Calls that must not
+// allocate (thread flag) use a plain asynchronous copy instead.
+__global__ void copy_items_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+namespace {
+thread_local bool t_no_host_alloc = false;
+struct Staged {
+  void* host = nullptr;
+  const void* dev = nullptr;
+  size_t bytes = 0;
+};
+}  // namespace
+
+void set_no_host_alloc(bool on) { t_no_host_alloc = on; }
+
+cudaError_t upload_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s) {
+  if (count == 0) return cudaSuccess;
+  const size_t bytes = sizeof(WorkItem) * count;
+  if (t_no_host_alloc)
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, Staged> cache;   // (list, device)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const void* dptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    Staged& st = cache[std::make_pair((const void*)src, dev)];
+    if (st.bytes != bytes) {
+      // the cached lists never change or move; a list seen with another
+      // size is a new list at a reused address
+      if (st.host) cudaFreeHost(st.host);
+      st = Staged{};
+      void* h = nullptr;
+      if ((e = cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess)
+        return e;
+      std::memcpy(h, src, bytes);
+      void* d = nullptr;
+      if ((e = cudaHostGetDevicePointer(&d, h, 0)) != cudaSuccess) {
+        cudaFreeHost(h);
+        return e;
+      }
+      st.host = h;
+      st.dev = d;
+      st.bytes = bytes;
+    }
+    dptr = st.dev;
+  }
+  const int64_t n16 = (int64_t)(bytes / 16);
+  count_launch();
+  copy_items_kernel<<<grid_for(n16, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(dptr),
+                                                        reinterpret_cast<uint4*>(dst), n16);
   return cudaGetLastError();
 }
 

@@ -426,8 +426,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   }
   const PrepItems& P = prep_items(kp);
   if (!P.items.empty())
-    BK_TRY(cudaMemcpyAsync(a.items, P.items.data(), sizeof(WorkItem) * P.items.size(),
-                           cudaMemcpyHostToDevice, s));
+    BK_TRY(upload_items(P.items.data(), P.items.size(), a.items, s));
   count_launch();
   diag_mean_kernel<<<1, 256, 0, s>>>(a.X, k, a.damp, a.scal);
   BK_TRY(cudaGetLastError());
