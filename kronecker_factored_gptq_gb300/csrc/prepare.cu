@@ -140,31 +140,30 @@ constexpr int PB = 16;                 // panel width
 constexpr int PP = NB + 1;             // shared pitch (odd: row and column walks are conflict-free)
 constexpr size_t kPotrfSmem = sizeof(float) * (3 * NB * PP + NB);
 
-// One 4 x 4 tile (rows m0.., columns n0..) of C = alpha * A * B, all in
+// One 4 x 2 tile (rows m0.., columns n0..) of C = alpha * A * B, all in
 // shared memory with pitch PP, K range [k0, k1).
 __device__ __forceinline__ void tile_mm(float* C, const float* A, const float* B, int m0, int n0,
                                         int k0, int k1, float alpha) {
-  float acc[4][4];
+  float acc[4][2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
 #pragma unroll 4
   for (int k = k0; k < k1; ++k) {
-    float a[4], b[4];
+    float a[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[i] = A[(m0 + i) * PP + k];
+    const float b0 = B[k * PP + n0], b1 = B[k * PP + n0 + 1];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = B[k * PP + n0 + j];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    for (int i = 0; i < 4; ++i) {
+      acc[i][0] = fmaf(a[i], b0, acc[i][0]);
+      acc[i][1] = fmaf(a[i], b1, acc[i][1]);
+    }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) C[(m0 + i) * PP + n0 + j] = alpha * acc[i][j];
+  for (int i = 0; i < 4; ++i) {
+    C[(m0 + i) * PP + n0] = alpha * acc[i][0];
+    C[(m0 + i) * PP + n0 + 1] = alpha * acc[i][1];
+  }
 }
 
 __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi, float* Gilo,
@@ -188,47 +187,79 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
     X[r * PP + c] = 0.f;
   }
   __syncthreads();
-  for (int sb = 0; sb < NB / PB; ++sb) {
-    const int q = sb * PB;
-    // (1) diagonal 16 x 16 block: warp 0, lanes r and r + 16 hold row r
-    if (warp == 0) {
-      const int r = lane & (PB - 1);
-      float a[PB];
+  // (1) the diagonal 16 x 16 block of panel q / PB: warp 0, lanes r and
+  // r + 16 hold row r; pivots through rsqrt, 1 / pivot kept in dinv
+  auto factor_diag = [&](int q) {
+    const int r = lane & (PB - 1);
+    float a[PB];
 #pragma unroll
-      for (int c = 0; c < PB; ++c) a[c] = (c <= r) ? G[(q + r) * PP + q + c] : 0.f;
-      int badj = -1;   // first non-positive or non-finite pivot (replaced by 1)
+    for (int c = 0; c < PB; ++c) a[c] = (c <= r) ? G[(q + r) * PP + q + c] : 0.f;
+    int badj = -1;   // first non-positive or non-finite pivot (replaced by 1)
 #pragma unroll
-      for (int j = 0; j < PB; ++j) {
-        float d = __shfl_sync(FULLM, a[j], j);
-        const bool bad = !(d > 0.f) || !isfinite(d);
-        if (bad && badj < 0) badj = j;
-        d = bad ? 1.f : d;
-        const float inv = rsqrtf(d);
-        const float l = a[j] * inv;
-        if (r == j) a[j] = d * inv;
-        else if (r > j) a[j] = l;
-        if (lane == 0) dinv[q + j] = inv;
+    for (int j = 0; j < PB; ++j) {
+      float d = __shfl_sync(FULLM, a[j], j);
+      const bool bad = !(d > 0.f) || !isfinite(d);
+      if (bad && badj < 0) badj = j;
+      d = bad ? 1.f : d;
+      const float inv = rsqrtf(d);
+      const float l = a[j] * inv;
+      if (r == j) a[j] = d * inv;
+      else if (r > j) a[j] = l;
+      if (lane == 0) dinv[q + j] = inv;
 #pragma unroll
-        for (int k = 0; k < PB; ++k) {
-          if (k > j) {
-            const float lk = __shfl_sync(FULLM, l, k);
-            if (r >= k) a[k] = fmaf(-l, lk, a[k]);
-          }
+      for (int k = 0; k < PB; ++k) {
+        if (k > j) {
+          const float lk = __shfl_sync(FULLM, l, k);
+          if (r >= k) a[k] = fmaf(-l, lk, a[k]);
         }
       }
-      if (lane < PB) {
-#pragma unroll
-        for (int c = 0; c < PB; ++c)
-          if (c <= r) G[(q + r) * PP + q + c] = a[c];
-      }
-      if (lane == 0 && badj >= 0 && o + q + badj < k_real) {
-        atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + badj));
-        set_status(st, BAKRON_ERR_NOT_PD);
-      }
     }
-    __syncthreads();
-    const int base = q + PB, n2 = NB - base;
-    if (n2 <= 0) break;
+    if (lane < PB) {
+#pragma unroll
+      for (int c = 0; c < PB; ++c)
+        if (c <= r) G[(q + r) * PP + q + c] = a[c];
+    }
+    if (lane == 0 && badj >= 0 && o + q + badj < k_real) {
+      atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + badj));
+      set_status(st, BAKRON_ERR_NOT_PD);
+    }
+  };
+  // (3) one 4 x 4 tile (ti, tj), tj <= ti, of the trailing lower triangle
+  // from row / column `base` on: G[i][j] -= sum_t L21[i][t] L21[j][t] over the
+  // panel's columns q .. q + 15 (reads columns q.., writes columns >= base)
+  auto trail_tile = [&](int q, int base, int ti, int tj) {
+    const int i0 = base + 4 * ti, j0 = base + 4 * tj;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+    for (int tt = 0; tt < PB; ++tt) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = G[(i0 + i) * PP + q + tt];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = G[(j0 + j) * PP + q + tt];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j0 + j <= i0 + i) G[(i0 + i) * PP + j0 + j] -= acc[i][j];
+  };
+
+  // Panel loop with one panel of lookahead: the columns of the next panel
+  // are updated first, then warp 0 factors the next diagonal block while the
+  // other warps finish the trailing update.
+  if (warp == 0) factor_diag(0);
+  __syncthreads();
+  for (int sb = 0; sb < NB / PB - 1; ++sb) {
+    const int q = sb * PB, base = q + PB, n2 = NB - base, tn = n2 / 4;
     // (2) rows below: l = g L11^{-T}, one thread per row, column by column
     if (tid < n2) {
       const int r = base + tid;
@@ -245,38 +276,23 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
       for (int c = 0; c < PB; ++c) G[r * PP + q + c] = l[c];
     }
     __syncthreads();
-    // (3) trailing lower triangle: G[i][j] -= sum_t L21[i][t] L21[j][t] over
-    // 4 x 4 tiles (ti, tj), tj <= ti; reads columns q.., writes columns >= base
-    {
-      const int tn = n2 / 4, ntiles = tn * (tn + 1) / 2;
-      for (int t = tid; t < ntiles; t += NT) {
+    // (3a) the next panel's columns: tiles with tj < 4
+    for (int t = tid; t < 4 * tn; t += NT) {
+      const int ti = t >> 2, tj = t & 3;
+      if (tj <= ti) trail_tile(q, base, ti, tj);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      factor_diag(base);
+    } else {
+      // (3b) the other columns (tj >= 4), on warps 1 .. 15
+      const int nb = tn - 4, ntiles = nb > 0 ? nb * (nb + 1) / 2 : 0;
+      for (int t = tid - 32; t < ntiles; t += NT - 32) {
         int ti = (int)((sqrtf(8.f * (float)t + 1.f) - 1.f) * 0.5f);
         while ((ti + 1) * (ti + 2) / 2 <= t) ++ti;
         while (ti * (ti + 1) / 2 > t) --ti;
         const int tj = t - ti * (ti + 1) / 2;
-        const int i0 = base + 4 * ti, j0 = base + 4 * tj;
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 4
-        for (int tt = 0; tt < PB; ++tt) {
-          float av[4], bv[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) av[i] = G[(i0 + i) * PP + q + tt];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) bv[j] = G[(j0 + j) * PP + q + tt];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j0 + j <= i0 + i) G[(i0 + i) * PP + j0 + j] -= acc[i][j];
+        trail_tile(q, base, ti + 4, tj + 4);
       }
     }
     __syncthreads();
@@ -303,31 +319,55 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
   //   S21 = G21 inv(G11)   (inv(G11) lower: K starts at the tile's first column)
   //   X21 = -inv(G22) S21  (inv(G22) lower: K ends after the tile's last row)
   for (int b = PB; b < NB; b *= 2) {
-    const int tb = b / 4, tpp = tb * tb, total = (NB / (2 * b)) * tpp;
+    const int tm = b / 4, tn = b / 2, tpp = tm * tn, total = (NB / (2 * b)) * tpp;   // 4 x 2 tiles
+    // first product: K starts at the tile's first column, so the rows vary
+    // fastest and a warp's tiles share their K range
     for (int t = tid; t < total; t += NT) {
       const int p0 = (t / tpp) * 2 * b, w = t % tpp;
-      const int m0 = (w / tb) * 4, n0 = (w % tb) * 4;
+      const int m0 = (w % tm) * 4, n0 = (w / tm) * 2;
       tile_mm(S + (p0 + b) * PP + p0, G + (p0 + b) * PP + p0, X + p0 * PP + p0, m0, n0, n0, b, 1.f);
     }
     __syncthreads();
     for (int t = tid; t < total; t += NT) {
       const int p0 = (t / tpp) * 2 * b, w = t % tpp;
-      const int m0 = (w / tb) * 4, n0 = (w % tb) * 4;
+      const int m0 = (w / tn) * 4, n0 = (w % tn) * 2;   // K ends after the tile's last row
       tile_mm(X + (p0 + b) * PP + p0, X + (p0 + b) * PP + p0 + b, S + (p0 + b) * PP + p0, m0, n0, 0,
               min(b, m0 + 4), -1.f);
     }
     __syncthreads();
   }
   grid_dep_launch();
+  // the split and transposed-split copies of the inverse are only read
+  // after the whole chain: split_diag_kernel forms them from the plain
+  // copy left in Gihi's diagonal block
   for (int idx = tid; idx < NB * NB; idx += NT) {
     const int r = idx / NB, c = idx - r * NB;
     C[(o + r) * kp + o + c] = (c <= r) ? G[r * PP + c] : 0.f;
     const float x = (c <= r) ? X[r * PP + c] : 0.f;
+    Gihi[(o + r) * kp + o + c] = x;
+    inv_plain[r * NB + c] = x;
+  }
+}
+
+// For every diagonal 128-block kb: the plain inverse block x in Gihi becomes
+// (Gihi, Gilo) = split(x) and (GiThi, GiTlo) = split(x^T).  One CTA per block,
+// the block read whole into shared memory before any write.
+__global__ void __launch_bounds__(512) split_diag_kernel(float* Gihi, float* Gilo, float* GiThi,
+                                                         float* GiTlo, int64_t kp) {
+  extern __shared__ __align__(16) float xs[];   // [NB][PP]
+  const int64_t o = (int64_t)blockIdx.x * NB;
+  for (int idx = threadIdx.x; idx < NB * NB; idx += blockDim.x) {
+    const int r = idx / NB, c = idx - r * NB;
+    xs[r * PP + c] = Gihi[(o + r) * kp + o + c];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < NB * NB; idx += blockDim.x) {
+    const int r = idx / NB, c = idx - r * NB;
+    const float x = xs[r * PP + c];
     const float h = tf32_round(x);
     Gihi[(o + r) * kp + o + c] = h;
     Gilo[(o + r) * kp + o + c] = x - h;
-    inv_plain[r * NB + c] = x;
-    const float xt = (r <= c) ? X[c * PP + r] : 0.f;
+    const float xt = xs[c * PP + r];
     const float ht = tf32_round(xt);
     GiThi[(o + r) * kp + o + c] = ht;
     GiTlo[(o + r) * kp + o + c] = xt - ht;
@@ -422,6 +462,8 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   if (!attr_set) {
     BK_TRY(cudaFuncSetAttribute(potrf_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kPotrfSmem));
+    BK_TRY(cudaFuncSetAttribute(split_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(sizeof(float) * NB * PP)));
     attr_set = true;
   }
   const PrepItems& P = prep_items(kp);
@@ -494,7 +536,12 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     const int64_t last = (nblk >= 2 ? nblk - 2 : 0);
     BK_TRY(cudaStreamWaitEvent(s, a.ev[3 * last + 2], 0));
   }
-  // G^{-1} by recursive doubling (tensor cores)
+  // split forms of the diagonal inverse blocks, then G^{-1} by recursive
+  // doubling (tensor cores)
+  count_launch();
+  split_diag_kernel<<<(unsigned)nblk, 512, sizeof(float) * NB * PP, s>>>(a.Gihi, a.Gilo, a.GiThi,
+                                                                        a.GiTlo, kp);
+  BK_TRY(cudaGetLastError());
   for (size_t lvl = 0; lvl < P.t_off.size(); ++lvl) {
     PropArgs t{};
     t.A_hi = a.GiThi; t.A_lo = a.GiTlo; t.lda = kp; t.a_rows = kp;
