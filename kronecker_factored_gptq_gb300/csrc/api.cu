@@ -330,7 +330,8 @@ PLayout prepare_layout(int64_t n, int64_t m) {
 // reusable events.  Held under a lock for the whole (synchronous) call.
 struct PrepStreams {
   cudaStream_t main[2] = {};       // high priority: the diagonal-block chains
-  cudaStream_t side[2] = {};       // low priority: lookahead panels and updates
+  cudaStream_t side[2] = {};       // lower priority: lookahead panels and updates
+  cudaStream_t bulk[2] = {};       // lowest priority: updates needed two steps later
   cudaEvent_t fork = nullptr, join = nullptr;
   std::vector<cudaEvent_t> events;
   std::mutex mu;
@@ -351,7 +352,10 @@ cudaError_t prep_streams(PrepStreams** out) {
     for (int w = 0; w < 2; ++w) {
       if ((e = cudaStreamCreateWithPriority(&a.main[w], cudaStreamNonBlocking, hi)) != cudaSuccess)
         return e;
-      if ((e = cudaStreamCreateWithPriority(&a.side[w], cudaStreamNonBlocking, lo)) != cudaSuccess)
+      if ((e = cudaStreamCreateWithPriority(&a.side[w], cudaStreamNonBlocking, (lo + hi) / 2)) !=
+          cudaSuccess)
+        return e;
+      if ((e = cudaStreamCreateWithPriority(&a.bulk[w], cudaStreamNonBlocking, lo)) != cudaSuccess)
         return e;
     }
     if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
@@ -701,7 +705,7 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   PrepStreams* ps = nullptr;
   TRY_CUDA(prep_streams(&ps));
   std::lock_guard<std::mutex> plk(ps->mu);
-  const size_t ev_per = 3 * (size_t)(std::max(L.kp[0], L.kp[1]) / T + 1);
+  const size_t ev_per = 5 * (size_t)(std::max(L.kp[0], L.kp[1]) / T + 1);
   TRY_CUDA(prep_events(ps, 2 * ev_per));
   TRY_CUDA(cudaEventRecord(ps->fork, s));
   for (int which = 0; which < 2; ++which) {
@@ -714,6 +718,7 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
     cudaEvent_t start = ps->events[which * ev_per + ev_per - 1];
     TRY_CUDA(cudaEventRecord(start, fs));
     TRY_CUDA(cudaStreamWaitEvent(ps->side[which], start, 0));
+    TRY_CUDA(cudaStreamWaitEvent(ps->bulk[which], start, 0));
     PrepareFactorArgs pa{};
     pa.X = X; pa.k = k; pa.damp = which == 0 ? damp_A : damp_B;
     pa.U = which == 0 ? UA : UB;
@@ -733,6 +738,7 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
     pa.which = which;
     pa.st = st;
     pa.side = ps->side[which];
+    pa.bulk = ps->bulk[which];
     pa.ev = ps->events.data() + which * ev_per;
     TRY_CUDA(run_prepare_factor(pa, fs));
     // join the factor's chain back onto the caller's stream

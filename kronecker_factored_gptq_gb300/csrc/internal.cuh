@@ -165,7 +165,8 @@ struct PrepareFactorArgs {
   int which;                     // 0 = A, 1 = B (info slot)
   DevStatus* st;
   cudaStream_t side;             // lookahead stream of this factor
-  cudaEvent_t* ev;               // 3 * (kp / 128) events
+  cudaStream_t bulk;             // lowest-priority stream of this factor
+  cudaEvent_t* ev;               // 5 * (kp / 128) events
 };
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s);
 int64_t prepare_pad(int64_t k);

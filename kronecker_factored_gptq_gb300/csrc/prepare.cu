@@ -409,7 +409,9 @@ namespace {
 // every doubling level the T^T tiles and the X21 tiles.
 struct PrepItems {
   std::vector<WorkItem> items;
-  std::vector<int> syrk_off, syrk_n;   // per kb
+  // per kb: the urgent tile (kb+1, kb+1) at syrk_off, then syrk_n1 tiles of
+  // column kb+1 and tile (kb+2, kb+2), then syrk_n2 other tiles
+  std::vector<int> syrk_off, syrk_n1, syrk_n2;
   std::vector<int> t_off, t_n, x_off, x_n, t_maxk, x_maxk;  // per level
 };
 
@@ -423,9 +425,16 @@ const PrepItems& prep_items(int64_t kp) {
   const int nb = (int)(kp / NB);
   for (int kb = 0; kb < nb; ++kb) {
     P.syrk_off.push_back((int)P.items.size());
-    for (int r = kb + 1; r < nb; ++r)
-      for (int c = kb + 1; c <= r; ++c) P.items.push_back(WorkItem{r, c, kb, kb + 1});
-    P.syrk_n.push_back((int)P.items.size() - P.syrk_off.back());
+    if (kb + 1 < nb) P.items.push_back(WorkItem{kb + 1, kb + 1, kb, kb + 1});
+    const size_t s1 = P.items.size();
+    for (int r = kb + 2; r < nb; ++r) P.items.push_back(WorkItem{r, kb + 1, kb, kb + 1});
+    if (kb + 2 < nb) P.items.push_back(WorkItem{kb + 2, kb + 2, kb, kb + 1});
+    P.syrk_n1.push_back((int)(P.items.size() - s1));
+    const size_t s2 = P.items.size();
+    for (int r = kb + 3; r < nb; ++r)
+      for (int c = kb + 2; c <= r; ++c)
+        if (!(r == kb + 2 && c == kb + 2)) P.items.push_back(WorkItem{r, c, kb, kb + 1});
+    P.syrk_n2.push_back((int)(P.items.size() - s2));
   }
   for (int B = 1; B < nb; B *= 2) {
     P.t_off.push_back((int)P.items.size());
@@ -475,18 +484,24 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   count_launch();
   flip_damp_kernel<<<grid_for(kp * kp), 256, 0, s>>>(a.X, k, a.scal, a.C, kp);
   BK_TRY(cudaGetLastError());
-  // Right-looking blocked Cholesky with one block column of lookahead.  On
-  // the factor's stream: the diagonal block kb, then the part of step kb
-  // that block kb+1 needs (panel row block kb+1, its split, and the update
-  // of tile (kb+1, kb+1)).  On the side stream: the rest of the panel and of
-  // the trailing update.  Step kb's urgent part waits for the side work of
-  // step kb-1 (it updated the column kb tiles).  Each factor uses three
-  // events per block column.  The 128 x 128 inverse of the diagonal block
-  // alternates between two scratch buffers, because the side stream may
-  // still be reading block kb's while block kb+1 is factored.
+  // Right-looking blocked Cholesky with lookahead, on three streams per
+  // factor.  Main (high priority): the diagonal block kb, then what block
+  // kb+1 needs from step kb (panel row block kb+1, tile (kb+1, kb+1)).
+  // Lookahead stream: the rest of step kb's panel, then S1(kb) = the
+  // trailing tiles of column kb+1 and tile (kb+2, kb+2) (what step kb+1
+  // reads).  Bulk stream (lowest priority): S2(kb) = the other trailing
+  // tiles, needed two steps later.  Every tile receives its updates in a
+  // fixed order (S2 of earlier steps, then S1, then the urgent update), so
+  // the result is the same bit for bit on every run: S1(kb) waits for
+  // S2(kb-1), and step kb's urgent part waits for S1(kb-1).  Events per
+  // block column: ev_pot, ev_urg, ev_pan, ev_s1, ev_s2.  The 128 x 128
+  // inverse of the diagonal block alternates between two scratch buffers,
+  // because the lookahead stream may still read block kb's while block kb+1
+  // is factored (potrf(kb+2) runs after S1(kb), which follows panel(kb)).
   float* invbuf[2] = {a.Tlo, a.Tlo + NB * NB};
   const PrepItems& PI = P;
   bool side_used = false;
+  int64_t last = 0;
   for (int64_t kb = 0; kb < nblk; ++kb) {
     float* inv_plain = invbuf[kb & 1];
     count_launch();
@@ -494,9 +509,10 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
                          a.Gilo, a.GiThi, a.GiTlo, inv_plain, kp, kb, k, a.st, a.which));
     const int64_t rest = kp - (kb + 1) * NB;
     if (rest <= 0) break;
-    cudaEvent_t ev_pot = a.ev[3 * kb], ev_urg = a.ev[3 * kb + 1], ev_def = a.ev[3 * kb + 2];
+    cudaEvent_t* ev = a.ev + 5 * kb;
+    cudaEvent_t ev_pot = ev[0], ev_urg = ev[1], ev_pan = ev[2], ev_s1 = ev[3], ev_s2 = ev[4];
     BK_TRY(cudaEventRecord(ev_pot, s));
-    if (kb >= 1) BK_TRY(cudaStreamWaitEvent(s, a.ev[3 * (kb - 1) + 2], 0));
+    if (kb >= 1) BK_TRY(cudaStreamWaitEvent(s, a.ev[5 * (kb - 1) + 3], 0));
     float* panel = a.C + (kb + 1) * NB * kp + kb * NB;
     const int64_t off = (kb + 1) * NB * kp + kb * NB;
     // P = panel inv(G_kk)^T in place, plus its split, for rows [r0, r0 + rows)
@@ -519,22 +535,29 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
       q.st = a.st;
       return launch_prop_tc(q, str);
     };
-    // urgent: row block kb+1 and tile (kb+1, kb+1) (the first syrk item)
+    // urgent: row block kb+1 and tile (kb+1, kb+1)
     BK_TRY(panel_rows(0, NB, s, true));
     BK_TRY(cudaEventRecord(ev_urg, s));
     BK_TRY(syrk(PI.syrk_off[kb], 1, s, false));
-    // deferred: the other panel rows and trailing tiles
     side_used = true;
+    last = kb;
+    // lookahead stream: the other panel rows, then S1(kb)
     BK_TRY(cudaStreamWaitEvent(a.side, ev_pot, 0));
     if (rest > NB) BK_TRY(panel_rows(NB, rest - NB, a.side, false));
+    BK_TRY(cudaEventRecord(ev_pan, a.side));
     BK_TRY(cudaStreamWaitEvent(a.side, ev_urg, 0));
-    BK_TRY(syrk(PI.syrk_off[kb] + 1, PI.syrk_n[kb] - 1, a.side, false));
-    BK_TRY(cudaEventRecord(ev_def, a.side));
+    if (kb >= 1) BK_TRY(cudaStreamWaitEvent(a.side, a.ev[5 * (kb - 1) + 4], 0));
+    BK_TRY(syrk(PI.syrk_off[kb] + 1, PI.syrk_n1[kb], a.side, false));
+    BK_TRY(cudaEventRecord(ev_s1, a.side));
+    // bulk stream: S2(kb) (reads the panel rows below kb+1 only)
+    BK_TRY(cudaStreamWaitEvent(a.bulk, ev_pan, 0));
+    BK_TRY(syrk(PI.syrk_off[kb] + 1 + PI.syrk_n1[kb], PI.syrk_n2[kb], a.bulk, false));
+    BK_TRY(cudaEventRecord(ev_s2, a.bulk));
   }
   if (side_used) {
-    // the last deferred step joins the factor's stream before the inverse
-    const int64_t last = (nblk >= 2 ? nblk - 2 : 0);
-    BK_TRY(cudaStreamWaitEvent(s, a.ev[3 * last + 2], 0));
+    // the last deferred updates join the factor's stream before the inverse
+    BK_TRY(cudaStreamWaitEvent(s, a.ev[5 * last + 3], 0));
+    BK_TRY(cudaStreamWaitEvent(s, a.ev[5 * last + 4], 0));
   }
   // split forms of the diagonal inverse blocks, then G^{-1} by recursive
   // doubling (tensor cores)
