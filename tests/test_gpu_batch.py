@@ -76,3 +76,22 @@ def test_batch_reports_each_status():
     with pytest.raises(kb.BakronError) as ei:
         kb.bakron_quantize_batch(reqs)
     assert ei.value.status == 3 and ei.value.statuses == [0, 3]
+
+
+def test_batch_more_problems_than_stream_sets():
+    """Eleven problems on eight stream sets (three queue behind others)."""
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    probs = [_problem(70 + 13 * i, 90 + 7 * i, 100 + i, one_sided=(i % 3 == 2)) for i in range(11)]
+    reqs = []
+    for p in probs:
+        dW, dUA, ds = to_dev(p["w"].W, p["UA32"], p["s"])
+        req = dict(W=dW, UA=dUA, scale=ds, qmin=p["qmin"], qmax=p["qmax"])
+        if p["UB32"] is not None:
+            req["UB"] = to_dev(p["UB32"])[0]
+        reqs.append(req)
+    outs = kb.bakron_quantize_batch(reqs)
+    for p, (V, C) in zip(probs, outs):
+        w = p["w"]
+        UB = p["UB32"] if p["UB32"] is not None else np.eye(w.m, dtype=np.float32)
+        check_parity(w.W, p["UA32"], UB, p["s"], p["qmin"], p["qmax"], V.cpu().numpy(),
+                     C.cpu().numpy().astype(np.float64))

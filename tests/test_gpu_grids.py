@@ -156,3 +156,23 @@ def test_grid_full_size_strips():
         g = O.antidiag(w.W[:a, :b], UA64[:b, :b], UB64[:a, :a], sub, guide=c[:a, :b], guide_tol=TOL)
         assert np.count_nonzero(g.codes != c[:a, :b]) == 0
         assert g.overrides <= MAX_FRAC * a * b
+
+
+@pytest.mark.parametrize("m,n,group,one_sided", [(40, 100, 32, False), (33, 70, 64, True),
+                                                  (5, 40, 32, False)])
+def test_grid_ragged_groups_and_small_shapes(m, n, group, one_sided):
+    """Groups that do not divide n (the last group is short) and problems
+    smaller than one tile."""
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    w = WL.random_problem(m, n, seed=m * 11 + n, bits=4)
+    UA32, UB32 = shared_factors(w.A, w.damp_A, w.B, w.damp_B)
+    s, z, qmin, qmax = gpu_grid(w.W, 4, True, group)
+    _, s_ref, z_ref = oracle_grid_of(w.W, 4, True, group)
+    np.testing.assert_array_equal(s, s_ref)
+    np.testing.assert_array_equal(z, z_ref)
+    dW, dUA, dUB, ds, dz = to_dev(w.W, UA32, UB32, s, z)
+    V, c, pre = kb.bakron_quantize_grid(dW, dUA, None if one_sided else dUB, ds, dz, group, qmin, qmax,
+                                        want_preround=True)
+    grid = as_grid(s, z, qmin, qmax, group, n)
+    check_grid_parity(w.W, UA32, None if one_sided else UB32, grid, V.cpu().numpy(),
+                      c.cpu().numpy().astype(np.float64), pre.cpu().numpy(), one_sided=one_sided)
