@@ -323,15 +323,15 @@ PLayout prepare_layout(int64_t n, int64_t m) {
   return L;
 }
 
-// A second stream (and fork/join events) per device, created once, on which
-// the B factor is prepared while A runs on the caller's stream.
-// Streams of the factor preparation, per device, created once: the second
-// factor's main stream and one lookahead stream per factor, plus a pool of
-// reusable events.  Held under a lock for the whole (synchronous) call.
+// Streams of the factor preparation, per device, created once: four per
+// factor (the chain, its lookahead, the bulk updates, the rows of G^{-1}), so
+// the two factors are prepared side by side, plus fork/join events and a pool
+// of reusable events.  Held under a lock for the whole (synchronous) call.
 struct PrepStreams {
   cudaStream_t main[2] = {};       // high priority: the diagonal-block chains
   cudaStream_t side[2] = {};       // lower priority: lookahead panels and updates
   cudaStream_t bulk[2] = {};       // lowest priority: updates needed two steps later
+  cudaStream_t inv[2] = {};        // lowest priority: the block rows of G^{-1}
   cudaEvent_t fork = nullptr, join = nullptr;
   std::vector<cudaEvent_t> events;
   std::mutex mu;
@@ -356,6 +356,8 @@ cudaError_t prep_streams(PrepStreams** out) {
           cudaSuccess)
         return e;
       if ((e = cudaStreamCreateWithPriority(&a.bulk[w], cudaStreamNonBlocking, lo)) != cudaSuccess)
+        return e;
+      if ((e = cudaStreamCreateWithPriority(&a.inv[w], cudaStreamNonBlocking, lo)) != cudaSuccess)
         return e;
     }
     if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
@@ -708,17 +710,18 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   const size_t ev_per = 5 * (size_t)(std::max(L.kp[0], L.kp[1]) / T + 1);
   TRY_CUDA(prep_events(ps, 2 * ev_per));
   TRY_CUDA(cudaEventRecord(ps->fork, s));
-  for (int which = 0; which < 2; ++which) {
+  // enqueue one factor's preparation on its own streams, after the fork
+  auto enqueue = [&](int which) -> cudaError_t {
     const float* X = which == 0 ? A : B;
     const int64_t k = which == 0 ? n : m;
-    if (!X || k == 0) continue;
     cudaStream_t fs = ps->main[which];
-    TRY_CUDA(cudaStreamWaitEvent(fs, ps->fork, 0));
-    // the lookahead stream starts after the factor's stream reaches this point
+    cudaError_t e;
+    if ((e = cudaStreamWaitEvent(fs, ps->fork, 0)) != cudaSuccess) return e;
+    // the other streams start after the factor's stream reaches this point
     cudaEvent_t start = ps->events[which * ev_per + ev_per - 1];
-    TRY_CUDA(cudaEventRecord(start, fs));
-    TRY_CUDA(cudaStreamWaitEvent(ps->side[which], start, 0));
-    TRY_CUDA(cudaStreamWaitEvent(ps->bulk[which], start, 0));
+    if ((e = cudaEventRecord(start, fs)) != cudaSuccess) return e;
+    for (cudaStream_t o : {ps->side[which], ps->bulk[which], ps->inv[which]})
+      if ((e = cudaStreamWaitEvent(o, start, 0)) != cudaSuccess) return e;
     PrepareFactorArgs pa{};
     pa.X = X; pa.k = k; pa.damp = which == 0 ? damp_A : damp_B;
     pa.U = which == 0 ? UA : UB;
@@ -739,13 +742,33 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
     pa.st = st;
     pa.side = ps->side[which];
     pa.bulk = ps->bulk[which];
+    pa.inv = ps->inv[which];
     pa.ev = ps->events.data() + which * ev_per;
-    TRY_CUDA(run_prepare_factor(pa, fs));
-    // join the factor's chain back onto the caller's stream
-    cudaEvent_t done = ps->events[which * ev_per + ev_per - 2];
-    TRY_CUDA(cudaEventRecord(done, fs));
-    TRY_CUDA(cudaStreamWaitEvent(s, done, 0));
+    if ((e = run_prepare_factor(pa, fs)) != cudaSuccess) return e;
+    return cudaEventRecord(ps->events[which * ev_per + ev_per - 2], fs);
+  };
+  // Each factor's chain takes milliseconds of host time to enqueue, so with
+  // two factors B is enqueued from a second host thread and both chains start
+  // on the device together.
+  cudaError_t err[2] = {cudaSuccess, cudaSuccess};
+  const bool two = B && m > 0;
+  if (two) {
+    int dev = 0;
+    TRY_CUDA(cudaGetDevice(&dev));
+    std::thread tb([&] {
+      err[1] = cudaSetDevice(dev);
+      if (err[1] == cudaSuccess) err[1] = enqueue(1);
+    });
+    err[0] = enqueue(0);
+    tb.join();
+  } else {
+    err[0] = enqueue(0);
   }
+  TRY_CUDA(err[0]);
+  TRY_CUDA(err[1]);
+  // join the chains back onto the caller's stream
+  for (int which = 0; which < (two ? 2 : 1); ++which)
+    TRY_CUDA(cudaStreamWaitEvent(s, ps->events[which * ev_per + ev_per - 2], 0));
   DevStatus h{};
   bakron_status r = finish(s, st, &h);
   if (info) {

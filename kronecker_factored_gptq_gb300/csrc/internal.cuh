@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "bakron.h"
@@ -112,6 +114,12 @@ cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t upload_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s);
 void set_no_host_alloc(bool on);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: `done` is the call site's own flag word (bit d set
+// once device d is done), so concurrent callers and several devices are safe.
+cudaError_t ensure_smem_limit(const void* kernel, size_t bytes,
+                              std::atomic<unsigned long long>& done);
+
 // Process-wide count of kernel launches made by the library.
 void count_launch(int k = 1);
 long long launches_so_far();
@@ -158,7 +166,8 @@ struct PrepareFactorArgs {
   float* Chi; float* Clo;        // Kp x Kp: split panels of G (strictly lower blocks)
   float* Gihi; float* Gilo;      // Kp x Kp: split G^{-1} (lower)
   float* GiThi; float* GiTlo;    // Kp x Kp: split (G^{-1})^T (upper)
-  float* Thi; float* Tlo;        // Kp x Kp scratch: panel products, then T^T split
+  float* Thi; float* Tlo;        // Kp x Kp scratch: split sums of the inverse rows
+                                 // (upper tiles), diagonal inverses (last band)
   float* scal;                   // device scalar (lambda)
   WorkItem* items;               // device buffer of prepare_items_count(kp) items
   int64_t kp;
@@ -166,7 +175,8 @@ struct PrepareFactorArgs {
   DevStatus* st;
   cudaStream_t side;             // lookahead stream of this factor
   cudaStream_t bulk;             // lowest-priority stream of this factor
-  cudaEvent_t* ev;               // 5 * (kp / 128) events
+  cudaStream_t inv;              // lowest-priority stream: the rows of G^{-1}
+  cudaEvent_t* ev;               // 5 * (kp / 128) + 1 events
 };
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s);
 int64_t prepare_pad(int64_t k);

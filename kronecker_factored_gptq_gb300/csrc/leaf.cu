@@ -517,17 +517,11 @@ constexpr int kLeafBlock = 16;
 
 cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s) {
   constexpr int S = kLeafBlock;
-  static bool attr_set = false;
+  static std::atomic<unsigned long long> done[2];
   constexpr size_t smem = Cfg<S>::SMEM;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(leaf_kernel<S, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(leaf_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_limit((const void*)leaf_kernel<S, false>, smem, done[0]);
+  if (e == cudaSuccess) e = ensure_smem_limit((const void*)leaf_kernel<S, true>, smem, done[1]);
+  if (e != cudaSuccess) return e;
   count_launch();
   if (a.preround)
     return launch_kernel(leaf_kernel<S, true>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);

@@ -257,6 +257,18 @@ struct Staged {
 
 void set_no_host_alloc(bool on) { t_no_host_alloc = on; }
 
+cudaError_t ensure_smem_limit(const void* kernel, size_t bytes,
+                              std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 cudaError_t upload_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s) {
   if (count == 0) return cudaSuccess;
   const size_t bytes = sizeof(WorkItem) * count;

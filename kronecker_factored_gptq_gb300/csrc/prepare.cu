@@ -125,8 +125,8 @@ __global__ void flip_damp_kernel(const float* __restrict__ X, int64_t k, const f
 }
 
 // Factor the diagonal block C[kb, kb] (128 x 128) in shared memory; write
-// G_kk (lower, zero upper) back, inv(G_kk) split into Ginv's and (transposed)
-// into Ginv^T's diagonal block, and plainly into inv_plain (128 x 128).
+// G_kk (lower, zero upper) back and inv(G_kk) plainly into Ginv's diagonal
+// block (Gihi) and into inv_plain (128 x 128).
 //
 // Right-looking with 16-wide column panels: warp 0 factors the 16 x 16
 // diagonal block in registers (lane = row, shuffles), one thread per row
@@ -337,9 +337,9 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
     __syncthreads();
   }
   grid_dep_launch();
-  // the split and transposed-split copies of the inverse are only read
-  // after the whole chain: split_diag_kernel forms them from the plain
-  // copy left in Gihi's diagonal block
+  // the split and transposed-split copies of the inverse are not read by the
+  // chain: split_diag_kernel forms them, on the inverse's own stream, from the
+  // plain copy left in Gihi's diagonal block
   for (int idx = tid; idx < NB * NB; idx += NT) {
     const int r = idx / NB, c = idx - r * NB;
     C[(o + r) * kp + o + c] = (c <= r) ? G[r * PP + c] : 0.f;
@@ -349,13 +349,13 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
   }
 }
 
-// For every diagonal 128-block kb: the plain inverse block x in Gihi becomes
-// (Gihi, Gilo) = split(x) and (GiThi, GiTlo) = split(x^T).  One CTA per block,
-// the block read whole into shared memory before any write.
+// Diagonal 128-block kb: the plain inverse block x in Gihi becomes
+// (Gihi, Gilo) = split(x) and (GiThi, GiTlo) = split(x^T).  One CTA, the block
+// read whole into shared memory before any write.
 __global__ void __launch_bounds__(512) split_diag_kernel(float* Gihi, float* Gilo, float* GiThi,
-                                                         float* GiTlo, int64_t kp) {
+                                                         float* GiTlo, int64_t kp, int64_t kb) {
   extern __shared__ __align__(16) float xs[];   // [NB][PP]
-  const int64_t o = (int64_t)blockIdx.x * NB;
+  const int64_t o = kb * NB;
   for (int idx = threadIdx.x; idx < NB * NB; idx += blockDim.x) {
     const int r = idx / NB, c = idx - r * NB;
     xs[r * PP + c] = Gihi[(o + r) * kp + o + c];
@@ -407,12 +407,21 @@ namespace {
 // Work items of the tensor-core products of one factor of padded order kp:
 // for every Cholesky step kb the lower tiles of the trailing matrix, then for
 // every doubling level the T^T tiles and the X21 tiles.
+// Largest launch of the inverse's products while the chain runs.
+constexpr int kInvChunk = 1 << 20;
+
 struct PrepItems {
   std::vector<WorkItem> items;
   // per kb: the urgent tile (kb+1, kb+1) at syrk_off, then syrk_n1 tiles of
   // column kb+1 and tile (kb+2, kb+2), then syrk_n2 other tiles
   std::vector<int> syrk_off, syrk_n1, syrk_n2;
-  std::vector<int> t_off, t_n, x_off, x_n, t_maxk, x_maxk;  // per level
+  // recursive doubling of G^{-1}: per level (block size B = 2^level) and per
+  // pair of neighbouring blocks [p0, p0 + B), [p0 + B, e2) (p = p0 / 2B), the
+  // items of T = (G21 Ginv11)^T and of Ginv21 = -Ginv22 T^T
+  struct Pair {
+    int t_off, t_n, t_maxk, x_off, x_n, x_maxk;
+  };
+  std::vector<std::vector<Pair>> pairs;
 };
 
 const PrepItems& prep_items(int64_t kp) {
@@ -437,26 +446,22 @@ const PrepItems& prep_items(int64_t kp) {
     P.syrk_n2.push_back((int)(P.items.size() - s2));
   }
   for (int B = 1; B < nb; B *= 2) {
-    P.t_off.push_back((int)P.items.size());
-    int mk = 0;
-    for (int p0 = 0; p0 < nb; p0 += 2 * B) {
-      const int b1 = p0, e1 = p0 + B, b2 = p0 + B, e2 = std::min(p0 + 2 * B, nb);
-      if (b2 >= e2) continue;
+    P.pairs.emplace_back();
+    for (int p0 = 0; p0 + B < nb; p0 += 2 * B) {
+      const int b1 = p0, e1 = p0 + B, b2 = e1, e2 = std::min(p0 + 2 * B, nb);
+      PrepItems::Pair q{};
+      q.t_off = (int)P.items.size();
       for (int r = b1; r < e1; ++r)
-        for (int n = b2; n < e2; ++n) { P.items.push_back(WorkItem{r, n, r, e1}); mk = std::max(mk, e1 - r); }
+        for (int n = b2; n < e2; ++n) P.items.push_back(WorkItem{r, n, r, e1});
+      q.t_n = (int)P.items.size() - q.t_off;
+      q.t_maxk = B;
+      q.x_off = (int)P.items.size();
+      for (int r = e2 - 1; r >= b2; --r)   // longest first
+        for (int n = b1; n < e1; ++n) P.items.push_back(WorkItem{r, n, b2, r + 1});
+      q.x_n = (int)P.items.size() - q.x_off;
+      q.x_maxk = e2 - b2;
+      P.pairs.back().push_back(q);
     }
-    P.t_n.push_back((int)P.items.size() - P.t_off.back());
-    P.t_maxk.push_back(mk);
-    P.x_off.push_back((int)P.items.size());
-    mk = 0;
-    for (int p0 = 0; p0 < nb; p0 += 2 * B) {
-      const int b1 = p0, e1 = p0 + B, b2 = p0 + B, e2 = std::min(p0 + 2 * B, nb);
-      if (b2 >= e2) continue;
-      for (int r = b2; r < e2; ++r)
-        for (int n = b1; n < e1; ++n) { P.items.push_back(WorkItem{r, n, b2, r + 1}); mk = std::max(mk, r + 1 - b2); }
-    }
-    P.x_n.push_back((int)P.items.size() - P.x_off.back());
-    P.x_maxk.push_back(mk);
   }
   return cache.emplace(kp, std::move(P)).first->second;
 }
@@ -467,14 +472,9 @@ int64_t prepare_items_count(int64_t kp) { return kp > 0 ? (int64_t)prep_items(kp
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   const int64_t k = a.k, kp = a.kp;
   const int64_t nblk = kp / NB;
-  static bool attr_set = false;
-  if (!attr_set) {
-    BK_TRY(cudaFuncSetAttribute(potrf_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kPotrfSmem));
-    BK_TRY(cudaFuncSetAttribute(split_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(sizeof(float) * NB * PP)));
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> done[2];
+  BK_TRY(ensure_smem_limit((const void*)potrf_block_kernel, kPotrfSmem, done[0]));
+  BK_TRY(ensure_smem_limit((const void*)split_diag_kernel, sizeof(float) * NB * PP, done[1]));
   const PrepItems& P = prep_items(kp);
   if (!P.items.empty())
     BK_TRY(upload_items(P.items.data(), P.items.size(), a.items, s));
@@ -498,8 +498,80 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   // inverse of the diagonal block alternates between two scratch buffers,
   // because the lookahead stream may still read block kb's while block kb+1
   // is factored (potrf(kb+2) runs after S1(kb), which follows panel(kb)).
-  float* invbuf[2] = {a.Tlo, a.Tlo + NB * NB};
+  // The buffers sit in the last 128-row band of Tlo, which the inverse's
+  // products below never write (their T tiles lie above the diagonal).
+  float* const band = a.Tlo + (kp - NB) * kp;
+  float* invbuf[2] = {band, nblk > 1 ? band + NB * NB : band};
   const PrepItems& PI = P;
+  // G^{-1} by recursive doubling on the inverse stream, as the chain makes
+  // the inputs available.  For a pair of neighbouring diagonal ranges,
+  //   Ginv21 = -Ginv22 G21 Ginv11,
+  // formed as T = (G21 Ginv11)^T (tensor cores, stored in T's upper tiles),
+  // then Ginv21 = -Ginv22 T^T (written with its transpose into GiT).  T can
+  // run once the first range is inverted and the panels of its columns are
+  // final (events ev_urg, ev_pan of its last column); the second product
+  // once the second range is inverted, i.e. right after the chain reaches the
+  // pair's last block.  Only the second products of the pairs that end at the
+  // last block run after the chain.  Every tile of Ginv is written once, so
+  // the result does not depend on how the streams interleave.
+  auto pair_product = [&](int lvl, int p, bool tpart, cudaStream_t str) -> cudaError_t {
+    const PrepItems::Pair& pr = P.pairs[lvl][p];
+    PropArgs q{};
+    if (tpart) {
+      q.A_hi = a.GiThi; q.A_lo = a.GiTlo; q.lda = kp; q.a_rows = kp;
+      q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
+      q.out_hi = a.Thi; q.out_lo = a.Tlo; q.ldo = kp;
+      q.items = a.items + pr.t_off; q.n_items = pr.t_n; q.max_k = pr.t_maxk;
+      q.alpha = 1.f;
+    } else {
+      q.A_hi = a.Gihi; q.A_lo = a.Gilo; q.lda = kp; q.a_rows = kp;
+      q.B_hi = a.Thi; q.B_lo = a.Tlo; q.ldb = kp; q.b_rows = kp;
+      q.out_hi = a.Gihi; q.out_lo = a.Gilo; q.ldo = kp;
+      q.tr_hi = a.GiThi; q.tr_lo = a.GiTlo; q.ldt = kp;
+      q.items = a.items + pr.x_off; q.n_items = pr.x_n; q.max_k = pr.x_maxk;
+      q.alpha = -1.f;
+    }
+    q.stage = 1;
+    q.st = a.st;
+    // on the inverse stream, at most kInvChunk CTAs per launch, so the chain's
+    // kernels find free SMs between the chunks
+    const int cap = str == a.inv ? kInvChunk : q.n_items;
+    const WorkItem* items = q.items;
+    const int n = q.n_items;
+    for (int i0 = 0; i0 < n; i0 += cap) {
+      q.items = items + i0;
+      q.n_items = std::min(cap, n - i0);
+      BK_TRY(launch_prop_tc(q, str));
+    }
+    return cudaSuccess;
+  };
+  // second products of the pairs whose second range ends at block e
+  // (ascending levels: each needs the smaller pairs inside its range)
+  auto close_pairs = [&](int64_t e, cudaStream_t str) -> cudaError_t {
+    for (int lvl = 0; lvl < (int)P.pairs.size(); ++lvl) {
+      const int64_t B = (int64_t)1 << lvl;
+      const int64_t p0 = (e - 1) / (2 * B) * (2 * B);
+      if (p0 + B >= e) continue;                       // e is inside a first range
+      if (e != std::min(p0 + 2 * B, nblk)) continue;   // not this pair's end
+      BK_TRY(pair_product(lvl, (int)(p0 / (2 * B)), false, str));
+    }
+    return cudaSuccess;
+  };
+  // first products of the pairs whose first range ends at block e1
+  auto open_pairs = [&](int64_t e1, cudaStream_t str) -> cudaError_t {
+    for (int lvl = 0; lvl < (int)P.pairs.size(); ++lvl) {
+      const int64_t B = (int64_t)1 << lvl;
+      if (e1 % B != 0 || ((e1 / B) & 1) == 0 || e1 >= nblk) continue;
+      BK_TRY(pair_product(lvl, (int)((e1 - B) / (2 * B)), true, str));
+    }
+    return cudaSuccess;
+  };
+  auto split_diag = [&](int64_t i, cudaStream_t str) -> cudaError_t {
+    count_launch();
+    split_diag_kernel<<<1, 512, sizeof(float) * NB * PP, str>>>(a.Gihi, a.Gilo, a.GiThi, a.GiTlo, kp,
+                                                                i);
+    return cudaGetLastError();
+  };
   bool side_used = false;
   int64_t last = 0;
   for (int64_t kb = 0; kb < nblk; ++kb) {
@@ -553,37 +625,25 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     BK_TRY(cudaStreamWaitEvent(a.bulk, ev_pan, 0));
     BK_TRY(syrk(PI.syrk_off[kb] + 1 + PI.syrk_n1[kb], PI.syrk_n2[kb], a.bulk, false));
     BK_TRY(cudaEventRecord(ev_s2, a.bulk));
+    // inverse stream: block kb's inverse, the pairs it closes, then the
+    // pairs whose first range it ends (their panels are final at ev_pan)
+    BK_TRY(cudaStreamWaitEvent(a.inv, ev_pot, 0));
+    BK_TRY(split_diag(kb, a.inv));
+    BK_TRY(close_pairs(kb + 1, a.inv));
+    BK_TRY(cudaStreamWaitEvent(a.inv, ev_urg, 0));
+    BK_TRY(cudaStreamWaitEvent(a.inv, ev_pan, 0));
+    BK_TRY(open_pairs(kb + 1, a.inv));
   }
   if (side_used) {
-    // the last deferred updates join the factor's stream before the inverse
+    // the last deferred updates and the inverse rows join the factor's stream
     BK_TRY(cudaStreamWaitEvent(s, a.ev[5 * last + 3], 0));
     BK_TRY(cudaStreamWaitEvent(s, a.ev[5 * last + 4], 0));
+    BK_TRY(cudaEventRecord(a.ev[5 * nblk], a.inv));
+    BK_TRY(cudaStreamWaitEvent(s, a.ev[5 * nblk], 0));
   }
-  // split forms of the diagonal inverse blocks, then G^{-1} by recursive
-  // doubling (tensor cores)
-  count_launch();
-  split_diag_kernel<<<(unsigned)nblk, 512, sizeof(float) * NB * PP, s>>>(a.Gihi, a.Gilo, a.GiThi,
-                                                                        a.GiTlo, kp);
-  BK_TRY(cudaGetLastError());
-  for (size_t lvl = 0; lvl < P.t_off.size(); ++lvl) {
-    PropArgs t{};
-    t.A_hi = a.GiThi; t.A_lo = a.GiTlo; t.lda = kp; t.a_rows = kp;
-    t.B_hi = a.Chi; t.B_lo = a.Clo; t.ldb = kp; t.b_rows = kp;
-    t.out_hi = a.Thi; t.out_lo = a.Tlo; t.ldo = kp;
-    t.items = a.items + P.t_off[lvl]; t.n_items = P.t_n[lvl]; t.max_k = P.t_maxk[lvl];
-    t.stage = 1; t.alpha = 1.f;
-    t.st = a.st;
-    BK_TRY(launch_prop_tc(t, s));
-    PropArgs x{};
-    x.A_hi = a.Gihi; x.A_lo = a.Gilo; x.lda = kp; x.a_rows = kp;
-    x.B_hi = a.Thi; x.B_lo = a.Tlo; x.ldb = kp; x.b_rows = kp;
-    x.out_hi = a.Gihi; x.out_lo = a.Gilo; x.ldo = kp;
-    x.tr_hi = a.GiThi; x.tr_lo = a.GiTlo; x.ldt = kp;
-    x.items = a.items + P.x_off[lvl]; x.n_items = P.x_n[lvl]; x.max_k = P.x_maxk[lvl];
-    x.stage = 1; x.alpha = -1.f;
-    x.st = a.st;
-    BK_TRY(launch_prop_tc(x, s));
-  }
+  // the last block's inverse and the pairs that end there
+  BK_TRY(split_diag(nblk - 1, s));
+  BK_TRY(close_pairs(nblk, s));
   count_launch();
   finalize_kernel<<<grid_for(k * k), 256, 0, s>>>(a.C, a.Gihi, a.Gilo, kp, k, a.U, a.L);
   return cudaGetLastError();

@@ -414,27 +414,24 @@ bool make_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ld) {
 }  // namespace
 
 bool prop_tc_supported() {
-  static int cached = -1;
-  if (cached >= 0) return cached == 1;
+  static std::atomic<int> cached{-1};
+  const int c = cached.load(std::memory_order_acquire);
+  if (c >= 0) return c == 1;
   int dev = 0, major = 0, minor = 0;
   bool ok = cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
             major == 10 && minor == 3 && encode_fn() != nullptr;
   if (!ok) (void)cudaGetLastError();
-  cached = ok ? 1 : 0;
+  cached.store(ok ? 1 : 0, std::memory_order_release);
   return ok;
 }
 
 cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prop_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> done;
+  cudaError_t e = ensure_smem_limit((const void*)prop_tc_kernel, kSmem, done);
+  if (e != cudaSuccess) return e;
   CUtensorMap ahi, alo, bhi, blo;
   if (!make_map(&ahi, p.A_hi, p.a_rows, p.lda) || !make_map(&alo, p.A_lo, p.a_rows, p.lda) ||
       !make_map(&bhi, p.B_hi, p.b_rows, p.ldb) || !make_map(&blo, p.B_lo, p.b_rows, p.ldb))

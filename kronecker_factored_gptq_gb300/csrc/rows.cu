@@ -231,16 +231,10 @@ __global__ void __launch_bounds__(NTH, 1) rows_leaf_kernel(LeafArgs a) {
 }
 
 cudaError_t launch_rows_leaf(const LeafArgs& a, int n_row_tiles, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(rows_leaf_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRowsSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(rows_leaf_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kRowsSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> done[2];
+  cudaError_t e = ensure_smem_limit((const void*)rows_leaf_kernel<false>, kRowsSmem, done[0]);
+  if (e == cudaSuccess) e = ensure_smem_limit((const void*)rows_leaf_kernel<true>, kRowsSmem, done[1]);
+  if (e != cudaSuccess) return e;
   count_launch();
   if (a.preround)
     return launch_kernel(rows_leaf_kernel<true>, dim3(n_row_tiles), dim3(NTH), kRowsSmem, s,
