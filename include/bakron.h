@@ -11,11 +11,16 @@
  * ---------------------------------------
  * - Matrices are dense, row-major, contiguous, fp32 (codes: int8).
  * - Pointers named "host" are host memory; every other pointer is DEVICE
- *   memory on the current CUDA device, owned by the caller.  The library
- *   never allocates, frees or retains device memory: the caller passes a
- *   workspace of at least the size the matching *_workspace_size call
- *   reports.  Inputs are read-only; outputs must not alias inputs, each
- *   other or the workspace.
+ *   memory on the current CUDA device, owned by the caller.  The caller
+ *   passes a workspace of at least the size the matching *_workspace_size
+ *   call reports; the library allocates no other per-call memory.  The one
+ *   exception is its schedules: the first call for a problem shape on a
+ *   device builds the shape's work lists (16 bytes per 128-tile product,
+ *   e.g. 0.8 MB for an 8192 x 8192 factor) and keeps one copy of each in
+ *   mapped pinned host memory and one in device memory until the process
+ *   exits, so that later calls read them in place.  bakron_quantize_noalloc
+ *   allocates nothing.  Inputs are read-only; outputs must not alias inputs,
+ *   each other or the workspace.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *   enqueued on it; every compute call then synchronises the stream and reads
  *   back a device status word, so the returned status is final.  Outputs are

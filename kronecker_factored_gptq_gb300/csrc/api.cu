@@ -523,7 +523,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   auto next_event = [&](cudaEvent_t* ev) { return pool_event(ss, nev++, ev); };
   char* base = (char*)ws;
   DevStatus* st = (DevStatus*)(base + L.status);
-  WorkItem* items = (WorkItem*)(base + L.sched);
+  const WorkItem* items = (const WorkItem*)(base + L.sched);
   float* sp = (float*)(base + L.scale);
   float* zp = (float*)(base + L.zero);
   float* wt = (float*)(base + L.wt);
@@ -540,8 +540,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
   }
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
-  if (!sch.items.empty())
-    TRY_CUDA(upload_items(sch.items.data(), sch.items.size(), items, cs));
+  TRY_CUDA(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
@@ -813,7 +812,7 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   auto next_event = [&](cudaEvent_t* ev) { return pool_event(ss, nev++, ev); };
   char* base = (char*)ws;
   DevStatus* st = (DevStatus*)(base + L.status);
-  WorkItem* items = (WorkItem*)(base + L.sched);
+  const WorkItem* items = (const WorkItem*)(base + L.sched);
   float* sp = (float*)(base + L.scale);
   float* zp = (float*)(base + L.zero);
   float* wt = (float*)(base + L.wt);
@@ -834,8 +833,7 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
     TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
   }
   TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
-  if (!sch.items.empty())
-    TRY_CUDA(upload_items(sch.items.data(), sch.items.size(), items, cs));
+  TRY_CUDA(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();

@@ -111,7 +111,12 @@ cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Copy a cached host work list into the workspace (see misc.cu); the
 // no-allocation entry point sets the thread flag for the length of its call.
-cudaError_t upload_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s);
+// Device address of a host-built work list for kernels on stream s: its
+// device-resident copy (made by the first call, later calls wait for it), or
+// ws_dst after copying the list there (calls that must not allocate, and
+// calls during stream capture before the resident copy exists).
+cudaError_t stage_items(const WorkItem* src, size_t count, WorkItem* ws_dst, cudaStream_t s,
+                        const WorkItem** out);
 void set_no_host_alloc(bool on);
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current

@@ -233,13 +233,17 @@ cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cu
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------ work-item upload
-// The host-built work lists of a cached schedule are staged once in mapped
-// pinned host memory and copied into the workspace by a kernel that reads
-// them over the host link.  A DMA copy would queue on the host-to-device
-// copy engine behind any large transfer the caller has in flight (such as
-// the next problem's inputs) and stall the solve.  Calls that must not
-// allocate (thread flag) use a plain asynchronous copy instead.
+// ------------------------------------------------------ work-item staging
+// The host-built work lists of a cached schedule never change, so each list
+// gets one device-resident copy per device, made by the first call that needs
+// it and read in place by every later call.  The first call stages the list in
+// mapped pinned host memory and copies it with a kernel that reads it over the
+// host link (a DMA copy would queue on the host-to-device copy engine behind
+// any large transfer the caller has in flight, such as the next problem's
+// inputs), then records an event that later calls on other streams wait for.
+// Calls that must not allocate (thread flag) copy into the caller's
+// workspace with a plain asynchronous copy; calls made while their stream is
+// being captured into a graph copy into the workspace with the kernel.
 __global__ void copy_items_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -249,8 +253,10 @@ __global__ void copy_items_kernel(const uint4* __restrict__ src, uint4* __restri
 namespace {
 thread_local bool t_no_host_alloc = false;
 struct Staged {
-  void* host = nullptr;
-  const void* dev = nullptr;
+  void* host = nullptr;         // mapped pinned copy of the list
+  const void* mapped = nullptr; // its device address
+  void* resident = nullptr;     // device-resident copy (null while capturing)
+  cudaEvent_t ready = nullptr;  // recorded after the resident copy was made
   size_t bytes = 0;
 };
 }  // namespace
@@ -269,44 +275,79 @@ cudaError_t ensure_smem_limit(const void* kernel, size_t bytes,
   return e;
 }
 
-cudaError_t upload_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s) {
+cudaError_t stage_items(const WorkItem* src, size_t count, WorkItem* ws_dst, cudaStream_t s,
+                        const WorkItem** out) {
+  *out = ws_dst;
   if (count == 0) return cudaSuccess;
   const size_t bytes = sizeof(WorkItem) * count;
-  if (t_no_host_alloc)
-    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s);
+  if (t_no_host_alloc) return cudaMemcpyAsync(ws_dst, src, bytes, cudaMemcpyHostToDevice, s);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return e;
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, Staged> cache;   // (list, device)
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const void* dptr = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    Staged& st = cache[std::make_pair((const void*)src, dev)];
-    if (st.bytes != bytes) {
-      // the cached lists never change or move; a list seen with another
-      // size is a new list at a reused address
-      if (st.host) cudaFreeHost(st.host);
-      st = Staged{};
-      void* h = nullptr;
-      if ((e = cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess)
-        return e;
-      std::memcpy(h, src, bytes);
-      void* d = nullptr;
-      if ((e = cudaHostGetDevicePointer(&d, h, 0)) != cudaSuccess) {
-        cudaFreeHost(h);
-        return e;
-      }
-      st.host = h;
-      st.dev = d;
-      st.bytes = bytes;
-    }
-    dptr = st.dev;
-  }
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   const int64_t n16 = (int64_t)(bytes / 16);
+  std::lock_guard<std::mutex> lk(mu);
+  Staged& st = cache[std::make_pair((const void*)src, dev)];
+  if (st.bytes != bytes) {
+    // the cached lists never change or move; a list seen with another size
+    // is a new list at a reused address (the old copies are released once
+    // the device is idle)
+    if (st.host || st.resident) {
+      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return e;
+      if (st.host) cudaFreeHost(st.host);
+      if (st.resident) cudaFree(st.resident);
+      if (st.ready) cudaEventDestroy(st.ready);
+    }
+    st = Staged{};
+    void* h = nullptr;
+    if ((e = cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess)
+      return e;
+    std::memcpy(h, src, bytes);
+    void* d = nullptr;
+    if ((e = cudaHostGetDevicePointer(&d, h, 0)) != cudaSuccess) {
+      cudaFreeHost(h);
+      return e;
+    }
+    st.host = h;
+    st.mapped = d;
+    st.bytes = bytes;
+  }
+  if (!st.resident && !capturing) {
+    void* r = nullptr;
+    if ((e = cudaMalloc(&r, bytes)) != cudaSuccess) return e;
+    cudaEvent_t ev = nullptr;
+    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
+      cudaFree(r);
+      return e;
+    }
+    count_launch();
+    copy_items_kernel<<<grid_for(n16, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(st.mapped),
+                                                          reinterpret_cast<uint4*>(r), n16);
+    if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev, s)) != cudaSuccess) {
+      // nothing was queued that reads r, or the copy is queued but unusable:
+      // release after the stream is done with it
+      cudaStreamSynchronize(s);
+      cudaFree(r);
+      cudaEventDestroy(ev);
+      return e;
+    }
+    st.resident = r;
+    st.ready = ev;
+    *out = reinterpret_cast<const WorkItem*>(r);
+    return cudaSuccess;
+  }
+  if (st.resident) {
+    *out = reinterpret_cast<const WorkItem*>(st.resident);
+    return cudaStreamWaitEvent(s, st.ready, 0);
+  }
+  // capturing before any resident copy exists: copy into the workspace
   count_launch();
-  copy_items_kernel<<<grid_for(n16, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(dptr),
-                                                        reinterpret_cast<uint4*>(dst), n16);
+  copy_items_kernel<<<grid_for(n16, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(st.mapped),
+                                                        reinterpret_cast<uint4*>(ws_dst), n16);
   return cudaGetLastError();
 }
 

@@ -476,8 +476,8 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   BK_TRY(ensure_smem_limit((const void*)potrf_block_kernel, kPotrfSmem, done[0]));
   BK_TRY(ensure_smem_limit((const void*)split_diag_kernel, sizeof(float) * NB * PP, done[1]));
   const PrepItems& P = prep_items(kp);
-  if (!P.items.empty())
-    BK_TRY(upload_items(P.items.data(), P.items.size(), a.items, s));
+  const WorkItem* items = a.items;
+  BK_TRY(stage_items(P.items.data(), P.items.size(), a.items, s, &items));
   count_launch();
   diag_mean_kernel<<<1, 256, 0, s>>>(a.X, k, a.damp, a.scal);
   BK_TRY(cudaGetLastError());
@@ -521,14 +521,14 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
       q.A_hi = a.GiThi; q.A_lo = a.GiTlo; q.lda = kp; q.a_rows = kp;
       q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
       q.out_hi = a.Thi; q.out_lo = a.Tlo; q.ldo = kp;
-      q.items = a.items + pr.t_off; q.n_items = pr.t_n; q.max_k = pr.t_maxk;
+      q.items = items + pr.t_off; q.n_items = pr.t_n; q.max_k = pr.t_maxk;
       q.alpha = 1.f;
     } else {
       q.A_hi = a.Gihi; q.A_lo = a.Gilo; q.lda = kp; q.a_rows = kp;
       q.B_hi = a.Thi; q.B_lo = a.Tlo; q.ldb = kp; q.b_rows = kp;
       q.out_hi = a.Gihi; q.out_lo = a.Gilo; q.ldo = kp;
       q.tr_hi = a.GiThi; q.tr_lo = a.GiTlo; q.ldt = kp;
-      q.items = a.items + pr.x_off; q.n_items = pr.x_n; q.max_k = pr.x_maxk;
+      q.items = items + pr.x_off; q.n_items = pr.x_n; q.max_k = pr.x_maxk;
       q.alpha = -1.f;
     }
     q.stage = 1;
@@ -536,10 +536,10 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     // on the inverse stream, at most kInvChunk CTAs per launch, so the chain's
     // kernels find free SMs between the chunks
     const int cap = str == a.inv ? kInvChunk : q.n_items;
-    const WorkItem* items = q.items;
+    const WorkItem* first = q.items;
     const int n = q.n_items;
     for (int i0 = 0; i0 < n; i0 += cap) {
-      q.items = items + i0;
+      q.items = first + i0;
       q.n_items = std::min(cap, n - i0);
       BK_TRY(launch_prop_tc(q, str));
     }
@@ -602,7 +602,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
       q.A_hi = a.Chi; q.A_lo = a.Clo; q.lda = kp; q.a_rows = kp;
       q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
       q.wt = a.C; q.ldw = kp;
-      q.items = a.items + i0; q.n_items = n; q.max_k = 1;
+      q.items = items + i0; q.n_items = n; q.max_k = 1;
       q.stage = 2;
       q.st = a.st;
       return launch_prop_tc(q, str);

@@ -43,7 +43,7 @@ def test_rowscale_bit_exact(kb):
         np.testing.assert_array_equal(s, O.row_scale(W, qmax))
 
 
-@pytest.mark.parametrize("n", [64, 200, 384])
+@pytest.mark.parametrize("n", [64, 200, 384, 677, 1300])
 def test_prepare_matches_oracle(kb, n):
     w = WL.random_problem(n, n, seed=n, oversample=3)
     dA, dB = to_dev(w.A, w.B)
