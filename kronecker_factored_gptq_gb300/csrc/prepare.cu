@@ -138,7 +138,7 @@ __global__ void flip_damp_kernel(const float* __restrict__ X, int64_t k, const f
 // tiles over both triangular operands.
 constexpr int PB = 16;                 // panel width
 constexpr int PP = NB + 1;             // shared pitch (odd: row and column walks are conflict-free)
-constexpr size_t kPotrfSmem = sizeof(float) * (3 * NB * PP + NB);
+constexpr size_t kPotrfSmem = sizeof(float) * (3 * NB * PP + NB + 2 * PB);
 
 // One 4 x 2 tile (rows m0.., columns n0..) of C = alpha * A * B, all in
 // shared memory with pitch PP, K range [k0, k1).
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
   float* X = G + NB * PP;          // [NB][PP] the inverse
   float* S = X + NB * PP;          // [NB][PP] scratch
   float* dinv = S + NB * PP;       // [NB] 1 / G[j][j]
-  const unsigned FULLM = 0xffffffffu;
+  float* colv = dinv + NB;         // [2][PB] column exchange of the 16 x 16 factorisation
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NT = 512;
   const int64_t o = kb * NB;
@@ -188,29 +188,36 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
   }
   __syncthreads();
   // (1) the diagonal 16 x 16 block of panel q / PB: warp 0, lanes r and
-  // r + 16 hold row r; pivots through rsqrt, 1 / pivot kept in dinv
+  // r + 16 hold row r; pivots through rsqrt, 1 / pivot kept in dinv.  Each
+  // column step publishes the rows' current column-j entries through shared
+  // memory (double-buffered, one warp barrier per step) instead of 15 warp
+  // shuffles: measured, the shuffles ran ~10x slower whenever warp 0 worked
+  // alone while the other warps waited at the block barrier.
   auto factor_diag = [&](int q) {
     const int r = lane & (PB - 1);
     float a[PB];
+    float myinv = 0.f;   // 1 / pivot of this lane's row
 #pragma unroll
     for (int c = 0; c < PB; ++c) a[c] = (c <= r) ? G[(q + r) * PP + q + c] : 0.f;
-    int badj = -1;   // first non-positive or non-finite pivot (replaced by 1)
+    int badj = PB;   // first non-positive or non-finite pivot (replaced by 1)
 #pragma unroll
     for (int j = 0; j < PB; ++j) {
-      float d = __shfl_sync(FULLM, a[j], j);
+      float* cv = colv + (j & 1) * PB;
+      cv[r] = a[j];   // lanes r and r + 16 store the same value
+      __syncwarp();
+      float d = cv[j];
       const bool bad = !(d > 0.f) || !isfinite(d);
-      if (bad && badj < 0) badj = j;
+      badj = (bad && badj == PB) ? j : badj;
       d = bad ? 1.f : d;
       const float inv = rsqrtf(d);
+      myinv = (r == j) ? inv : myinv;
       const float l = a[j] * inv;
-      if (r == j) a[j] = d * inv;
-      else if (r > j) a[j] = l;
-      if (lane == 0) dinv[q + j] = inv;
+      a[j] = (r == j) ? d * inv : ((r > j) ? l : a[j]);
 #pragma unroll
       for (int k = 0; k < PB; ++k) {
         if (k > j) {
-          const float lk = __shfl_sync(FULLM, l, k);
-          if (r >= k) a[k] = fmaf(-l, lk, a[k]);
+          const float lk = cv[k] * inv;   // row k's entry of column j of the factor
+          a[k] = (r >= k) ? fmaf(-l, lk, a[k]) : a[k];
         }
       }
     }
@@ -218,10 +225,13 @@ __global__ void __launch_bounds__(512) potrf_block_kernel(float* C, float* Gihi,
 #pragma unroll
       for (int c = 0; c < PB; ++c)
         if (c <= r) G[(q + r) * PP + q + c] = a[c];
+      dinv[q + r] = myinv;
     }
-    if (lane == 0 && badj >= 0 && o + q + badj < k_real) {
-      atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + badj));
-      set_status(st, BAKRON_ERR_NOT_PD);
+    if (lane == 0) {
+      if (badj < PB && o + q + badj < k_real) {
+        atomicMin(reinterpret_cast<long long*>(&st->info[which]), (long long)(o + q + badj));
+        set_status(st, BAKRON_ERR_NOT_PD);
+      }
     }
   };
   // (3) one 4 x 4 tile (ti, tj), tj <= ti, of the trailing lower triangle
