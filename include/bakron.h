@@ -93,6 +93,31 @@ int bakron_version(void);
  * across a region counts the library's kernels in it. */
 int64_t bakron_kernel_launches(void);
 
+/* The work lists the library schedules for a problem shape, for inspection
+ * and host-side tests.  Pure host code (no CUDA call; works without a GPU).
+ * Shapes are in 128-tiles: M row tiles and N column tiles of W.
+ *   BAKRON_SCHEDULE_SOLVE    the two-sided divide and conquer over the tile
+ *                            anti-diagonals 0 .. M+N-2 (bakron_quantize)
+ *   BAKRON_SCHEDULE_ROWS     the one-sided solve over column tiles (UB NULL)
+ *   BAKRON_SCHEDULE_PREPARE  the preparation of a factor of M 128-blocks
+ *                            (N is ignored)
+ * out receives int32 values, host memory; *len (host) the count the
+ * schedule needs.  Nothing is written to out when cap < *len (pass cap = 0
+ * to size it).  M, N in [1, 8192]; anything else is BAKRON_ERR_INVALID_ARG.
+ * Layout (every offset counts work items, each item 4 values r, c, k0, k1):
+ *   SOLVE / ROWS: n_ops, n_chunks, n_items; n_ops records of 7 values
+ *     kind (0 leaf, 1 propagation), D (leaf diagonal or column tile), I0,
+ *     ntiles, depth, chunk0, nchunks; n_chunks records of 6 values
+ *     dlo, dhi (target range), off1, n1 (stage-1 items), off, n (stage-2
+ *     items; ROWS has no stage-1 items); the items.
+ *   PREPARE: nb, n_items, n_levels; nb records syrk_off, n1, n2 (the
+ *     trailing updates of step kb: the urgent tile, n1 lookahead tiles, n2
+ *     bulk tiles); per doubling level n_pairs then n_pairs records t_off,
+ *     t_n, x_off, x_n; the items. */
+enum { BAKRON_SCHEDULE_SOLVE = 0, BAKRON_SCHEDULE_ROWS = 1, BAKRON_SCHEDULE_PREPARE = 2 };
+bakron_status bakron_schedule_export(int kind, int64_t M, int64_t N, int32_t* out, int64_t cap,
+                                     int64_t* len);
+
 /* Workspace bytes bakron_quantize / bakron_quantize_antidiag need for an
  * m x n problem (written to *bytes, host).  Pure host arithmetic. */
 bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts,

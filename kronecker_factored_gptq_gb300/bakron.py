@@ -26,7 +26,7 @@ EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bak
            "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
            "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
            "bakron_grid_params", "bakron_quantize_grid", "bakron_batch_workspace_size",
-           "bakron_quantize_batch"]
+           "bakron_quantize_batch", "bakron_schedule_export"]
 FACTORS_KFAC = 0
 FACTORS_SHAMPOO = 1
 
@@ -99,7 +99,8 @@ def lib():
                                         vp, sz, vp]
     L.bakron_factors_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
     L.bakron_factors.argtypes = [vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, sz, vp]
-    for f in ("bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
+    L.bakron_schedule_export.argtypes = [ctypes.c_int, i64, i64, vp, i64, ctypes.POINTER(i64)]
+    for f in ("bakron_schedule_export", "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
               "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
               "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
               "bakron_grid_params", "bakron_quantize_grid", "bakron_batch_workspace_size",
@@ -112,6 +113,27 @@ def lib():
 def kernel_launches():
     """Kernels the library has launched in this process so far."""
     return int(lib().bakron_kernel_launches())
+
+
+SCHEDULE_SOLVE = 0
+SCHEDULE_ROWS = 1
+SCHEDULE_PREPARE = 2
+
+
+def schedule_export(kind, M, N=1):
+    """The library's work lists for a shape in 128-tiles (host only, no GPU):
+    an int32 numpy array in the layout bakron_schedule_export documents."""
+    import numpy as np
+    n = ctypes.c_int64(0)
+    st = lib().bakron_schedule_export(int(kind), int(M), int(N), None, 0, ctypes.byref(n))
+    if st != OK:
+        raise BakronError(st, "bakron_schedule_export")
+    out = np.zeros(max(1, n.value), dtype=np.int32)
+    st = lib().bakron_schedule_export(int(kind), int(M), int(N), ctypes.c_void_p(out.ctypes.data),
+                                      n.value, ctypes.byref(n))
+    if st != OK:
+        raise BakronError(st, "bakron_schedule_export")
+    return out[:n.value]
 
 
 def default_opts(**kw):

@@ -154,6 +154,38 @@ void build_rec(Schedule& s, int D0, int D1, int depth) {
   build_rec(s, Dm, D1, depth + 1);
 }
 
+// Deferred propagation chunks that the critical stream has not yet waited
+// for, each with the target range [dlo, dhi) it updates (tile anti-diagonals,
+// or column tiles on the one-sided path).  A leaf waits for those covering
+// its diagonal; a propagation waits, before its first chunk, for those
+// covering any of its targets.  Both add into the same W~ tiles from
+// different streams (atomic adds, so overlapping was correct), and waiting
+// fixes the order of the adds, so the fp32 result is the same on every run.
+// (The propagation's own deferred chunks follow its first chunk through an
+// event, so they are ordered after the wait too.)  Each event is waited for
+// once; mostly it has completed long before.
+struct PendingChunks {
+  struct Item {
+    cudaEvent_t ev;
+    int dlo, dhi;
+  };
+  std::vector<Item> v;
+  void add(cudaEvent_t ev, int dlo, int dhi) { v.push_back(Item{ev, dlo, dhi}); }
+  cudaError_t order_before(cudaStream_t cs, int lo, int hi) {
+    size_t w = 0;
+    for (size_t i = 0; i < v.size(); ++i) {
+      if (v[i].dlo < hi && v[i].dhi > lo) {
+        const cudaError_t e = cudaStreamWaitEvent(cs, v[i].ev, 0);
+        if (e != cudaSuccess) return e;
+      } else {
+        v[w++] = v[i];
+      }
+    }
+    v.resize(w);
+    return cudaSuccess;
+  }
+};
+
 const Schedule& get_schedule(int M, int N) {
   static std::mutex mu;
   static std::map<std::pair<int, int>, Schedule> cache;
@@ -563,10 +595,10 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   la.V = V; la.codes = codes; la.preround = preround;
   la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
   la.st = st;
-  std::vector<std::vector<cudaEvent_t>> waits((size_t)L.N + 1);
+  PendingChunks pending;
   for (const RowsOp& op : sch.ops) {
     if (op.kind == 0) {
-      for (cudaEvent_t ev : waits[op.J]) TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+      TRY_CUDA(pending.order_before(cs, op.J, op.J + 1));
       la.D = op.J;
       la.I0 = 0;
       la.pdl = op.J > 0;   // the first leaf reads the factor the kernel before it wrote
@@ -581,6 +613,9 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     p2.wt = wt; p2.ldw = L.Np;
     p2.stage = 2;
     p2.st = st;
+    if (op.nchunks > 0)
+      TRY_CUDA(pending.order_before(cs, sch.chunks[op.chunk0].dlo,
+                                    sch.chunks[op.chunk0 + op.nchunks - 1].dhi));
     for (int c = 0; c < op.nchunks; ++c) {
       const Chunk& ch = sch.chunks[op.chunk0 + c];
       if (o.times) o.times->prop_flops += ch.flops;
@@ -605,7 +640,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
         cudaEvent_t done;
         TRY_CUDA(next_event(&done));
         TRY_CUDA(cudaEventRecord(done, cstr));
-        for (int d = ch.dlo; d < ch.dhi; ++d) waits[d].push_back(done);
+        pending.add(done, ch.dlo, ch.dhi);
       }
     }
   }
@@ -661,6 +696,65 @@ const char* bakron_status_string(int st) {
 int bakron_version(void) { return 10000; }
 
 int64_t bakron_kernel_launches(void) { return (int64_t)bakron::launches_so_far(); }
+
+bakron_status bakron_schedule_export(int kind, int64_t M, int64_t N, int32_t* out, int64_t cap,
+                                     int64_t* len) {
+  if (!len || cap < 0 || (cap > 0 && !out)) return BAKRON_ERR_INVALID_ARG;
+  if (M < 1 || M > 8192 || (kind != BAKRON_SCHEDULE_PREPARE && (N < 1 || N > 8192)))
+    return BAKRON_ERR_INVALID_ARG;
+  std::vector<int32_t> v;
+  auto items = [&](const std::vector<WorkItem>& it) {
+    for (const WorkItem& w : it) {
+      v.push_back(w.r);
+      v.push_back(w.c);
+      v.push_back(w.k0);
+      v.push_back(w.k1);
+    }
+  };
+  auto chunks = [&](const std::vector<Chunk>& ch) {
+    for (const Chunk& c : ch) {
+      v.push_back(c.dlo);
+      v.push_back(c.dhi);
+      v.push_back(c.off1);
+      v.push_back(c.n1);
+      v.push_back(c.off);
+      v.push_back(c.n);
+    }
+  };
+  if (kind == BAKRON_SCHEDULE_SOLVE) {
+    const Schedule& s = get_schedule((int)M, (int)N);
+    v.push_back((int32_t)s.ops.size());
+    v.push_back((int32_t)s.chunks.size());
+    v.push_back((int32_t)s.items.size());
+    for (const Op& op : s.ops) {
+      const int32_t rec[7] = {op.kind, op.kind == 0 ? op.D : 0, op.kind == 0 ? op.I0 : 0,
+                              op.kind == 0 ? op.ntiles : 0, op.kind == 1 ? op.depth : 0,
+                              op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
+      v.insert(v.end(), rec, rec + 7);
+    }
+    chunks(s.chunks);
+    items(s.items);
+  } else if (kind == BAKRON_SCHEDULE_ROWS) {
+    const RowsSchedule& s = get_rows_schedule((int)M, (int)N);
+    v.push_back((int32_t)s.ops.size());
+    v.push_back((int32_t)s.chunks.size());
+    v.push_back((int32_t)s.items.size());
+    for (const RowsOp& op : s.ops) {
+      const int32_t rec[7] = {op.kind, op.kind == 0 ? op.J : 0, 0, op.kind == 0 ? (int32_t)M : 0,
+                              op.depth, op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
+      v.insert(v.end(), rec, rec + 7);
+    }
+    chunks(s.chunks);
+    items(s.items);
+  } else if (kind == BAKRON_SCHEDULE_PREPARE) {
+    prepare_schedule_export(M, v);
+  } else {
+    return BAKRON_ERR_INVALID_ARG;
+  }
+  *len = (int64_t)v.size();
+  if (cap >= *len && *len > 0) std::memcpy(out, v.data(), sizeof(int32_t) * v.size());
+  return BAKRON_OK;
+}
 
 bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts, size_t* bytes) {
   if (!bytes || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
@@ -858,11 +952,10 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   la.V = V; la.codes = codes; la.preround = preround;
   la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
   la.st = st;
-  // events each leaf must wait for (deferred chunks covering its diagonal)
-  std::vector<std::vector<cudaEvent_t>> waits((size_t)(L.M + L.N));
+  PendingChunks pending;
   for (const Op& op : sch.ops) {
     if (op.kind == 0) {
-      for (cudaEvent_t ev : waits[op.D]) TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+      TRY_CUDA(pending.order_before(cs, op.D, op.D + 1));
       la.D = op.D;
       la.I0 = op.I0;
       // the first leaf reads the factors the kernel directly before it wrote;
@@ -893,6 +986,9 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
       pa.pdl = str == cs;
       return o.use_3xtf32 ? launch_prop_tc(pa, str) : launch_prop_simt(pa, str);
     };
+    if (op.nchunks > 0)
+      TRY_CUDA(pending.order_before(cs, sch.chunks[op.chunk0].dlo,
+                                    sch.chunks[op.chunk0 + op.nchunks - 1].dhi));
     cudaEvent_t ev_s1 = nullptr;
     for (int c = 0; c < op.nchunks; ++c) {
       const Chunk& ch = sch.chunks[op.chunk0 + c];
@@ -922,7 +1018,7 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
         cudaEvent_t done;
         TRY_CUDA(next_event(&done));
         TRY_CUDA(cudaEventRecord(done, cstr));
-        for (int d = ch.dlo; d < ch.dhi; ++d) waits[d].push_back(done);
+        pending.add(done, ch.dlo, ch.dhi);
       }
     }
   }

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <vector>
 #include <stdint.h>
 
 #include "bakron.h"
@@ -186,5 +187,8 @@ struct PrepareFactorArgs {
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s);
 int64_t prepare_pad(int64_t k);
 int64_t prepare_items_count(int64_t kp);
+// The preparation schedule of a factor of nb 128-blocks, in the layout of
+// bakron_schedule_export.
+void prepare_schedule_export(int64_t nb, std::vector<int32_t>& out);
 
 }  // namespace bakron

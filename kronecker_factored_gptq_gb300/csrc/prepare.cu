@@ -479,6 +479,34 @@ const PrepItems& prep_items(int64_t kp) {
 
 int64_t prepare_items_count(int64_t kp) { return kp > 0 ? (int64_t)prep_items(kp).items.size() : 0; }
 
+void prepare_schedule_export(int64_t nb, std::vector<int32_t>& out) {
+  const PrepItems& P = prep_items(nb * NB);
+  out.clear();
+  out.push_back((int32_t)nb);
+  out.push_back((int32_t)P.items.size());
+  out.push_back((int32_t)P.pairs.size());
+  for (int64_t kb = 0; kb < nb; ++kb) {
+    out.push_back(P.syrk_off[kb]);
+    out.push_back(P.syrk_n1[kb]);
+    out.push_back(P.syrk_n2[kb]);
+  }
+  for (const auto& level : P.pairs) {
+    out.push_back((int32_t)level.size());
+    for (const PrepItems::Pair& q : level) {
+      out.push_back(q.t_off);
+      out.push_back(q.t_n);
+      out.push_back(q.x_off);
+      out.push_back(q.x_n);
+    }
+  }
+  for (const WorkItem& w : P.items) {
+    out.push_back(w.r);
+    out.push_back(w.c);
+    out.push_back(w.k0);
+    out.push_back(w.k1);
+  }
+}
+
 cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   const int64_t k = a.k, kp = a.kp;
   const int64_t nblk = kp / NB;

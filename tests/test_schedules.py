@@ -1,0 +1,351 @@
+"""Host-side checks of the library's schedules (no GPU): the work lists come
+from the C ABI (bakron_schedule_export), the checks from the method.
+
+Two-sided solve ("BaKron" page, Algorithm 1 and the divide-and-conquer
+discussion of the propagation): the error of tile (I, J) reaches every tile
+(I', J') with I' >= I, J' >= J, through Y[I][J'] = sum_J E[I][J] U_A[J][J']
+(stage 1) and W~[I'][J'] -= sum_I U_B[I][I']^T Y[I][J'] (stage 2).  The
+schedule must apply each (source, target) contribution exactly once, from a
+source whose leaf has run, before the leaf of the target.  One-sided solve
+(B = I): the same over column tiles.  Preparation: the blocked Cholesky's
+trailing updates and the recursive-doubling inverse.
+
+The stream model mirrors the executor's rules in csrc/api.cu: leaves, the
+first chunk of each propagation and its waits on the critical stream, the
+other chunks on one side stream per recursion depth after the first chunk's
+stage 1, and a list of deferred chunks each waited for once, by the first
+leaf or propagation that touches its targets.  The checks then require every
+update of a W~ tile (so their fp32 order is fixed), every Y tile's writer
+and readers, and every E tile's producer and readers to be ordered by stream
+order and events.
+"""
+
+import numpy as np
+import pytest
+
+from kronecker_factored_gptq_gb300 import bakron as kb
+
+
+def parse_solve(a):
+    n_ops, n_chunks, n_items = (int(x) for x in a[:3])
+    p = 3
+    ops = a[p:p + 7 * n_ops].reshape(n_ops, 7); p += 7 * n_ops
+    chunks = a[p:p + 6 * n_chunks].reshape(n_chunks, 6); p += 6 * n_chunks
+    items = a[p:p + 4 * n_items].reshape(n_items, 4); p += 4 * n_items
+    assert p == len(a)
+    return ops, chunks, items
+
+
+def parse_prepare(a):
+    nb, n_items, n_levels = (int(x) for x in a[:3])
+    p = 3
+    syrk = a[p:p + 3 * nb].reshape(nb, 3); p += 3 * nb
+    levels = []
+    for _ in range(n_levels):
+        n = int(a[p]); p += 1
+        levels.append(a[p:p + 4 * n].reshape(n, 4)); p += 4 * n
+    items = a[p:p + 4 * n_items].reshape(n_items, 4); p += 4 * n_items
+    assert p == len(a)
+    return syrk, levels, items
+
+
+class Streams:
+    """Happens-before over nodes enqueued on streams with events."""
+
+    def __init__(self):
+        self.anc = []          # ancestor bitmask per node
+        self.last = {}         # stream -> last node
+        self.pending_waits = {}
+
+    def node(self, stream):
+        m = 0
+        if stream in self.last:
+            p = self.last[stream]
+            m |= self.anc[p] | (1 << p)
+        for p in self.pending_waits.pop(stream, []):
+            m |= self.anc[p] | (1 << p)
+        self.anc.append(m)
+        i = len(self.anc) - 1
+        self.last[stream] = i
+        return i
+
+    def record(self, stream):
+        """An event recorded now on `stream`: the node it completes after
+        (a marker node when waits were enqueued after the last node)."""
+        if self.pending_waits.get(stream):
+            self.node(stream)
+        return self.last.get(stream)
+
+    def wait(self, stream, ev):
+        if ev is not None:
+            self.pending_waits.setdefault(stream, []).append(ev)
+
+    def before(self, a, b):
+        return bool((self.anc[b] >> a) & 1)
+
+
+def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
+    """Builds the stream model and returns (S, accesses) where accesses maps
+    ('W', tile) / ('Y', depth, tile) / ('E', tile) to [(node, 'r'|'w')]."""
+    S = Streams()
+    acc = {}
+
+    def touch(key, node, mode):
+        acc.setdefault(key, []).append((node, mode))
+
+    pending = []   # (event node, dlo, dhi)
+
+    def order_before(lo, hi):
+        keep = []
+        for ev, dlo, dhi in pending:
+            if dlo < hi and dhi > lo:
+                S.wait("cs", ev)
+            else:
+                keep.append((ev, dlo, dhi))
+        pending[:] = keep
+
+    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops:
+        if kind == 0:
+            order_before(D, D + 1)
+            n = S.node("cs")
+            if one_sided:
+                tiles = [(I, D) for I in range(ntiles)]
+            else:
+                tiles = [(I0 + t, D - I0 - t) for t in range(ntiles)]
+            for t in tiles:
+                touch(("W", t), n, "w")   # reads W~, the last of its updates
+                touch(("E", t), n, "w")
+            continue
+        if wait_at_propagation and nchunks > 0:
+            order_before(chunks[chunk0][0], chunks[chunk0 + nchunks - 1][1])
+        ev_s1 = None
+        for c in range(nchunks):
+            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c]
+            stream = "cs" if c == 0 else "side%d" % depth
+            if c == 1:
+                S.wait(stream, ev_s1)
+            if n1 > 0:
+                s1 = S.node(stream)
+                for Jp, I, k0, k1 in items[off1:off1 + n1]:
+                    touch(("Y", depth, (I, Jp)), s1, "w")
+                    for J in range(k0, k1):
+                        touch(("E", (I, J)), s1, "r")
+            if c == 0:
+                ev_s1 = S.record("cs")
+            if nn > 0:
+                s2 = S.node(stream)
+                for Ip, Jp, k0, k1 in items[off:off + nn]:
+                    touch(("W", (Ip, Jp)), s2, "w")
+                    for I in range(k0, k1):
+                        if one_sided:
+                            touch(("E", (Ip, I)), s2, "r")
+                        else:
+                            touch(("Y", depth, (I, Jp)), s2, "r")
+            if c > 0:
+                pending.append((S.record(stream), dlo, dhi))
+    return S, acc
+
+
+def ordering_violations(S, acc):
+    bad = []
+    for key, lst in acc.items():
+        lst = sorted(set(lst))
+        writers = [n for n, m in lst if m == "w"]
+        if key[0] == "W":
+            # every read-modify-write of a W~ tile (updates and the leaf) in
+            # one chain
+            for a_, b_ in zip(writers, writers[1:]):
+                if not S.before(a_, b_):
+                    bad.append((key, a_, b_))
+        else:
+            # each reader after the latest writer enqueued before it, and
+            # before the next writer (Y buffers are reused across
+            # propagations of the same depth)
+            for n, m in lst:
+                if m != "r":
+                    continue
+                prev = [w for w in writers if w < n]
+                nxt = [w for w in writers if w > n]
+                if not prev or not S.before(prev[-1], n):
+                    bad.append((key, "read before write", n))
+                if nxt and not S.before(n, nxt[0]):
+                    bad.append((key, "overwritten before read", n))
+    return bad
+
+
+def contributions_solve(ops, chunks, items, M, N):
+    """count[Ip, Jp, I, J]: times the error of tile (I, J) reaches (Ip, Jp);
+    also checks each contribution's source leaf precedes the propagation and
+    its target lies in the chunk's target range."""
+    count = np.zeros((M, N, M, N), dtype=np.int32)
+    done_diag = set()
+    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops:
+        if kind == 0:
+            done_diag.add(D)
+            continue
+        yset = {}
+        for c in range(nchunks):
+            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c]
+            for Jp, I, k0, k1 in items[off1:off1 + n1]:
+                assert (I, Jp) not in yset, "Y tile computed twice in one propagation"
+                yset[(I, Jp)] = (c, range(k0, k1))
+                for J in range(k0, k1):
+                    assert I + J in done_diag, "stage 1 reads an unfinished source"
+            for Ip, Jp, k0, k1 in items[off:off + nn]:
+                assert dlo <= Ip + Jp < dhi, "stage-2 target outside its chunk's range"
+                for I in range(k0, k1):
+                    cy, js = yset[(I, Jp)]
+                    assert cy <= c, "stage 2 reads a Y tile of a later chunk"
+                    for J in js:
+                        assert I <= Ip and J <= Jp
+                        count[Ip, Jp, I, J] += 1
+    return count
+
+
+def expected_counts(M, N):
+    I = np.arange(M)[:, None, None, None]
+    J = np.arange(N)[None, :, None, None]
+    i = np.arange(M)[None, None, :, None]
+    j = np.arange(N)[None, None, None, :]
+    return ((i <= I) & (j <= J) & ~((i == I) & (j == J))).astype(np.int32)
+
+
+SHAPES = [(1, 1), (1, 6), (6, 1), (2, 3), (4, 4), (5, 9), (8, 8), (11, 6), (16, 13)]
+
+
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_solve_schedule_applies_every_contribution_once(M, N):
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
+    leaves = [int(op[1]) for op in ops if op[0] == 0]
+    assert leaves == list(range(M + N - 1)), "one leaf per tile anti-diagonal, in order"
+    for op in ops:
+        if op[0] == 0:
+            D, I0, nt = int(op[1]), int(op[2]), int(op[3])
+            assert I0 == max(0, D - N + 1) and I0 + nt - 1 == min(D, M - 1)
+    count = contributions_solve(ops, chunks, items, M, N)
+    np.testing.assert_array_equal(count, expected_counts(M, N))
+
+
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_solve_streams_order_every_tile_access(M, N):
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
+    S, acc = model_solve(ops, chunks, items)
+    assert ordering_violations(S, acc) == []
+
+
+def test_solve_streams_without_the_propagation_wait_overlap():
+    """The checker is sensitive: with deferred chunks waited for only by the
+    leaf of their first target, a deeper propagation into the same diagonals
+    can update the same W~ tiles concurrently (seven diagonals suffice).  The
+    stage-2 updates are atomic adds, so that was correct, but the order of the
+    adds, and with it the fp32 rounding of W~, could change from run to run;
+    ordered updates make the solve bit-reproducible."""
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, 4, 4))
+    S, acc = model_solve(ops, chunks, items, wait_at_propagation=False)
+    bad = ordering_violations(S, acc)
+    assert bad and all(b[0][0] == "W" for b in bad)
+
+
+@pytest.mark.parametrize("M,N", [(1, 1), (3, 1), (1, 7), (4, 5), (9, 16), (6, 33)])
+def test_rows_schedule(M, N):
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_ROWS, M, N))
+    assert [int(op[1]) for op in ops if op[0] == 0] == list(range(N))
+    # exactly-once: column tile J reaches J' > J for every row tile, before leaf J'
+    count = np.zeros((M, N, N), dtype=np.int32)   # [row, target J', source J]
+    done = set()
+    for kind, J, _, _, depth, chunk0, nchunks in ops:
+        if kind == 0:
+            done.add(J)
+            continue
+        for c in range(nchunks):
+            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c]
+            assert n1 == 0
+            for I, Jp, k0, k1 in items[off:off + nn]:
+                assert dlo <= Jp < dhi
+                for Js in range(k0, k1):
+                    assert Js in done and Js < Jp
+                    count[I, Jp, Js] += 1
+    want = np.broadcast_to(np.tril(np.ones((N, N), dtype=np.int32), -1), (M, N, N))
+    np.testing.assert_array_equal(count, want)
+    S, acc = model_solve(ops, chunks, items, one_sided=True)
+    assert ordering_violations(S, acc) == []
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 8, 13, 17])
+def test_prepare_trailing_updates_once_in_groups(nb):
+    syrk, levels, items = parse_prepare(kb.schedule_export(kb.SCHEDULE_PREPARE, nb))
+    seen = {}
+    for j in range(nb):
+        off, n1, n2 = (int(x) for x in syrk[j])
+        grp = [items[off:off + 1] if j + 1 < nb else items[off:off]]
+        grp.append(items[off + 1:off + 1 + n1])
+        grp.append(items[off + 1 + n1:off + 1 + n1 + n2])
+        urgent, s1, s2 = ({(int(r), int(c)) for r, c, k0, k1 in g} for g in grp)
+        for g in grp:
+            for r, c, k0, k1 in g:
+                assert (k0, k1) == (j, j + 1), "one panel per trailing update"
+                key = (int(r), int(c), j)
+                assert key not in seen
+                seen[key] = True
+        # the urgent tile is what the next diagonal block reads, the
+        # lookahead group what the next step's panel reads
+        assert urgent == ({(j + 1, j + 1)} if j + 1 < nb else set())
+        want1 = {(r, j + 1) for r in range(j + 2, nb)} | ({(j + 2, j + 2)} if j + 2 < nb else set())
+        assert s1 == want1
+        assert s2 == {(r, c) for r in range(j + 3, nb) for c in range(j + 2, r + 1)}
+    want = {(r, c, j) for c in range(nb) for r in range(c, nb) for j in range(c)}
+    assert set(seen) == want
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 6, 8, 11, 16])
+def test_prepare_doubling_inverts_a_block_triangle(nb):
+    """Run the doubling pairs level by level on a random lower-triangular G of
+    nb 3 x 3 blocks (T = (G21 Ginv11)^T, then Ginv21 = -Ginv22 T^T with its
+    transposed copy): the result is G^{-1}."""
+    _, levels, items = parse_prepare(kb.schedule_export(kb.SCHEDULE_PREPARE, nb))
+    b = 3
+    n = nb * b
+    rng = np.random.default_rng(nb)
+    G = np.tril(rng.standard_normal((n, n))) + 4 * np.eye(n)
+
+    def t(X, r, c):
+        return X[r * b:(r + 1) * b, c * b:(c + 1) * b]
+
+    Gi = np.full((n, n), np.nan)
+    GiT = np.full((n, n), np.nan)
+    T = np.full((n, n), np.nan)
+    for i in range(nb):
+        for j in range(nb):
+            if j > i:
+                t(Gi, i, j)[:] = 0.0
+                t(GiT, j, i)[:] = 0.0
+        x = np.linalg.inv(t(G, i, i))
+        t(Gi, i, i)[:] = x
+        t(GiT, i, i)[:] = x.T
+    assert len(levels) == max(0, int(np.ceil(np.log2(nb))))
+    for pairs in levels:
+        for t_off, t_n, x_off, x_n in pairs:
+            for r, c, k0, k1 in items[t_off:t_off + t_n]:
+                t(T, r, c)[:] = sum(t(GiT, r, k) @ t(G, c, k).T for k in range(k0, k1))
+            for r, c, k0, k1 in items[x_off:x_off + x_n]:
+                x = -sum(t(Gi, r, k) @ t(T, c, k).T for k in range(k0, k1))
+                t(Gi, r, c)[:] = x
+                t(GiT, c, r)[:] = x.T
+    assert np.all(np.isfinite(Gi))
+    np.testing.assert_allclose(Gi @ G, np.eye(n), atol=1e-12)
+    np.testing.assert_array_equal(GiT, Gi.T)
+
+
+def test_schedule_export_rejects_bad_arguments():
+    import ctypes
+    L = kb.lib()
+    n = ctypes.c_int64(0)
+    for args in ((0, 0, 4), (0, 4, 0), (1, 8193, 1), (2, 0, 1), (9, 2, 2)):
+        assert L.bakron_schedule_export(args[0], args[1], args[2], None, 0, ctypes.byref(n)) == 1
+    assert L.bakron_schedule_export(0, 4, 4, None, 0, None) == 1
+    # a buffer smaller than the schedule is left untouched
+    need = ctypes.c_int64(0)
+    assert L.bakron_schedule_export(0, 3, 3, None, 0, ctypes.byref(need)) == 0
+    buf = (ctypes.c_int32 * 4)(-7, -7, -7, -7)
+    assert L.bakron_schedule_export(0, 3, 3, buf, 4, ctypes.byref(n)) == 0
+    assert n.value == need.value and list(buf) == [-7, -7, -7, -7]
