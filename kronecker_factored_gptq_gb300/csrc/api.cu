@@ -693,7 +693,7 @@ const char* bakron_status_string(int st) {
   }
 }
 
-int bakron_version(void) { return 10000; }
+int bakron_version(void) { return 10400; }
 
 int64_t bakron_kernel_launches(void) { return (int64_t)bakron::launches_so_far(); }
 
