@@ -178,27 +178,28 @@ def contributions_solve(ops, chunks, items, M, N):
     also checks each contribution's source leaf precedes the propagation and
     its target lies in the chunk's target range."""
     count = np.zeros((M, N, M, N), dtype=np.int32)
-    done_diag = set()
-    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops:
+    last_leaf = -1   # leaves run in diagonal order
+    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops.tolist():
         if kind == 0:
-            done_diag.add(D)
+            assert D == last_leaf + 1
+            last_leaf = D
             continue
         yset = {}
         for c in range(nchunks):
-            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c]
-            for Jp, I, k0, k1 in items[off1:off1 + n1]:
+            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
+            for Jp, I, k0, k1 in items[off1:off1 + n1].tolist():
                 assert (I, Jp) not in yset, "Y tile computed twice in one propagation"
-                yset[(I, Jp)] = (c, range(k0, k1))
-                for J in range(k0, k1):
-                    assert I + J in done_diag, "stage 1 reads an unfinished source"
-            for Ip, Jp, k0, k1 in items[off:off + nn]:
+                assert 0 <= k0 < k1 <= Jp + 1
+                assert I + k1 - 1 <= last_leaf, "stage 1 reads an unfinished source"
+                yset[(I, Jp)] = (c, k0, k1)
+            for Ip, Jp, k0, k1 in items[off:off + nn].tolist():
                 assert dlo <= Ip + Jp < dhi, "stage-2 target outside its chunk's range"
+                assert Ip + Jp > last_leaf, "stage 2 updates a finished tile"
+                assert 0 <= k0 < k1 <= Ip + 1
                 for I in range(k0, k1):
-                    cy, js = yset[(I, Jp)]
+                    cy, j0, j1 = yset[(I, Jp)]
                     assert cy <= c, "stage 2 reads a Y tile of a later chunk"
-                    for J in js:
-                        assert I <= Ip and J <= Jp
-                        count[Ip, Jp, I, J] += 1
+                    count[Ip, Jp, I, j0:j1] += 1
     return count
 
 
@@ -226,7 +227,16 @@ def test_solve_schedule_applies_every_contribution_once(M, N):
     np.testing.assert_array_equal(count, expected_counts(M, N))
 
 
-@pytest.mark.parametrize("M,N", SHAPES)
+@pytest.mark.parametrize("M,N", [(64, 64), (32, 112), (112, 32)])
+def test_solve_schedule_full_size_shapes(M, N):
+    """The 8192 x 8192 and the 4096 x 14336 / 14336 x 4096 workloads' tile
+    grids: every contribution exactly once, before its target's leaf."""
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
+    count = contributions_solve(ops, chunks, items, M, N)
+    np.testing.assert_array_equal(count, expected_counts(M, N))
+
+
+@pytest.mark.parametrize("M,N", SHAPES + [(64, 64), (32, 112)])
 def test_solve_streams_order_every_tile_access(M, N):
     ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
     S, acc = model_solve(ops, chunks, items)
