@@ -256,7 +256,7 @@ def test_solve_streams_without_the_propagation_wait_overlap():
     assert bad and all(b[0][0] == "W" for b in bad)
 
 
-@pytest.mark.parametrize("M,N", [(1, 1), (3, 1), (1, 7), (4, 5), (9, 16), (6, 33)])
+@pytest.mark.parametrize("M,N", [(1, 1), (3, 1), (1, 7), (4, 5), (9, 16), (6, 33), (64, 64), (32, 112)])
 def test_rows_schedule(M, N):
     ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_ROWS, M, N))
     assert [int(op[1]) for op in ops if op[0] == 0] == list(range(N))
