@@ -281,7 +281,7 @@ def test_rows_schedule(M, N):
     assert ordering_violations(S, acc) == []
 
 
-@pytest.mark.parametrize("nb", [1, 2, 3, 5, 8, 13, 17])
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 8, 13, 17, 64, 112])
 def test_prepare_trailing_updates_once_in_groups(nb):
     syrk, levels, items = parse_prepare(kb.schedule_export(kb.SCHEDULE_PREPARE, nb))
     seen = {}
@@ -307,7 +307,7 @@ def test_prepare_trailing_updates_once_in_groups(nb):
     assert set(seen) == want
 
 
-@pytest.mark.parametrize("nb", [1, 2, 3, 5, 6, 8, 11, 16])
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 6, 8, 11, 16, 64])
 def test_prepare_doubling_inverts_a_block_triangle(nb):
     """Run the doubling pairs level by level on a random lower-triangular G of
     nb 3 x 3 blocks (T = (G21 Ginv11)^T, then Ginv21 = -Ginv22 T^T with its
