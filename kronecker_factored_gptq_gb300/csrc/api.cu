@@ -848,12 +848,19 @@ bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const floa
   if (two) {
     int dev = 0;
     TRY_CUDA(cudaGetDevice(&dev));
-    std::thread tb([&] {
-      err[1] = cudaSetDevice(dev);
-      if (err[1] == cudaSuccess) err[1] = enqueue(1);
-    });
+    std::thread tb;
+    bool threaded = true;
+    try {
+      tb = std::thread([&] {
+        err[1] = cudaSetDevice(dev);
+        if (err[1] == cudaSuccess) err[1] = enqueue(1);
+      });
+    } catch (...) {
+      threaded = false;   // no thread to be had: enqueue B after A
+    }
     err[0] = enqueue(0);
-    tb.join();
+    if (threaded) tb.join();
+    else err[1] = enqueue(1);
   } else {
     err[0] = enqueue(0);
   }
@@ -1156,8 +1163,14 @@ bakron_status bakron_quantize_batch(int count, bakron_problem* p, const bakron_o
   };
   {
     std::vector<std::thread> th;
-    for (int k = 1; k < nslots; ++k) th.emplace_back(enqueue_slot, k);
+    int k = 1;
+    try {
+      for (; k < nslots; ++k) th.emplace_back(enqueue_slot, k);
+    } catch (...) {
+      // no more threads to be had: the remaining slots are enqueued here
+    }
     enqueue_slot(0);
+    for (int j = k; j < nslots; ++j) enqueue_slot(j);
     for (auto& t : th) t.join();
   }
   bakron_status first = BAKRON_OK;
