@@ -27,6 +27,11 @@
  *   unspecified when the status is not BAKRON_OK.
  * - Argument validation happens before anything is enqueued and returns
  *   BAKRON_ERR_INVALID_ARG with no side effects (no CUDA call is made).
+ * - Size limits: W is m x n with m, n <= 2^20 and at most 2^20 tiles of
+ *   128 x 128 (ceil(m/128) ceil(n/128) <= 2^20); factor orders of
+ *   bakron_prepare and bakron_factors are at most 65536.  Larger sizes, and a
+ *   host allocation failure while building a schedule, return
+ *   BAKRON_ERR_INVALID_ARG.
  */
 #ifndef BAKRON_H
 #define BAKRON_H
@@ -103,7 +108,8 @@ int64_t bakron_kernel_launches(void);
  *                            (N is ignored)
  * out receives int32 values, host memory; *len (host) the count the
  * schedule needs.  Nothing is written to out when cap < *len (pass cap = 0
- * to size it).  M, N in [1, 8192]; anything else is BAKRON_ERR_INVALID_ARG.
+ * to size it).  SOLVE / ROWS: M, N in [1, 8192] with M N <= 2^20; PREPARE:
+ * M in [1, 512]; anything else is BAKRON_ERR_INVALID_ARG.
  * Layout (every offset counts work items, each item 4 values r, c, k0, k1):
  *   SOLVE / ROWS: n_ops, n_chunks, n_items; n_ops records of 7 values
  *     kind (0 leaf, 1 propagation), D (leaf diagonal or column tile), I0,

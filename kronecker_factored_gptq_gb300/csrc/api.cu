@@ -519,7 +519,10 @@ struct PhaseTimer {
   }
 };
 
-bool sizes_ok(int64_t m, int64_t n) { return m >= 1 && n >= 1 && m <= (1 << 20) && n <= (1 << 20); }
+bool sizes_ok(int64_t m, int64_t n) {
+  return m >= 1 && n >= 1 && m <= (1 << 20) && n <= (1 << 20) &&
+         ((m + T - 1) / T) * ((n + T - 1) / T) <= kMaxTiles;
+}
 
 // The one-sided solve (U_B = I): see RowsSchedule.  Arguments validated by
 // bakron_quantize; the workspace layout is the two-sided one (its Y^T and
@@ -699,77 +702,90 @@ int64_t bakron_kernel_launches(void) { return (int64_t)bakron::launches_so_far()
 
 bakron_status bakron_schedule_export(int kind, int64_t M, int64_t N, int32_t* out, int64_t cap,
                                      int64_t* len) {
-  if (!len || cap < 0 || (cap > 0 && !out)) return BAKRON_ERR_INVALID_ARG;
-  if (M < 1 || M > 8192 || (kind != BAKRON_SCHEDULE_PREPARE && (N < 1 || N > 8192)))
-    return BAKRON_ERR_INVALID_ARG;
-  std::vector<int32_t> v;
-  auto items = [&](const std::vector<WorkItem>& it) {
-    for (const WorkItem& w : it) {
-      v.push_back(w.r);
-      v.push_back(w.c);
-      v.push_back(w.k0);
-      v.push_back(w.k1);
+  try {
+    if (!len || cap < 0 || (cap > 0 && !out)) return BAKRON_ERR_INVALID_ARG;
+    if (kind == BAKRON_SCHEDULE_PREPARE ? (M < 1 || M > kMaxOrder / T)
+                                        : (M < 1 || N < 1 || M > 8192 || N > 8192 || M * N > kMaxTiles))
+      return BAKRON_ERR_INVALID_ARG;
+    std::vector<int32_t> v;
+    auto items = [&](const std::vector<WorkItem>& it) {
+      for (const WorkItem& w : it) {
+        v.push_back(w.r);
+        v.push_back(w.c);
+        v.push_back(w.k0);
+        v.push_back(w.k1);
+      }
+    };
+    auto chunks = [&](const std::vector<Chunk>& ch) {
+      for (const Chunk& c : ch) {
+        v.push_back(c.dlo);
+        v.push_back(c.dhi);
+        v.push_back(c.off1);
+        v.push_back(c.n1);
+        v.push_back(c.off);
+        v.push_back(c.n);
+      }
+    };
+    if (kind == BAKRON_SCHEDULE_SOLVE) {
+      const Schedule& s = get_schedule((int)M, (int)N);
+      v.push_back((int32_t)s.ops.size());
+      v.push_back((int32_t)s.chunks.size());
+      v.push_back((int32_t)s.items.size());
+      for (const Op& op : s.ops) {
+        const int32_t rec[7] = {op.kind, op.kind == 0 ? op.D : 0, op.kind == 0 ? op.I0 : 0,
+                                op.kind == 0 ? op.ntiles : 0, op.kind == 1 ? op.depth : 0,
+                                op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
+        v.insert(v.end(), rec, rec + 7);
+      }
+      chunks(s.chunks);
+      items(s.items);
+    } else if (kind == BAKRON_SCHEDULE_ROWS) {
+      const RowsSchedule& s = get_rows_schedule((int)M, (int)N);
+      v.push_back((int32_t)s.ops.size());
+      v.push_back((int32_t)s.chunks.size());
+      v.push_back((int32_t)s.items.size());
+      for (const RowsOp& op : s.ops) {
+        const int32_t rec[7] = {op.kind, op.kind == 0 ? op.J : 0, 0, op.kind == 0 ? (int32_t)M : 0,
+                                op.depth, op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
+        v.insert(v.end(), rec, rec + 7);
+      }
+      chunks(s.chunks);
+      items(s.items);
+    } else if (kind == BAKRON_SCHEDULE_PREPARE) {
+      prepare_schedule_export(M, v);
+    } else {
+      return BAKRON_ERR_INVALID_ARG;
     }
-  };
-  auto chunks = [&](const std::vector<Chunk>& ch) {
-    for (const Chunk& c : ch) {
-      v.push_back(c.dlo);
-      v.push_back(c.dhi);
-      v.push_back(c.off1);
-      v.push_back(c.n1);
-      v.push_back(c.off);
-      v.push_back(c.n);
-    }
-  };
-  if (kind == BAKRON_SCHEDULE_SOLVE) {
-    const Schedule& s = get_schedule((int)M, (int)N);
-    v.push_back((int32_t)s.ops.size());
-    v.push_back((int32_t)s.chunks.size());
-    v.push_back((int32_t)s.items.size());
-    for (const Op& op : s.ops) {
-      const int32_t rec[7] = {op.kind, op.kind == 0 ? op.D : 0, op.kind == 0 ? op.I0 : 0,
-                              op.kind == 0 ? op.ntiles : 0, op.kind == 1 ? op.depth : 0,
-                              op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
-      v.insert(v.end(), rec, rec + 7);
-    }
-    chunks(s.chunks);
-    items(s.items);
-  } else if (kind == BAKRON_SCHEDULE_ROWS) {
-    const RowsSchedule& s = get_rows_schedule((int)M, (int)N);
-    v.push_back((int32_t)s.ops.size());
-    v.push_back((int32_t)s.chunks.size());
-    v.push_back((int32_t)s.items.size());
-    for (const RowsOp& op : s.ops) {
-      const int32_t rec[7] = {op.kind, op.kind == 0 ? op.J : 0, 0, op.kind == 0 ? (int32_t)M : 0,
-                              op.depth, op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
-      v.insert(v.end(), rec, rec + 7);
-    }
-    chunks(s.chunks);
-    items(s.items);
-  } else if (kind == BAKRON_SCHEDULE_PREPARE) {
-    prepare_schedule_export(M, v);
-  } else {
-    return BAKRON_ERR_INVALID_ARG;
+    *len = (int64_t)v.size();
+    if (cap >= *len && *len > 0) std::memcpy(out, v.data(), sizeof(int32_t) * v.size());
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
   }
-  *len = (int64_t)v.size();
-  if (cap >= *len && *len > 0) std::memcpy(out, v.data(), sizeof(int32_t) * v.size());
-  return BAKRON_OK;
 }
 
 bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts, size_t* bytes) {
-  if (!bytes || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
-  if (opts && !valid_opts(*opts)) return BAKRON_ERR_INVALID_ARG;
-  const QLayout q = quantize_layout(m, n);
-  const ALayout a = antidiag_layout(m, n);
-  *bytes = std::max(q.total, a.total);
-  return BAKRON_OK;
+  try {
+    if (!bytes || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
+    if (opts && !valid_opts(*opts)) return BAKRON_ERR_INVALID_ARG;
+    const QLayout q = quantize_layout(m, n);
+    const ALayout a = antidiag_layout(m, n);
+    *bytes = std::max(q.total, a.total);
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
 }
 
 bakron_status bakron_prepare_workspace_size(int64_t n, int64_t m, size_t* bytes) {
-  if (!bytes || n < 0 || m < 0 || (n == 0 && m == 0) || n > (1 << 20) || m > (1 << 20))
-    return BAKRON_ERR_INVALID_ARG;
-  *bytes = prepare_layout(n, m).total;
-  return BAKRON_OK;
+  try {
+    if (!bytes || n < 0 || m < 0 || (n == 0 && m == 0) || n > kMaxOrder || m > kMaxOrder)
+      return BAKRON_ERR_INVALID_ARG;
+    *bytes = prepare_layout(n, m).total;
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
 }
 
 bakron_status bakron_rowscale(const float* W, int64_t m, int64_t n, int qmax, float* scale,
@@ -784,101 +800,105 @@ bakron_status bakron_rowscale(const float* W, int64_t m, int64_t n, int qmax, fl
 bakron_status bakron_prepare(const float* A, int64_t n, float damp_A, const float* B, int64_t m,
                              float damp_B, float* UA, float* UB, float* LA, float* LB,
                              int64_t* info, void* ws, size_t ws_bytes, void* stream) {
-  if (!A || n < 1 || !UA || !ws) return BAKRON_ERR_INVALID_ARG;
-  if (B && (m < 1 || !UB)) return BAKRON_ERR_INVALID_ARG;
-  if (!B) m = 0;
-  if (!(damp_A >= 0.f) || !(damp_B >= 0.f)) return BAKRON_ERR_INVALID_ARG;
-  if (n > (1 << 20) || m > (1 << 20)) return BAKRON_ERR_INVALID_ARG;
-  const PLayout L = prepare_layout(n, m);
-  if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
-  if (!prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
-  cudaStream_t s = (cudaStream_t)stream;
-  char* base = (char*)ws;
-  DevStatus* st = (DevStatus*)(base + L.status);
-  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
-  TRY_CUDA(cudaMemsetAsync(st->info, 0x7f, sizeof(st->info), s));
-  PrepStreams* ps = nullptr;
-  TRY_CUDA(prep_streams(&ps));
-  std::lock_guard<std::mutex> plk(ps->mu);
-  const size_t ev_per = 5 * (size_t)(std::max(L.kp[0], L.kp[1]) / T + 1);
-  TRY_CUDA(prep_events(ps, 2 * ev_per));
-  TRY_CUDA(cudaEventRecord(ps->fork, s));
-  // enqueue one factor's preparation on its own streams, after the fork
-  auto enqueue = [&](int which) -> cudaError_t {
-    const float* X = which == 0 ? A : B;
-    const int64_t k = which == 0 ? n : m;
-    cudaStream_t fs = ps->main[which];
-    cudaError_t e;
-    if ((e = cudaStreamWaitEvent(fs, ps->fork, 0)) != cudaSuccess) return e;
-    // the other streams start after the factor's stream reaches this point
-    cudaEvent_t start = ps->events[which * ev_per + ev_per - 1];
-    if ((e = cudaEventRecord(start, fs)) != cudaSuccess) return e;
-    for (cudaStream_t o : {ps->side[which], ps->bulk[which], ps->inv[which]})
-      if ((e = cudaStreamWaitEvent(o, start, 0)) != cudaSuccess) return e;
-    PrepareFactorArgs pa{};
-    pa.X = X; pa.k = k; pa.damp = which == 0 ? damp_A : damp_B;
-    pa.U = which == 0 ? UA : UB;
-    pa.L = which == 0 ? LA : LB;
-    pa.C = (float*)(base + L.C[which]);
-    pa.Chi = (float*)(base + L.Chi[which]);
-    pa.Clo = (float*)(base + L.Clo[which]);
-    pa.Gihi = (float*)(base + L.Gihi[which]);
-    pa.Gilo = (float*)(base + L.Gilo[which]);
-    pa.GiThi = (float*)(base + L.GiThi[which]);
-    pa.GiTlo = (float*)(base + L.GiTlo[which]);
-    pa.Thi = (float*)(base + L.Thi[which]);
-    pa.Tlo = (float*)(base + L.Tlo[which]);
-    pa.items = (WorkItem*)(base + L.items[which]);
-    pa.scal = (float*)(base + L.scal) + which;
-    pa.kp = L.kp[which];
-    pa.which = which;
-    pa.st = st;
-    pa.side = ps->side[which];
-    pa.bulk = ps->bulk[which];
-    pa.inv = ps->inv[which];
-    pa.ev = ps->events.data() + which * ev_per;
-    if ((e = run_prepare_factor(pa, fs)) != cudaSuccess) return e;
-    return cudaEventRecord(ps->events[which * ev_per + ev_per - 2], fs);
-  };
-  // Each factor's chain takes milliseconds of host time to enqueue, so with
-  // two factors B is enqueued from a second host thread and both chains start
-  // on the device together.
-  cudaError_t err[2] = {cudaSuccess, cudaSuccess};
-  const bool two = B && m > 0;
-  if (two) {
-    int dev = 0;
-    TRY_CUDA(cudaGetDevice(&dev));
-    std::thread tb;
-    bool threaded = true;
-    try {
-      tb = std::thread([&] {
-        err[1] = cudaSetDevice(dev);
-        if (err[1] == cudaSuccess) err[1] = enqueue(1);
-      });
-    } catch (...) {
-      threaded = false;   // no thread to be had: enqueue B after A
+  try {
+    if (!A || n < 1 || !UA || !ws) return BAKRON_ERR_INVALID_ARG;
+    if (B && (m < 1 || !UB)) return BAKRON_ERR_INVALID_ARG;
+    if (!B) m = 0;
+    if (!(damp_A >= 0.f) || !(damp_B >= 0.f)) return BAKRON_ERR_INVALID_ARG;
+    if (n > kMaxOrder || m > kMaxOrder) return BAKRON_ERR_INVALID_ARG;
+    const PLayout L = prepare_layout(n, m);
+    if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
+    if (!prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* base = (char*)ws;
+    DevStatus* st = (DevStatus*)(base + L.status);
+    TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+    TRY_CUDA(cudaMemsetAsync(st->info, 0x7f, sizeof(st->info), s));
+    PrepStreams* ps = nullptr;
+    TRY_CUDA(prep_streams(&ps));
+    std::lock_guard<std::mutex> plk(ps->mu);
+    const size_t ev_per = 5 * (size_t)(std::max(L.kp[0], L.kp[1]) / T + 1);
+    TRY_CUDA(prep_events(ps, 2 * ev_per));
+    TRY_CUDA(cudaEventRecord(ps->fork, s));
+    // enqueue one factor's preparation on its own streams, after the fork
+    auto enqueue = [&](int which) -> cudaError_t {
+      const float* X = which == 0 ? A : B;
+      const int64_t k = which == 0 ? n : m;
+      cudaStream_t fs = ps->main[which];
+      cudaError_t e;
+      if ((e = cudaStreamWaitEvent(fs, ps->fork, 0)) != cudaSuccess) return e;
+      // the other streams start after the factor's stream reaches this point
+      cudaEvent_t start = ps->events[which * ev_per + ev_per - 1];
+      if ((e = cudaEventRecord(start, fs)) != cudaSuccess) return e;
+      for (cudaStream_t o : {ps->side[which], ps->bulk[which], ps->inv[which]})
+        if ((e = cudaStreamWaitEvent(o, start, 0)) != cudaSuccess) return e;
+      PrepareFactorArgs pa{};
+      pa.X = X; pa.k = k; pa.damp = which == 0 ? damp_A : damp_B;
+      pa.U = which == 0 ? UA : UB;
+      pa.L = which == 0 ? LA : LB;
+      pa.C = (float*)(base + L.C[which]);
+      pa.Chi = (float*)(base + L.Chi[which]);
+      pa.Clo = (float*)(base + L.Clo[which]);
+      pa.Gihi = (float*)(base + L.Gihi[which]);
+      pa.Gilo = (float*)(base + L.Gilo[which]);
+      pa.GiThi = (float*)(base + L.GiThi[which]);
+      pa.GiTlo = (float*)(base + L.GiTlo[which]);
+      pa.Thi = (float*)(base + L.Thi[which]);
+      pa.Tlo = (float*)(base + L.Tlo[which]);
+      pa.items = (WorkItem*)(base + L.items[which]);
+      pa.scal = (float*)(base + L.scal) + which;
+      pa.kp = L.kp[which];
+      pa.which = which;
+      pa.st = st;
+      pa.side = ps->side[which];
+      pa.bulk = ps->bulk[which];
+      pa.inv = ps->inv[which];
+      pa.ev = ps->events.data() + which * ev_per;
+      if ((e = run_prepare_factor(pa, fs)) != cudaSuccess) return e;
+      return cudaEventRecord(ps->events[which * ev_per + ev_per - 2], fs);
+    };
+    // Each factor's chain takes milliseconds of host time to enqueue, so with
+    // two factors B is enqueued from a second host thread and both chains start
+    // on the device together.
+    cudaError_t err[2] = {cudaSuccess, cudaSuccess};
+    const bool two = B && m > 0;
+    if (two) {
+      int dev = 0;
+      TRY_CUDA(cudaGetDevice(&dev));
+      std::thread tb;
+      bool threaded = true;
+      try {
+        tb = std::thread([&] {
+          err[1] = cudaSetDevice(dev);
+          if (err[1] == cudaSuccess) err[1] = enqueue(1);
+        });
+      } catch (...) {
+        threaded = false;   // no thread to be had: enqueue B after A
+      }
+      err[0] = enqueue(0);
+      if (threaded) tb.join();
+      else err[1] = enqueue(1);
+    } else {
+      err[0] = enqueue(0);
     }
-    err[0] = enqueue(0);
-    if (threaded) tb.join();
-    else err[1] = enqueue(1);
-  } else {
-    err[0] = enqueue(0);
-  }
-  TRY_CUDA(err[0]);
-  TRY_CUDA(err[1]);
-  // join the chains back onto the caller's stream
-  for (int which = 0; which < (two ? 2 : 1); ++which)
-    TRY_CUDA(cudaStreamWaitEvent(s, ps->events[which * ev_per + ev_per - 2], 0));
-  DevStatus h{};
-  bakron_status r = finish(s, st, &h);
-  if (info) {
-    for (int w = 0; w < 2; ++w) {
-      const int64_t k = w == 0 ? n : m;
-      const long long f = h.info[w];
-      info[w] = (k > 0 && f >= 0 && f < k) ? (k - 1 - f) : -1;
+    TRY_CUDA(err[0]);
+    TRY_CUDA(err[1]);
+    // join the chains back onto the caller's stream
+    for (int which = 0; which < (two ? 2 : 1); ++which)
+      TRY_CUDA(cudaStreamWaitEvent(s, ps->events[which * ev_per + ev_per - 2], 0));
+    DevStatus h{};
+    bakron_status r = finish(s, st, &h);
+    if (info) {
+      for (int w = 0; w < 2; ++w) {
+        const int64_t k = w == 0 ? n : m;
+        const long long f = h.info[w];
+        info[w] = (k > 0 && f >= 0 && f < k) ? (k - 1 - f) : -1;
+      }
     }
+    return r;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
   }
-  return r;
 }
 
 }  // extern "C"
@@ -1066,9 +1086,13 @@ bakron_status bakron_quantize(const float* W, int64_t m, int64_t n, const float*
                               const float* scale, int qmin, int qmax, float* V, int8_t* codes,
                               float* preround, const bakron_opts* opts, void* ws,
                               size_t ws_bytes, void* stream) {
-  const GridIn gr{scale, nullptr, n, 1};
-  return quantize_impl(W, m, n, UA, UB, gr, qmin, qmax, V, codes, preround, opts, ws, ws_bytes,
-                       stream);
+  try {
+    const GridIn gr{scale, nullptr, n, 1};
+    return quantize_impl(W, m, n, UA, UB, gr, qmin, qmax, V, codes, preround, opts, ws, ws_bytes,
+                         stream);
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
 }
 
 bakron_status bakron_quantize_grid(const float* W, int64_t m, int64_t n, const float* UA,
@@ -1076,11 +1100,15 @@ bakron_status bakron_quantize_grid(const float* W, int64_t m, int64_t n, const f
                                    int64_t group, int qmin, int qmax, float* V, int8_t* codes,
                                    float* preround, const bakron_opts* opts, void* ws,
                                    size_t ws_bytes, void* stream) {
-  const int64_t ng = grid_groups(n, group);
-  if (ng < 1 || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
-  const GridIn gr{scale, zero, ng == 1 ? n : group, ng};
-  return quantize_impl(W, m, n, UA, UB, gr, qmin, qmax, V, codes, preround, opts, ws, ws_bytes,
-                       stream);
+  try {
+    const int64_t ng = grid_groups(n, group);
+    if (ng < 1 || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
+    const GridIn gr{scale, zero, ng == 1 ? n : group, ng};
+    return quantize_impl(W, m, n, UA, UB, gr, qmin, qmax, V, codes, preround, opts, ws, ws_bytes,
+                         stream);
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
 }
 
 bakron_status bakron_grid_params(const float* W, int64_t m, int64_t n, int bits, int asymmetric,
@@ -1100,97 +1128,105 @@ bakron_status bakron_grid_params(const float* W, int64_t m, int64_t n, int bits,
 
 bakron_status bakron_batch_workspace_size(int count, const bakron_problem* p,
                                           const bakron_opts* opts, size_t* bytes) {
-  if (count < 1 || !p || !bytes) return BAKRON_ERR_INVALID_ARG;
-  size_t total = 0;
-  for (int i = 0; i < count; ++i) {
-    size_t b = 0;
-    bakron_status st = bakron_workspace_size(p[i].m, p[i].n, opts, &b);
-    if (st != BAKRON_OK) return st;
-    total += (b + 1023) / 1024 * 1024;
+  try {
+    if (count < 1 || !p || !bytes) return BAKRON_ERR_INVALID_ARG;
+    size_t total = 0;
+    for (int i = 0; i < count; ++i) {
+      size_t b = 0;
+      bakron_status st = bakron_workspace_size(p[i].m, p[i].n, opts, &b);
+      if (st != BAKRON_OK) return st;
+      total += (b + 1023) / 1024 * 1024;
+    }
+    *bytes = total;
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
   }
-  *bytes = total;
-  return BAKRON_OK;
 }
 
 bakron_status bakron_quantize_batch(int count, bakron_problem* p, const bakron_opts* opts, void* ws,
                                     size_t ws_bytes, void* stream) {
-  size_t need = 0;
-  bakron_status vs = bakron_batch_workspace_size(count, p, opts, &need);
-  if (vs != BAKRON_OK) return vs;
-  if (!ws || ws_bytes < need) return BAKRON_ERR_INVALID_ARG;
-  for (int i = 0; i < count; ++i) {
-    p[i].status = BAKRON_OK;
-    if (grid_groups(p[i].n, p[i].group) < 1) return BAKRON_ERR_INVALID_ARG;
-  }
-  cudaStream_t s = (cudaStream_t)stream;
-  const int nslots = std::min(count, kSlots);
-  std::vector<SolveStreams*> sets(nslots, nullptr);
-  std::vector<std::unique_lock<std::mutex>> locks;
-  std::vector<size_t> nev(nslots, 0);
-  for (int k = 0; k < nslots; ++k) {
-    TRY_CUDA(solve_streams(&sets[k], k));
-    locks.emplace_back(sets[k]->mu);
-  }
-  std::vector<BatchCtx> ctx(count);
-  std::vector<int> enq(count, 0);
-  std::vector<size_t> offs(count + 1, 0);
-  for (int i = 0; i < count; ++i) {
-    size_t b = 0;
-    bakron_workspace_size(p[i].m, p[i].n, opts, &b);
-    offs[i + 1] = offs[i] + (b + 1023) / 1024 * 1024;
-  }
-  (void)prop_tc_supported();   // cached before the enqueuing threads start
-  int dev = 0;
-  TRY_CUDA(cudaGetDevice(&dev));
-  // one host thread per stream set enqueues its problems, so a launch queue
-  // that fills up for one problem does not hold back the others
-  auto enqueue_slot = [&](int k) {
-    if (cudaSetDevice(dev) != cudaSuccess) {
-      for (int i = k; i < count; i += nslots) p[i].status = BAKRON_ERR_CUDA;
-      return;
+  try {
+    size_t need = 0;
+    bakron_status vs = bakron_batch_workspace_size(count, p, opts, &need);
+    if (vs != BAKRON_OK) return vs;
+    if (!ws || ws_bytes < need) return BAKRON_ERR_INVALID_ARG;
+    for (int i = 0; i < count; ++i) {
+      p[i].status = BAKRON_OK;
+      if (grid_groups(p[i].n, p[i].group) < 1) return BAKRON_ERR_INVALID_ARG;
     }
-    for (int i = k; i < count; i += nslots) {
-      const int64_t ng = grid_groups(p[i].n, p[i].group);
-      const GridIn gr{p[i].scale, p[i].zero, ng == 1 ? p[i].n : p[i].group, ng};
-      ctx[i].ss = sets[k];
-      ctx[i].nev = &nev[k];
-      const bakron_status st = quantize_impl(
-          p[i].W, p[i].m, p[i].n, p[i].UA, p[i].UB, gr, p[i].qmin, p[i].qmax, p[i].V, p[i].codes,
-          nullptr, opts, (char*)ws + offs[i], offs[i + 1] - offs[i], stream, &ctx[i]);
-      p[i].status = st;
-      enq[i] = st == BAKRON_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int nslots = std::min(count, kSlots);
+    std::vector<SolveStreams*> sets(nslots, nullptr);
+    std::vector<std::unique_lock<std::mutex>> locks;
+    std::vector<size_t> nev(nslots, 0);
+    for (int k = 0; k < nslots; ++k) {
+      TRY_CUDA(solve_streams(&sets[k], k));
+      locks.emplace_back(sets[k]->mu);
     }
-  };
-  {
-    std::vector<std::thread> th;
-    int k = 1;
-    try {
-      for (; k < nslots; ++k) th.emplace_back(enqueue_slot, k);
-    } catch (...) {
-      // no more threads to be had: the remaining slots are enqueued here
+    std::vector<BatchCtx> ctx(count);
+    std::vector<int> enq(count, 0);
+    std::vector<size_t> offs(count + 1, 0);
+    for (int i = 0; i < count; ++i) {
+      size_t b = 0;
+      bakron_workspace_size(p[i].m, p[i].n, opts, &b);
+      offs[i + 1] = offs[i] + (b + 1023) / 1024 * 1024;
     }
-    enqueue_slot(0);
-    for (int j = k; j < nslots; ++j) enqueue_slot(j);
-    for (auto& t : th) t.join();
+    (void)prop_tc_supported();   // cached before the enqueuing threads start
+    int dev = 0;
+    TRY_CUDA(cudaGetDevice(&dev));
+    // one host thread per stream set enqueues its problems, so a launch queue
+    // that fills up for one problem does not hold back the others
+    auto enqueue_slot = [&](int k) {
+      if (cudaSetDevice(dev) != cudaSuccess) {
+        for (int i = k; i < count; i += nslots) p[i].status = BAKRON_ERR_CUDA;
+        return;
+      }
+      for (int i = k; i < count; i += nslots) {
+        const int64_t ng = grid_groups(p[i].n, p[i].group);
+        const GridIn gr{p[i].scale, p[i].zero, ng == 1 ? p[i].n : p[i].group, ng};
+        ctx[i].ss = sets[k];
+        ctx[i].nev = &nev[k];
+        const bakron_status st = quantize_impl(
+            p[i].W, p[i].m, p[i].n, p[i].UA, p[i].UB, gr, p[i].qmin, p[i].qmax, p[i].V, p[i].codes,
+            nullptr, opts, (char*)ws + offs[i], offs[i + 1] - offs[i], stream, &ctx[i]);
+        p[i].status = st;
+        enq[i] = st == BAKRON_OK;
+      }
+    };
+    {
+      std::vector<std::thread> th;
+      int k = 1;
+      try {
+        for (; k < nslots; ++k) th.emplace_back(enqueue_slot, k);
+      } catch (...) {
+        // no more threads to be had: the remaining slots are enqueued here
+      }
+      enqueue_slot(0);
+      for (int j = k; j < nslots; ++j) enqueue_slot(j);
+      for (auto& t : th) t.join();
+    }
+    bakron_status first = BAKRON_OK;
+    for (int i = 0; i < count; ++i)
+      if (!enq[i] && first == BAKRON_OK) first = (bakron_status)p[i].status;
+    // join every enqueued problem onto the caller's stream, then read the
+    // status blocks
+    std::vector<DevStatus> hs(count);
+    for (int i = 0; i < count; ++i)
+      if (enq[i]) TRY_CUDA(cudaStreamWaitEvent(s, ctx[i].done, 0));
+    for (int i = 0; i < count; ++i)
+      if (enq[i])
+        TRY_CUDA(cudaMemcpyAsync(&hs[i], ctx[i].st, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+    TRY_CUDA(cudaStreamSynchronize(s));
+    for (int i = 0; i < count; ++i)
+      if (enq[i]) {
+        p[i].status = hs[i].status;
+        if (first == BAKRON_OK && hs[i].status != BAKRON_OK) first = (bakron_status)hs[i].status;
+      }
+    return first;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
   }
-  bakron_status first = BAKRON_OK;
-  for (int i = 0; i < count; ++i)
-    if (!enq[i] && first == BAKRON_OK) first = (bakron_status)p[i].status;
-  // join every enqueued problem onto the caller's stream, then read the
-  // status blocks
-  std::vector<DevStatus> hs(count);
-  for (int i = 0; i < count; ++i)
-    if (enq[i]) TRY_CUDA(cudaStreamWaitEvent(s, ctx[i].done, 0));
-  for (int i = 0; i < count; ++i)
-    if (enq[i])
-      TRY_CUDA(cudaMemcpyAsync(&hs[i], ctx[i].st, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
-  TRY_CUDA(cudaStreamSynchronize(s));
-  for (int i = 0; i < count; ++i)
-    if (enq[i]) {
-      p[i].status = hs[i].status;
-      if (first == BAKRON_OK && hs[i].status != BAKRON_OK) first = (bakron_status)hs[i].status;
-    }
-  return first;
 }
 
 bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n, const float* UA,
@@ -1199,41 +1235,45 @@ bakron_status bakron_quantize_antidiag(const float* W, int64_t m, int64_t n, con
                                        const int8_t* guide_codes, float guide_tol,
                                        int64_t* overrides, const bakron_opts* opts_in, void* ws,
                                        size_t ws_bytes, void* stream) {
-  bakron_opts o;
-  bakron_default_opts(&o);
-  if (opts_in) o = *opts_in;
-  if (!valid_opts(o)) return BAKRON_ERR_INVALID_ARG;
-  if (!W || !UA || !UB || !scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
-  if (!sizes_ok(m, n) || qmin > qmax) return BAKRON_ERR_INVALID_ARG;
-  if (guide_codes && !(guide_tol >= 0.f)) return BAKRON_ERR_INVALID_ARG;
-  const ALayout L = antidiag_layout(m, n);
-  if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  char* base = (char*)ws;
-  DevStatus* st = (DevStatus*)(base + L.status);
-  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
-  TRY_CUDA(launch_check_finite(scale, m, st, s));
-  TRY_CUDA(cudaMemcpyAsync(base + L.wt, W, sizeof(float) * m * n, cudaMemcpyDeviceToDevice, s));
-  AntidiagArgs a{};
-  a.wt = (float*)(base + L.wt);
-  a.UA = UA; a.UB = UB; a.scale = scale;
-  a.ebuf = (float*)(base + L.ebuf);
-  a.V = V; a.codes = codes; a.preround = preround;
-  a.guide = guide_codes; a.guide_tol = guide_tol;
-  a.m = m; a.n = n; a.qmin = qmin; a.qmax = qmax;
-  a.budget = o.spin_budget_cycles > 0 ? o.spin_budget_cycles : 4000000000LL;
-  a.fault_inject = o.fault_inject;
-  a.st = st;
-  int unsupported = 0;
-  TRY_CUDA(launch_antidiag(a, &unsupported, s));
-  if (unsupported) {
-    TRY_CUDA(cudaStreamSynchronize(s));
-    return BAKRON_ERR_UNSUPPORTED;
+  try {
+    bakron_opts o;
+    bakron_default_opts(&o);
+    if (opts_in) o = *opts_in;
+    if (!valid_opts(o)) return BAKRON_ERR_INVALID_ARG;
+    if (!W || !UA || !UB || !scale || !V || !codes || !ws) return BAKRON_ERR_INVALID_ARG;
+    if (!sizes_ok(m, n) || qmin > qmax) return BAKRON_ERR_INVALID_ARG;
+    if (guide_codes && !(guide_tol >= 0.f)) return BAKRON_ERR_INVALID_ARG;
+    const ALayout L = antidiag_layout(m, n);
+    if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* base = (char*)ws;
+    DevStatus* st = (DevStatus*)(base + L.status);
+    TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+    TRY_CUDA(launch_check_finite(scale, m, st, s));
+    TRY_CUDA(cudaMemcpyAsync(base + L.wt, W, sizeof(float) * m * n, cudaMemcpyDeviceToDevice, s));
+    AntidiagArgs a{};
+    a.wt = (float*)(base + L.wt);
+    a.UA = UA; a.UB = UB; a.scale = scale;
+    a.ebuf = (float*)(base + L.ebuf);
+    a.V = V; a.codes = codes; a.preround = preround;
+    a.guide = guide_codes; a.guide_tol = guide_tol;
+    a.m = m; a.n = n; a.qmin = qmin; a.qmax = qmax;
+    a.budget = o.spin_budget_cycles > 0 ? o.spin_budget_cycles : 4000000000LL;
+    a.fault_inject = o.fault_inject;
+    a.st = st;
+    int unsupported = 0;
+    TRY_CUDA(launch_antidiag(a, &unsupported, s));
+    if (unsupported) {
+      TRY_CUDA(cudaStreamSynchronize(s));
+      return BAKRON_ERR_UNSUPPORTED;
+    }
+    DevStatus h{};
+    bakron_status r = finish(s, st, &h);
+    if (overrides) *overrides = (int64_t)h.overrides;
+    return r;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
   }
-  DevStatus h{};
-  bakron_status r = finish(s, st, &h);
-  if (overrides) *overrides = (int64_t)h.overrides;
-  return r;
 }
 
 }  // extern "C"

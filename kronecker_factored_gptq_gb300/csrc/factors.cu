@@ -124,7 +124,7 @@ FLayout factors_layout(int64_t N, int64_t n, int64_t m) {
 }
 
 bool dims_ok(int64_t N, int64_t n, int64_t m) {
-  return N >= 1 && N <= (1 << 24) && n >= 0 && m >= 0 && n <= (1 << 20) && m <= (1 << 20) &&
+  return N >= 1 && N <= (1 << 24) && n >= 0 && m >= 0 && n <= kMaxOrder && m <= kMaxOrder &&
          (n > 0 || m > 0);
 }
 }  // namespace
@@ -135,84 +135,92 @@ using namespace bakron;
 
 extern "C" bakron_status bakron_factors_workspace_size(int64_t N, int64_t n, int64_t m,
                                                        size_t* bytes) {
-  if (!bytes || !dims_ok(N, n, m)) return BAKRON_ERR_INVALID_ARG;
-  *bytes = factors_layout(N, n, m).total;
-  return BAKRON_OK;
+  try {
+    if (!bytes || !dims_ok(N, n, m)) return BAKRON_ERR_INVALID_ARG;
+    *bytes = factors_layout(N, n, m).total;
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
 }
 
 extern "C" bakron_status bakron_factors(const float* X, int64_t N, int64_t n, const float* G,
                                         int64_t m, int mode, float* A, float* B, void* ws,
                                         size_t ws_bytes, void* stream) {
-  if (!dims_ok(N, n, m) || !ws) return BAKRON_ERR_INVALID_ARG;
-  if (mode != BAKRON_FACTORS_KFAC && mode != BAKRON_FACTORS_SHAMPOO) return BAKRON_ERR_INVALID_ARG;
-  const bool wantA = A != nullptr, wantB = B != nullptr;
-  if (!wantA && !wantB) return BAKRON_ERR_INVALID_ARG;
-  // an output needs its own side's samples; Shampoo weights need the other side's
-  if (wantA && (!X || n < 1)) return BAKRON_ERR_INVALID_ARG;
-  if (wantB && (!G || m < 1)) return BAKRON_ERR_INVALID_ARG;
-  if (mode == BAKRON_FACTORS_SHAMPOO && (!X || !G || n < 1 || m < 1)) return BAKRON_ERR_INVALID_ARG;
-  const FLayout L = factors_layout(N, wantA || mode == BAKRON_FACTORS_SHAMPOO ? n : 0,
-                                   wantB || mode == BAKRON_FACTORS_SHAMPOO ? m : 0);
-  if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
-  if (!prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
-  cudaStream_t s = (cudaStream_t)stream;
-  char* base = (char*)ws;
-  DevStatus* st = (DevStatus*)(base + L.status);
-  WorkItem* items = (WorkItem*)(base + L.items);
-  float* sqa = (float*)(base + L.sqa);
-  float* sqg = (float*)(base + L.sqg);
-  float* P = (float*)(base + L.P);
-#define FTRY(x)                                        \
-  do {                                                 \
-    if ((x) != cudaSuccess) return BAKRON_ERR_CUDA;    \
-  } while (0)
-  FTRY(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
-  const bool sh = mode == BAKRON_FACTORS_SHAMPOO;
-  if (sh) {
-    count_launch(2);
-    row_norms_kernel<<<grid_1d(N, 8), 256, 0, s>>>(X, N, n, sqa);
-    FTRY(cudaGetLastError());
-    row_norms_kernel<<<grid_1d(N, 8), 256, 0, s>>>(G, N, m, sqg);
-    FTRY(cudaGetLastError());
+  try {
+    if (!dims_ok(N, n, m) || !ws) return BAKRON_ERR_INVALID_ARG;
+    if (mode != BAKRON_FACTORS_KFAC && mode != BAKRON_FACTORS_SHAMPOO) return BAKRON_ERR_INVALID_ARG;
+    const bool wantA = A != nullptr, wantB = B != nullptr;
+    if (!wantA && !wantB) return BAKRON_ERR_INVALID_ARG;
+    // an output needs its own side's samples; Shampoo weights need the other side's
+    if (wantA && (!X || n < 1)) return BAKRON_ERR_INVALID_ARG;
+    if (wantB && (!G || m < 1)) return BAKRON_ERR_INVALID_ARG;
+    if (mode == BAKRON_FACTORS_SHAMPOO && (!X || !G || n < 1 || m < 1)) return BAKRON_ERR_INVALID_ARG;
+    const FLayout L = factors_layout(N, wantA || mode == BAKRON_FACTORS_SHAMPOO ? n : 0,
+                                     wantB || mode == BAKRON_FACTORS_SHAMPOO ? m : 0);
+    if (ws_bytes < L.total) return BAKRON_ERR_INVALID_ARG;
+    if (!prop_tc_supported()) return BAKRON_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* base = (char*)ws;
+    DevStatus* st = (DevStatus*)(base + L.status);
+    WorkItem* items = (WorkItem*)(base + L.items);
+    float* sqa = (float*)(base + L.sqa);
+    float* sqg = (float*)(base + L.sqg);
+    float* P = (float*)(base + L.P);
+  #define FTRY(x)                                        \
+    do {                                                 \
+      if ((x) != cudaSuccess) return BAKRON_ERR_CUDA;    \
+    } while (0)
+    FTRY(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+    const bool sh = mode == BAKRON_FACTORS_SHAMPOO;
+    if (sh) {
+      count_launch(2);
+      row_norms_kernel<<<grid_1d(N, 8), 256, 0, s>>>(X, N, n, sqa);
+      FTRY(cudaGetLastError());
+      row_norms_kernel<<<grid_1d(N, 8), 256, 0, s>>>(G, N, m, sqg);
+      FTRY(cudaGetLastError());
+    }
+    // lower tiles of the largest factor; a factor of order kp uses the first
+    // kp/T (kp/T + 1)/2 of them (row-major over the lower triangle)
+    const int64_t tiles = L.pp / T;
+    std::vector<WorkItem> lower;
+    lower.reserve((size_t)(tiles * (tiles + 1) / 2));
+    for (int r = 0; r < tiles; ++r)
+      for (int c = 0; c <= r; ++c) lower.push_back(WorkItem{r, c, 0, (int)(L.Np / T)});
+    FTRY(cudaMemcpyAsync(items, lower.data(), sizeof(WorkItem) * lower.size(), cudaMemcpyHostToDevice,
+                         s));
+    for (int side = 0; side < 2; ++side) {
+      const bool want = side == 0 ? wantA : wantB;
+      if (!want) continue;
+      const float* Z = side == 0 ? X : G;
+      const int64_t k = side == 0 ? n : m, kp = pad(k);
+      const float* w = sh ? (side == 0 ? sqg : sqa) : nullptr;
+      float* hi = (float*)(base + (side == 0 ? L.xhi : L.ghi));
+      float* lo = (float*)(base + (side == 0 ? L.xlo : L.glo));
+      count_launch();
+      transpose_scale_split_kernel<<<dim3((unsigned)(L.Np / 32), (unsigned)(kp / 32)), 256, 0, s>>>(
+          Z, N, k, w, hi, lo, L.Np);
+      FTRY(cudaGetLastError());
+      PropArgs q{};
+      q.A_hi = hi; q.A_lo = lo; q.lda = L.Np; q.a_rows = kp;
+      q.B_hi = hi; q.B_lo = lo; q.ldb = L.Np; q.b_rows = kp;
+      q.wt = P; q.ldw = kp;
+      q.items = items; q.n_items = (int)((kp / T) * (kp / T + 1) / 2); q.max_k = (int)(L.Np / T);
+      q.stage = 3;
+      q.alpha = (float)(1.0 / (double)N);
+      q.st = st;
+      FTRY(launch_prop_tc(q, s));
+      count_launch();
+      mirror_crop_kernel<<<grid_1d(k * k, 256), 256, 0, s>>>(P, kp, k, side == 0 ? A : B);
+      FTRY(cudaGetLastError());
+    }
+  #undef FTRY
+    DevStatus h{};
+    if (cudaMemcpyAsync(&h, st, sizeof(DevStatus), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return BAKRON_ERR_CUDA;
+    return (bakron_status)h.status;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
   }
-  // lower tiles of the largest factor; a factor of order kp uses the first
-  // kp/T (kp/T + 1)/2 of them (row-major over the lower triangle)
-  const int64_t tiles = L.pp / T;
-  std::vector<WorkItem> lower;
-  lower.reserve((size_t)(tiles * (tiles + 1) / 2));
-  for (int r = 0; r < tiles; ++r)
-    for (int c = 0; c <= r; ++c) lower.push_back(WorkItem{r, c, 0, (int)(L.Np / T)});
-  FTRY(cudaMemcpyAsync(items, lower.data(), sizeof(WorkItem) * lower.size(), cudaMemcpyHostToDevice,
-                       s));
-  for (int side = 0; side < 2; ++side) {
-    const bool want = side == 0 ? wantA : wantB;
-    if (!want) continue;
-    const float* Z = side == 0 ? X : G;
-    const int64_t k = side == 0 ? n : m, kp = pad(k);
-    const float* w = sh ? (side == 0 ? sqg : sqa) : nullptr;
-    float* hi = (float*)(base + (side == 0 ? L.xhi : L.ghi));
-    float* lo = (float*)(base + (side == 0 ? L.xlo : L.glo));
-    count_launch();
-    transpose_scale_split_kernel<<<dim3((unsigned)(L.Np / 32), (unsigned)(kp / 32)), 256, 0, s>>>(
-        Z, N, k, w, hi, lo, L.Np);
-    FTRY(cudaGetLastError());
-    PropArgs q{};
-    q.A_hi = hi; q.A_lo = lo; q.lda = L.Np; q.a_rows = kp;
-    q.B_hi = hi; q.B_lo = lo; q.ldb = L.Np; q.b_rows = kp;
-    q.wt = P; q.ldw = kp;
-    q.items = items; q.n_items = (int)((kp / T) * (kp / T + 1) / 2); q.max_k = (int)(L.Np / T);
-    q.stage = 3;
-    q.alpha = (float)(1.0 / (double)N);
-    q.st = st;
-    FTRY(launch_prop_tc(q, s));
-    count_launch();
-    mirror_crop_kernel<<<grid_1d(k * k, 256), 256, 0, s>>>(P, kp, k, side == 0 ? A : B);
-    FTRY(cudaGetLastError());
-  }
-#undef FTRY
-  DevStatus h{};
-  if (cudaMemcpyAsync(&h, st, sizeof(DevStatus), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return BAKRON_ERR_CUDA;
-  return (bakron_status)h.status;
 }

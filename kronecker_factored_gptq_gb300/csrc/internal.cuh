@@ -13,6 +13,13 @@ namespace bakron {
 
 constexpr int kTile = 128;          // tile edge T of the solver
 
+// Largest problems the entry points accept: at most kMaxTiles 128-tiles of W
+// (m n <= 2^34 elements, 64 GiB in fp32) and factor orders up to kMaxOrder.
+// The host work lists then stay below a few hundred MB, and no single GPU
+// could hold a larger workspace.
+constexpr int64_t kMaxTiles = int64_t(1) << 20;
+constexpr int64_t kMaxOrder = int64_t(1) << 16;
+
 // Device-side status block, at the start of every workspace.
 struct DevStatus {
   int status;          // bakron_status, first error wins (atomicCAS from 0)

@@ -93,3 +93,20 @@ def test_invalid_arguments_return_before_any_cuda_call(L):
     assert L.bakron_prepare(fake, 4, -1.0, None, 0, 0.0, fake, None, None, None, None, fake,
                             1 << 20, None) == 1
     assert L.bakron_rowscale(fake, 4, 4, 0, fake, None) == 1
+
+
+def test_size_limits(L):
+    """Documented caps: at most 2^20 tiles of W, factor orders up to 65536
+    (the host work lists stay small; no GPU could hold larger workspaces)."""
+    b = ctypes.c_size_t(0)
+    n = ctypes.c_int64(0)
+    assert L.bakron_workspace_size(1 << 20, 128, None, ctypes.byref(b)) == 0   # 8192 x 1 tiles
+    assert L.bakron_workspace_size((1 << 17) + 1, 1 << 17, None, ctypes.byref(b)) == 1   # 1025 x 1024
+    assert L.bakron_workspace_size(1 << 20, 1 << 20, None, ctypes.byref(b)) == 1
+    assert L.bakron_prepare_workspace_size(1 << 12, 0, ctypes.byref(b)) == 0
+    assert L.bakron_prepare_workspace_size((1 << 16) + 1, 0, ctypes.byref(b)) == 1
+    assert L.bakron_prepare_workspace_size(1 << 20, 1 << 20, ctypes.byref(b)) == 1
+    assert L.bakron_factors_workspace_size(100, (1 << 16) + 1, 0, ctypes.byref(b)) == 1
+    assert L.bakron_schedule_export(0, 2048, 1024, None, 0, ctypes.byref(n)) == 1
+    assert L.bakron_schedule_export(2, 513, 1, None, 0, ctypes.byref(n)) == 1
+    assert L.bakron_schedule_export(2, 16, 1, None, 0, ctypes.byref(n)) == 0 and n.value > 0
