@@ -1,8 +1,9 @@
 """Host-side checks of the library's schedules (no GPU): the work lists come
 from the C ABI (bakron_schedule_export), the checks from the method.
 
-Two-sided solve ("BaKron" page, Algorithm 1 and the divide-and-conquer
-discussion of the propagation): the error of tile (I, J) reaches every tile
+Two-sided solve (summary page "FastKron: Efficient Quantization with
+Kronecker-Factored Hessians", the derivation of BaKron-antidiagonal and of the
+divide and conquer over anti-diagonals): the error of tile (I, J) reaches every tile
 (I', J') with I' >= I, J' >= J, through Y[I][J'] = sum_J E[I][J] U_A[J][J']
 (stage 1) and W~[I'][J'] -= sum_I U_B[I][I']^T Y[I][J'] (stage 2).  The
 schedule must apply each (source, target) contribution exactly once, from a
