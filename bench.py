@@ -110,23 +110,32 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-            except ValueError:
-                continue
+        with open(self.path) as f:
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
-        sm = [r[0] for r in rows]
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return summarize_clocks(lines)
+
+
+def summarize_clocks(lines):
+    """Median SM clock under load, the maximum clock, and every throttle
+    reason seen Active, from nvidia-smi CSV lines in ClockSampler.FIELDS
+    order (noheader, nounits); malformed lines are skipped."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+    sm = [r[0] for r in rows]
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows)}
 
 
 # ------------------------------------------------------------------ dist

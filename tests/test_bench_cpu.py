@@ -77,3 +77,41 @@ def test_dist_helpers_gloo_world2():
     assert all(p.exitcode == 0 for p in ps)
     got = dict(q.get(timeout=10) for _ in range(2))
     assert got == {0: 2.0, 1: 2.0}
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_clock_summary():
+    B = _bench_module()
+    lines = ["0, 2070, 2070, 812.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+             "0, 2055, 2070, 1390.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+             "garbage line\n",
+             "0, [N/A], 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active\n",
+             "0, 1800, 2070, 1400.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active\n"]
+    c = B.summarize_clocks(lines)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2055 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert B.summarize_clocks([]) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_traffic_from_profile_checks_the_kernel_source(tmp_path):
+    import hashlib
+    B = _bench_module()
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void k() {}\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    prof = tmp_path / "p.md"
+    prof.write_text("# summary\ntraffic_bytes_per_launch: 1234\nkernel_source_sha256_16: %s\n" % h)
+    assert B.traffic_per_launch(str(src), str(prof)) == 1234.0
+    src.write_text("__global__ void k() { /* changed */ }\n")
+    assert B.traffic_per_launch(str(src), str(prof)) is None          # stale capture
+    assert B.traffic_per_launch(str(tmp_path / "missing.cu"), str(prof)) is None
+    # the committed profile matches the committed kernel
+    assert B.traffic_per_launch("kronecker_factored_gptq_gb300/csrc/prop_tc.cu",
+                                "profiles/prop_tc_kernel_c8192_traffic.md") is not None
