@@ -21,6 +21,11 @@ Birnick & Saab):
   vec order) and BaKron (anti-diagonal parallelism + divide and conquer over
   the anti-diagonal dimension); plus textbook one-sided GPTQ (Hessian A (x) I).
   Theorem 3.2 on the summary page states the four give the same output.
+* ``rowacc``    - the same GPTQ output in the row-accumulator form (every
+  entry pushes its error along its row through U_A and the finished row
+  accumulator down its column through U_B), written in plain C
+  (``rowacc.c``, compiled by ``build_c.py``): m n (m + n) flops, so whole
+  solves at the full workload sizes can be compared.
 * ``hessians``  - K-FAC and one-step Shampoo Kronecker factors of a layer
   Hessian from activation and gradient samples (summary page, section on the
   Hessians).
@@ -44,6 +49,7 @@ from .solvers import (SolveResult, gptq_rows, naive_vec_gptq, antidiag,
 from .checks import (certificate, proxy_loss, cor34_bound, cor34_tight_bound,
                      compare_codes)
 from .hessians import kfac_factors, shampoo_factors
+from .rowacc import rowacc
 
 __all__ = [
     "damp", "rev_cholesky", "update_factor", "prepare", "lower_from_update",
@@ -51,5 +57,5 @@ __all__ = [
     "gptq_rows", "naive_vec_gptq", "antidiag", "recursive_vec", "bakron",
     "bakron_tiled_order_check",
     "certificate", "proxy_loss", "cor34_bound", "cor34_tight_bound",
-    "compare_codes", "SolveResult", "kfac_factors", "shampoo_factors",
+    "compare_codes", "SolveResult", "kfac_factors", "shampoo_factors", "rowacc",
 ]

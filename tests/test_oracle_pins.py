@@ -459,3 +459,82 @@ def test_grid_diagonal_factors_give_grid_rtn():
     UB = np.diag(rng.uniform(0.5, 2.0, 4))
     r = O.bakron(W, UA, UB, g)
     np.testing.assert_array_equal(r.codes, O.quantize_codes(W, g.S, g.qmin, g.qmax, g.Z))
+
+
+# ------------------------- the C row-accumulator solver (oracle/rowacc.c)
+
+@pytest.mark.parametrize("m,n", SHAPES + [(33, 20), (20, 33)])
+def test_rowacc_equals_naive_explicit_hessian(m, n):
+    """Theorem 3.2 for the row-accumulator form: the same codes as GPTQ on
+    vec(W) with the explicit mn x mn Hessian, the same pre-rounding values
+    and errors up to fp64 rounding (a different summation order)."""
+    from oracle.rowacc import rowacc
+    p = problem(m, n, seed=m * 100 + n + 7)
+    ref = O.naive_vec_gptq(p["W"], p["s"], p["qmin"], p["qmax"], A=p["A"], B=p["B"])
+    r = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"])
+    np.testing.assert_array_equal(r.codes, ref.codes)
+    np.testing.assert_allclose(r.preround, ref.preround, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r.E, ref.E, rtol=0, atol=1e-10)
+    np.testing.assert_array_equal(r.V, p["s"].astype(np.float64)[:, None] * r.codes)
+
+
+def test_rowacc_unclamped_and_64x64_match_antidiag():
+    from oracle.rowacc import rowacc
+    p = problem(64, 64, seed=17)
+    ones = np.ones(64, np.float32)
+    for W, s, lo, hi in ((p["W"], p["s"], p["qmin"], p["qmax"]), (10 * p["W"], ones, None, None)):
+        a = O.antidiag(W, p["UA"], p["UB"], s, lo, hi)
+        r = rowacc(W, p["UA"], p["UB"], s, lo, hi)
+        np.testing.assert_array_equal(r.codes, a.codes)
+        np.testing.assert_allclose(r.preround, a.preround, rtol=0, atol=1e-11)
+
+
+def test_rowacc_b_identity_and_diagonal_factors():
+    """B = I reduces to per-row GPTQ; diagonal A and B reduce to rounding to
+    nearest (no entry updates another)."""
+    from oracle.rowacc import rowacc
+    p = problem(7, 12, seed=19)
+    I = np.eye(7)
+    one = O.gptq_rows(p["W"], p["UA"], p["s"], p["qmin"], p["qmax"])
+    r = rowacc(p["W"], p["UA"], I, p["s"], p["qmin"], p["qmax"])
+    np.testing.assert_array_equal(r.codes, one.codes)
+    np.testing.assert_allclose(r.preround, one.preround, rtol=0, atol=1e-14)
+    rng = np.random.default_rng(20)
+    UA = np.diag(rng.uniform(0.5, 2.0, 12))
+    UB = np.diag(rng.uniform(0.5, 2.0, 7))
+    d = rowacc(p["W"], UA, UB, p["s"], -4, 3)
+    np.testing.assert_array_equal(d.codes, O.quantize_codes(p["W"], p["s"][:, None], -4, 3))
+
+
+def test_rowacc_guide_and_transpose_symmetry():
+    """A guide equal to the solver's own codes changes nothing; with a unit
+    grid, (W, A, B) and (W^T, B, A) are the same problem (vec order swaps)."""
+    from oracle.rowacc import rowacc
+    p = problem(9, 14, seed=21)
+    r = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"])
+    g = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], guide=r.codes)
+    np.testing.assert_array_equal(g.codes, r.codes)
+    assert g.overrides == 0
+    W = 40 * p["W"]
+    a = rowacc(W, p["UA"], p["UB"], np.ones(9, np.float32))
+    b = rowacc(W.T.copy(), p["UB"], p["UA"], np.ones(14, np.float32))
+    np.testing.assert_array_equal(a.codes, b.codes.T)
+    np.testing.assert_allclose(a.preround, b.preround.T, rtol=0, atol=1e-12)
+
+
+def test_rowacc_guide_takes_a_planted_near_tie():
+    """An entry placed exactly on a rounding boundary (entry (0, 0), which no
+    update reaches): round half to even takes one side; a guide with the other
+    code is followed there and counted."""
+    from oracle.rowacc import rowacc
+    p = problem(5, 6, seed=22)
+    W = p["W"].copy()
+    W[0, 0] = 0.5 * float(p["s"][0])
+    r = rowacc(W, p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"])
+    assert r.codes[0, 0] == 0.0
+    guide = r.codes.copy()
+    guide[0, 0] = 1.0
+    g = rowacc(W, p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], guide=guide)
+    assert g.codes[0, 0] == 1.0 and g.overrides >= 1
+    ref = O.antidiag(W, p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], guide=guide)
+    np.testing.assert_array_equal(g.codes, ref.codes)
