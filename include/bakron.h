@@ -61,13 +61,16 @@ typedef enum {
  * split. */
 typedef struct {
   double leaf_ms;         /* leaf sweeps (anti-diagonal steps inside tiles) */
-  double prop1_ms;        /* propagation stage 1: Y^T = U_A^T E_P^T */
+  double prop1_ms;        /* propagation stage 1: Y^T = U_A^T E_P^T (off the
+                             critical stream) */
   double prop2_ms;        /* propagation stage 2: W~_Q -= U_B^T Y */
   double other_ms;        /* padding, factor transposition/split */
   double prop_flops;      /* executed propagation flops (both stages) */
   int64_t leaf_launches;
   int64_t prop_launches;  /* launches of the propagation product kernel */
   int64_t other_launches;
+  double near_ms;         /* near products (both stages) between two leaves */
+  int64_t near_launches;
 } bakron_phase_times;
 
 typedef struct {
@@ -111,11 +114,20 @@ int64_t bakron_kernel_launches(void);
  * to size it).  SOLVE / ROWS: M, N in [1, 8192] with M N <= 2^20; PREPARE:
  * M in [1, 512]; anything else is BAKRON_ERR_INVALID_ARG.
  * Layout (every offset counts work items, each item 4 values r, c, k0, k1):
- *   SOLVE / ROWS: n_ops, n_chunks, n_items; n_ops records of 7 values
- *     kind (0 leaf, 1 propagation), D (leaf diagonal or column tile), I0,
- *     ntiles, depth, chunk0, nchunks; n_chunks records of 6 values
- *     dlo, dhi (target range), off1, n1 (stage-1 items), off, n (stage-2
- *     items; ROWS has no stage-1 items); the items.
+ *   SOLVE / ROWS: n_ops, n_chunks, n_items; n_ops records of 7 values, in
+ *     the order the solve issues them:
+ *       SOLVE leaf         0, D (tile anti-diagonal), I0, ntiles, 0, 0, 0
+ *       SOLVE near         2, D, 0, 0, 0, chunk, 1: the products from the
+ *                          left and upper neighbours (diagonal D - 1) into
+ *                          the tiles of D, between leaf D - 1 and leaf D
+ *       SOLVE propagation  1, last source diagonal (it starts after that
+ *                          leaf), s0, s1 (source diagonals [s0, s1)), depth,
+ *                          chunk0, nchunks
+ *       ROWS leaf          0, J (column tile), 0, M, depth, 0, 0
+ *       ROWS propagation   1, 0, 0, 0, depth, chunk0, nchunks;
+ *     n_chunks records of 6 values dlo, dhi (target range), off1, n1
+ *     (stage-1 items), off, n (stage-2 items; ROWS has no stage-1 items);
+ *     the items.
  *   PREPARE: nb, n_items, n_levels; nb records syrk_off, n1, n2 (the
  *     trailing updates of step kb: the urgent tile, n1 lookahead tiles, n2
  *     bulk tiles); per doubling level n_pairs then n_pairs records t_off,
@@ -293,9 +305,11 @@ bakron_status bakron_factors(const float* X, int64_t N, int64_t n, const float* 
  * preround output, but no workspace: the library uses a fixed 16 MiB scratch
  * array of its own on each GPU (held until the process exits), so m and n
  * must be at most 512 (larger sizes return BAKRON_ERR_INVALID_ARG).  The
- * first call on a device resolves that array's address (make it before any
- * stream capture).  All calls on a device share the array: calls that
- * overlap on the GPU race; serialise them. */
+ * first call on a device resolves that array's address, and (like the first
+ * bakron_quantize call on a device) creates the library's solve streams and
+ * the events it reuses from call to call: make it before any stream capture.
+ * No device memory is allocated by this entry point.  All calls on a device
+ * share the array: calls that overlap on the GPU race; serialise them. */
 bakron_status bakron_quantize_noalloc(const float* W, int64_t m, int64_t n,
                                       const float* UA, const float* UB,
                                       const float* scale, int qmin, int qmax,

@@ -35,7 +35,8 @@ class PhaseTimes(ctypes.Structure):
     _fields_ = [("leaf_ms", ctypes.c_double), ("prop1_ms", ctypes.c_double),
                 ("prop2_ms", ctypes.c_double), ("other_ms", ctypes.c_double),
                 ("prop_flops", ctypes.c_double), ("leaf_launches", ctypes.c_int64),
-                ("prop_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64)]
+                ("prop_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64),
+                ("near_ms", ctypes.c_double), ("near_launches", ctypes.c_int64)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -7,25 +7,36 @@
 // second half).  The recursion runs over TILE anti-diagonals D = I + J of
 // 128 x 128 tiles; every tile order with D increasing rounds an entry after
 // all entries to its top-left, which Theorem 3.2 says leaves the result
-// unchanged.  rec(D0, D1) with D1 - D0 == 1 is a leaf (all tiles of D in
-// parallel, one CTA each); otherwise, with Dm = (D0 + D1) / 2:
-//   rec(D0, Dm);
-//   stage 1: for every row tile I with tiles in band P = [D0, Dm):
-//            Y^T[J', I] = sum_{J in P_I, J <= J'} U_A^T[J', J] E[I, J]^T
-//   stage 2: for every tile (I', J') in band Q = [Dm, D1):
-//            W~[I', J'] -= sum_{I <= I'} U_B^T[I', I] Y^T[J', I]^T
-//   rec(Dm, D1).
-// Both stages are dense 128-tile products (the triangular diagonal blocks of
-// the factors carry their zeros), listed as work items built here once per
-// (M, N) and uploaded into the workspace.
+// unchanged.  The error of a tile reaches a later tile in two ways:
 //
-// Lookahead: both stages are split by the target tile anti-diagonal they
-// serve into chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...  The first
-// chunk is what the very next leaf needs and runs on the critical stream;
-// the others run on a side stream while the next leaves proceed, and every
-// leaf waits for the chunks covering its diagonal.  A stage-1 item Y^T[J',I]
-// is first read by targets on diagonal max(Dm, I + J'), so it belongs to the
-// chunk holding that diagonal.
+//  * near products: the tiles of diagonal D - 1 that touch a tile (I, J) of
+//    diagonal D, its left and upper neighbours, reach it through
+//      W~[I, J] -= U_B^T[I, I] (U_A^T[J, J-1] E[I, J-1]^T)^T
+//               +  U_B^T[I, I-1] (U_A^T[J, J] E[I-1, J]^T)^T,
+//    two stage-1 and one stage-2 product per tile, run on the critical
+//    stream between leaf D - 1 and leaf D;
+//  * propagation: every other (source, target) pair is two or more
+//    diagonals apart.  rec(D0, D1) with D1 - D0 >= 2 and Dm = (D0 + D1) / 2
+//    runs rec(D0, Dm), then propagates the sources [max(D0 - 1, 0), Dm - 1)
+//    into the targets [Dm, D1), then rec(Dm, D1).  A pair (s, t) with
+//    t - s >= 2 is propagated by the one node whose split separates s + 1
+//    from t; pairs with t - s = 1 never are (they are the near products).
+//    The propagation's last source is diagonal Dm - 2, so it starts after
+//    leaf Dm - 2 and runs beside leaf Dm - 1: no propagation sits between
+//    two leaves on the critical stream.
+//
+// A propagation is two stages over lists of dense 128-tile products (the
+// triangular diagonal blocks of the factors carry their zeros):
+//   stage 1: for every row tile I with source tiles:
+//            Y^T[J', I] = sum_{J in sources of row I, J <= J'} U_A^T[J', J] E[I, J]^T
+//   stage 2: for every target tile (I', J'):
+//            W~[I', J'] -= sum_{I <= I'} U_B^T[I', I] Y^T[J', I]^T
+// Both stages are split by the target tile anti-diagonal they serve into
+// chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...: the first chunk is what
+// leaf Dm needs and runs on a high-priority stream, the others on a
+// low-priority stream; every leaf waits for the chunks covering its
+// diagonal.  A stage-1 item Y^T[J', I] is first read by targets on diagonal
+// max(Dm, I + J'), so it belongs to the chunk holding that diagonal.
 #include <algorithm>
 #include <climits>
 #include <cstring>
@@ -51,11 +62,17 @@ struct Chunk {
   double flops1, flops;
 };
 
+// Ops in the order the executor issues them: for each diagonal D, the near
+// products into D (D >= 1), leaf D, then the propagation whose last source
+// is D (the node split at D + 2), if there is one.
 struct Op {
-  int kind;                // 0 = leaf, 1 = propagation
-  int D, I0, ntiles;       // leaf
-  int depth;               // recursion depth (selects the Y buffer and side stream)
-  int chunk0, nchunks;     // chunks (the first one is urgent)
+  int kind;                // 0 = leaf, 1 = propagation, 2 = near products
+  int D;                   // leaf / near: the tile anti-diagonal; propagation:
+                           // its last source diagonal (after whose leaf it starts)
+  int I0, ntiles;          // leaf: first row tile and tile count
+  int s0, s1;              // propagation: source diagonals [s0, s1)
+  int depth;               // propagation: recursion depth (Y buffer, streams)
+  int chunk0, nchunks;     // near: one chunk; propagation: its chunks
 };
 
 struct Schedule {
@@ -72,20 +89,24 @@ void sort_items(std::vector<WorkItem>& v, size_t from) {
   });
 }
 
-void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
+// Propagation of the sources [S0, S1) into the targets [T0, T1) (T0 >= S1 + 1).
+Op build_prop(Schedule& s, int S0, int S1, int T0, int T1, int depth) {
   const int M = s.M, N = s.N;
   Op op{};
   op.kind = 1;
+  op.D = S1 - 1;
+  op.s0 = S0;
+  op.s1 = S1;
   op.depth = depth;
   s.max_depth = std::max(s.max_depth, depth);
   op.chunk0 = (int)s.chunks.size();
-  // chunk boundaries over the target band [Dm, D1)
+  // chunk boundaries over the target band [T0, T1)
   std::vector<std::pair<int, int>> bounds;
-  for (int lo = Dm, width = 1; lo < D1;) {
-    const int hi = std::min(D1, lo + width);
+  for (int lo = T0, width = 1; lo < T1;) {
+    const int hi = std::min(T1, lo + width);
     bounds.emplace_back(lo, hi);
     lo = hi;
-    if (lo > Dm + 1) width *= 2;
+    if (lo > T0 + 1) width *= 2;
   }
   auto chunk_of = [&](int d) {
     int c = 0;
@@ -96,13 +117,13 @@ void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
   std::vector<std::vector<WorkItem>> s1(bounds.size());
   std::vector<double> f1(bounds.size(), 0.0);
   for (int I = 0; I < M; ++I) {
-    const int jlo = std::max(D0 - I, 0), jhi = std::min(Dm - I, N);
+    const int jlo = std::max(S0 - I, 0), jhi = std::min(S1 - I, N);
     if (jlo >= jhi) continue;
-    for (int Jp = jlo; Jp < std::min(D1 - I, N); ++Jp) {
-      const int lo = std::max(I, Dm - Jp), hi = std::min(M - 1, D1 - 1 - Jp);
-      if (lo > hi) continue;  // no tile of Q in column Jp at or below row I
+    for (int Jp = jlo; Jp < std::min(T1 - I, N); ++Jp) {
+      const int lo = std::max(I, T0 - Jp), hi = std::min(M - 1, T1 - 1 - Jp);
+      if (lo > hi) continue;  // no target in column Jp at or below row I
       const int k1 = std::min(jhi, Jp + 1);
-      const int c = chunk_of(std::max(Dm, I + Jp));
+      const int c = chunk_of(std::max(T0, I + Jp));
       s1[c].push_back(WorkItem{Jp, I, jlo, k1});
       f1[c] += 2.0 * T * T * T * (k1 - jlo);
     }
@@ -122,8 +143,9 @@ void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
     c.off = (int)s.items.size();
     for (int Ip = 0; Ip < M; ++Ip) {
       for (int Jp = std::max(c.dlo - Ip, 0); Jp < std::min(c.dhi - Ip, N); ++Jp) {
-        const int ilo = std::max(std::max(0, D0 - Jp), D0 - N + 1);
-        const int ihi = std::min(Ip, Dm - 1);
+        // source rows I <= Ip whose Y^T[Jp, I] is not empty
+        const int ilo = std::max(std::max(0, S0 - Jp), S0 - N + 1);
+        const int ihi = std::min(std::min(Ip, S1 - 1), M - 1);
         if (ilo > ihi) continue;
         s.items.push_back(WorkItem{Ip, Jp, ilo, ihi + 1});
         c.flops += 2.0 * T * T * T * (ihi + 1 - ilo);
@@ -135,35 +157,87 @@ void build_prop(Schedule& s, int D0, int Dm, int D1, int depth) {
     s.chunks.push_back(c);
   }
   op.nchunks = (int)s.chunks.size() - op.chunk0;
-  s.ops.push_back(op);
+  return op;
 }
 
-void build_rec(Schedule& s, int D0, int D1, int depth) {
-  if (D1 - D0 <= 1) {
-    Op op{};
-    op.kind = 0;
-    op.D = D0;
-    op.I0 = std::max(0, D0 - s.N + 1);
-    op.ntiles = std::min(D0, s.M - 1) - op.I0 + 1;
-    s.ops.push_back(op);
-    return;
+// Near products into the tiles of diagonal D from their left and upper
+// neighbours (diagonal D - 1): stage-1 items write Y^T[J, I] (from the left
+// neighbour, K = tile column J - 1) and Y^T[J, I - 1] (from the upper
+// neighbour, K = tile column J, the triangular diagonal block of U_A); the
+// stage-2 item of (I, J) sums U_B^T[I, I''] Y^T[J, I''] over I'' in
+// {I - 1, I}, whichever exist.
+Op build_near(Schedule& s, int D) {
+  const int M = s.M, N = s.N;
+  Op op{};
+  op.kind = 2;
+  op.D = D;
+  op.chunk0 = (int)s.chunks.size();
+  op.nchunks = 1;
+  const int I0 = std::max(0, D - N + 1), I1 = std::min(D, M - 1);
+  Chunk c{};
+  c.dlo = D;
+  c.dhi = D + 1;
+  c.off1 = (int)s.items.size();
+  for (int I = I0; I <= I1; ++I) {
+    const int J = D - I;
+    if (J >= 1) s.items.push_back(WorkItem{J, I, J - 1, J});
+    if (I >= 1) s.items.push_back(WorkItem{J, I - 1, J, J + 1});
   }
-  const int Dm = (D0 + D1) / 2;
-  build_rec(s, D0, Dm, depth + 1);
-  build_prop(s, D0, Dm, D1, depth);
-  build_rec(s, Dm, D1, depth + 1);
+  c.n1 = (int)s.items.size() - c.off1;
+  c.maxk1 = c.n1 > 0 ? 1 : 0;
+  c.flops1 = 2.0 * T * T * T * c.n1;
+  c.off = (int)s.items.size();
+  for (int I = I0; I <= I1; ++I) {
+    const int J = D - I;
+    const int k0 = I >= 1 ? I - 1 : I, k1 = J >= 1 ? I + 1 : I;
+    if (k1 <= k0) continue;
+    s.items.push_back(WorkItem{I, J, k0, k1});
+    c.flops += 2.0 * T * T * T * (k1 - k0);
+    c.maxk = std::max(c.maxk, k1 - k0);
+  }
+  c.n = (int)s.items.size() - c.off;
+  s.chunks.push_back(c);
+  return op;
 }
 
-// Deferred propagation chunks that the critical stream has not yet waited
-// for, each with the target range [dlo, dhi) it updates (tile anti-diagonals,
-// or column tiles on the one-sided path).  A leaf waits for those covering
-// its diagonal; a propagation waits, before its first chunk, for those
-// covering any of its targets.  Both add into the same W~ tiles from
-// different streams (atomic adds, so overlapping was correct), and waiting
-// fixes the order of the adds, so the fp32 result is the same on every run.
-// (The propagation's own deferred chunks follow its first chunk through an
-// event, so they are ordered after the wait too.)  Each event is waited for
-// once; mostly it has completed long before.
+// The propagations of the recursion, each filed under its last source
+// diagonal (at most one per diagonal: every split point is distinct).
+void build_rec(Schedule& s, int D0, int D1, int depth, std::vector<Op>& prop_after) {
+  if (D1 - D0 <= 1) return;
+  const int Dm = (D0 + D1) / 2;
+  build_rec(s, D0, Dm, depth + 1, prop_after);
+  const int S0 = std::max(D0 - 1, 0), S1 = Dm - 1;
+  if (S1 > S0) prop_after[S1 - 1] = build_prop(s, S0, S1, Dm, D1, depth);
+  build_rec(s, Dm, D1, depth + 1, prop_after);
+}
+
+void build_schedule(Schedule& s) {
+  const int ND = s.M + s.N - 1;
+  std::vector<Op> prop_after(ND, Op{-1});
+  build_rec(s, 0, ND, 0, prop_after);
+  for (int D = 0; D < ND; ++D) {
+    if (D >= 1) s.ops.push_back(build_near(s, D));
+    Op leaf{};
+    leaf.kind = 0;
+    leaf.D = D;
+    leaf.I0 = std::max(0, D - s.N + 1);
+    leaf.ntiles = std::min(D, s.M - 1) - leaf.I0 + 1;
+    s.ops.push_back(leaf);
+    if (prop_after[D].kind == 1) s.ops.push_back(prop_after[D]);
+  }
+}
+
+// Propagation chunks whose updates of W~ a later writer of the same tiles
+// must follow, each with the target range [dlo, dhi) it updates (tile
+// anti-diagonals, or column tiles on the one-sided path).  Before a stream
+// updates the diagonals [lo, hi) (a chunk's stage 2, the near products, a
+// leaf) it waits for every listed chunk that overlaps them, so each W~ tile
+// receives its updates in one fixed order and the fp32 result is the same on
+// every run.  A chunk whose whole range lies inside [lo, hi) is then dropped:
+// a writer after it overlaps [lo, hi) as well and follows it through the new
+// writer's own event (or through the stream, for the leaf and the near
+// products, which are the last writers of their diagonal).  A chunk that
+// reaches past [lo, hi) stays listed for the writers of its other diagonals.
 struct PendingChunks {
   struct Item {
     cudaEvent_t ev;
@@ -174,12 +248,12 @@ struct PendingChunks {
   cudaError_t order_before(cudaStream_t cs, int lo, int hi) {
     size_t w = 0;
     for (size_t i = 0; i < v.size(); ++i) {
-      if (v[i].dlo < hi && v[i].dhi > lo) {
+      const bool overlap = v[i].dlo < hi && v[i].dhi > lo;
+      if (overlap) {
         const cudaError_t e = cudaStreamWaitEvent(cs, v[i].ev, 0);
         if (e != cudaSuccess) return e;
-      } else {
-        v[w++] = v[i];
       }
+      if (!(overlap && v[i].dlo >= lo && v[i].dhi <= hi)) v[w++] = v[i];
     }
     v.resize(w);
     return cudaSuccess;
@@ -196,7 +270,7 @@ const Schedule& get_schedule(int M, int N) {
   Schedule s;
   s.M = M;
   s.N = N;
-  build_rec(s, 0, M + N - 1, 0);
+  build_schedule(s);
   return cache.emplace(key, std::move(s)).first->second;
 }
 
@@ -268,7 +342,8 @@ constexpr int kMaxDepth = 24;
 struct QLayout {
   int64_t M, N, Mp, Np;
   int ndepth;
-  size_t status, sched, scale, zero, wt, ehi, elo, yhi[kMaxDepth], ylo[kMaxDepth], lathi, latlo, lbthi,
+  size_t status, sched, scale, zero, wt, ehi, elo, ynhi, ynlo, yhi[kMaxDepth], ylo[kMaxDepth], lathi,
+      latlo, lbthi,
       lbtlo, total;
 };
 
@@ -294,6 +369,9 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   L.wt = take(f * L.Mp * L.Np);
   L.ehi = take(f * L.Mp * L.Np);
   L.elo = take(f * L.Mp * L.Np);
+  // the near products' Y^T pair (critical stream only)
+  L.ynhi = take(f * L.Np * L.Mp);
+  L.ynlo = take(f * L.Np * L.Mp);
   // one Y^T pair per recursion depth: a propagation's deferred chunks may
   // still be reading its Y^T while deeper propagations write theirs
   for (int d = 0; d < L.ndepth; ++d) {
@@ -410,11 +488,14 @@ cudaError_t prep_events(PrepStreams* ps, size_t n) {
 }
 
 // Streams of the solve, per device, created once: a high-priority critical
-// stream (leaves, stage 1, urgent stage-2 chunks) and one default-priority
-// side stream per recursion depth (deferred stage-2 chunks), plus a pool of
-// reusable events.  Calls are synchronous, so the pool is reused per call.
+// stream (leaves, near products; the one-sided path's urgent chunks), per
+// recursion depth an urgent stream (the first chunk of a propagation, what
+// the next leaves wait for) just below it in priority and a low-priority side
+// stream (the other chunks), plus a pool of reusable events.  Calls are
+// synchronous, so the pool is reused per call.
 struct SolveStreams {
   cudaStream_t crit = nullptr;
+  cudaStream_t urg[kMaxDepth] = {};
   cudaStream_t side[kMaxDepth] = {};
   std::vector<cudaEvent_t> events;
   std::mutex mu;
@@ -436,13 +517,42 @@ cudaError_t solve_streams(SolveStreams** out, int slot = 0) {
   if (!ss.crit) {
     int lo = 0, hi = 0;
     if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithPriority(&ss.crit, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
-    for (int d = 0; d < kMaxDepth; ++d)
-      if ((e = cudaStreamCreateWithPriority(&ss.side[d], cudaStreamNonBlocking, lo)) != cudaSuccess)
-        return e;
+    // greater priority = smaller number; urgent chunks one step below the
+    // critical stream when the device has the levels
+    const int urg = hi < lo ? hi + 1 : hi;
+    cudaStream_t c = nullptr, u[kMaxDepth] = {}, sd[kMaxDepth] = {};
+    e = cudaStreamCreateWithPriority(&c, cudaStreamNonBlocking, hi);
+    for (int d = 0; d < kMaxDepth && e == cudaSuccess; ++d) {
+      e = cudaStreamCreateWithPriority(&u[d], cudaStreamNonBlocking, urg);
+      if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&sd[d], cudaStreamNonBlocking, lo);
+    }
+    if (e != cudaSuccess) {
+      if (c) cudaStreamDestroy(c);
+      for (int d = 0; d < kMaxDepth; ++d) {
+        if (u[d]) cudaStreamDestroy(u[d]);
+        if (sd[d]) cudaStreamDestroy(sd[d]);
+      }
+      return e;
+    }
+    for (int d = 0; d < kMaxDepth; ++d) {
+      ss.urg[d] = u[d];
+      ss.side[d] = sd[d];
+    }
+    ss.crit = c;
   }
   *out = &ss;
   return cudaSuccess;
+}
+
+// After a failed enqueue: wait for whatever the call already queued on its
+// stream set, so nothing of it still reads or writes the caller's memory or
+// the workspace when the error is returned.
+void drain_solve_streams(SolveStreams* ss) {
+  cudaStreamSynchronize(ss->crit);
+  for (int d = 0; d < kMaxDepth; ++d) {
+    cudaStreamSynchronize(ss->urg[d]);
+    cudaStreamSynchronize(ss->side[d]);
+  }
 }
 
 cudaError_t pool_event(SolveStreams* ss, size_t idx, cudaEvent_t* ev) {
@@ -462,6 +572,17 @@ cudaError_t pool_event(SolveStreams* ss, size_t idx, cudaEvent_t* ev) {
     if (e_ != cudaSuccess) return BAKRON_ERR_CUDA;         \
   } while (0)
 
+// After work was forked onto a solve stream set `ss`: on failure, wait for
+// what is already queued there before returning the error.
+#define TRY_SOLVE(x)                                       \
+  do {                                                     \
+    cudaError_t e_ = (x);                                  \
+    if (e_ != cudaSuccess) {                               \
+      drain_solve_streams(ss);                             \
+      return BAKRON_ERR_CUDA;                              \
+    }                                                      \
+  } while (0)
+
 bakron_status finish(cudaStream_t s, const DevStatus* dst, DevStatus* host) {
   TRY_CUDA(cudaMemcpyAsync(host, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
   TRY_CUDA(cudaStreamSynchronize(s));
@@ -474,7 +595,8 @@ bool valid_opts(const bakron_opts& o) {
          (o.fault_inject == 0 || o.fault_inject == 1);
 }
 
-// Per-launch CUDA events for bakron_opts.times.
+// Per-launch CUDA events for bakron_opts.times: a pair around a launch on
+// the stream it is enqueued on.
 struct PhaseTimer {
   bakron_phase_times* out;
   cudaStream_t s;
@@ -486,18 +608,18 @@ struct PhaseTimer {
       cudaEventDestroy(r.second.second);
     }
   }
-  cudaEvent_t begin() {
+  cudaEvent_t begin(cudaStream_t on = nullptr) {
     if (!out) return nullptr;
     cudaEvent_t a;
     if (cudaEventCreate(&a) != cudaSuccess) return nullptr;
-    cudaEventRecord(a, s);
+    cudaEventRecord(a, on ? on : s);
     return a;
   }
-  void end(int cat, cudaEvent_t a) {
+  void end(int cat, cudaEvent_t a, cudaStream_t on = nullptr) {
     if (!out || !a) return;
     cudaEvent_t b;
     if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return; }
-    cudaEventRecord(b, s);
+    cudaEventRecord(b, on ? on : s);
     rec.push_back({cat, {a, b}});
   }
   void adopt(PhaseTimer& other) {
@@ -513,6 +635,7 @@ struct PhaseTimer {
         case 0: out->leaf_ms += ms; out->leaf_launches++; break;
         case 1: out->prop1_ms += ms; out->prop_launches++; break;
         case 2: out->prop2_ms += ms; out->prop_launches++; break;
+        case 4: out->near_ms += ms; out->near_launches++; break;
         default: out->other_ms += ms; out->other_launches++; break;
       }
     }
@@ -570,20 +693,20 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   cudaStream_t cs = ss->crit;
   {
     cudaEvent_t ev;
-    TRY_CUDA(next_event(&ev));
-    TRY_CUDA(cudaEventRecord(ev, s));
-    TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+    TRY_SOLVE(next_event(&ev));
+    TRY_SOLVE(cudaEventRecord(ev, s));
+    TRY_SOLVE(cudaStreamWaitEvent(cs, ev, 0));
   }
-  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
-  TRY_CUDA(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
+  TRY_SOLVE(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
+  TRY_SOLVE(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
-    TRY_CUDA(launch_check_finite(gr.scale, m * gr.ng, st, cs));
-    TRY_CUDA(launch_check_zero(gr.zero, m * gr.ng, qmin, qmax, st, cs));
-    TRY_CUDA(launch_pad_grid(gr.scale, gr.zero, m, gr.ng, sp, zp, L.Mp, cs));
-    TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
-    TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
+    TRY_SOLVE(launch_check_finite(gr.scale, m * gr.ng, st, cs));
+    TRY_SOLVE(launch_check_zero(gr.zero, m * gr.ng, qmin, qmax, st, cs));
+    TRY_SOLVE(launch_pad_grid(gr.scale, gr.zero, m, gr.ng, sp, zp, L.Mp, cs));
+    TRY_SOLVE(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
+    TRY_SOLVE(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
     pt.end(3, ev);
   }
   LeafArgs la{};
@@ -601,12 +724,12 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   PendingChunks pending;
   for (const RowsOp& op : sch.ops) {
     if (op.kind == 0) {
-      TRY_CUDA(pending.order_before(cs, op.J, op.J + 1));
+      TRY_SOLVE(pending.order_before(cs, op.J, op.J + 1));
       la.D = op.J;
       la.I0 = 0;
       la.pdl = op.J > 0;   // the first leaf reads the factor the kernel before it wrote
       cudaEvent_t ev = pt.begin();
-      TRY_CUDA(launch_rows_leaf(la, (int)L.M, cs));
+      TRY_SOLVE(launch_rows_leaf(la, (int)L.M, cs));
       pt.end(0, ev);
       continue;
     }
@@ -617,7 +740,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     p2.stage = 2;
     p2.st = st;
     if (op.nchunks > 0)
-      TRY_CUDA(pending.order_before(cs, sch.chunks[op.chunk0].dlo,
+      TRY_SOLVE(pending.order_before(cs, sch.chunks[op.chunk0].dlo,
                                     sch.chunks[op.chunk0 + op.nchunks - 1].dhi));
     for (int c = 0; c < op.nchunks; ++c) {
       const Chunk& ch = sch.chunks[op.chunk0 + c];
@@ -627,36 +750,36 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
       if (c == 1) {
         // the deferred chunks start once the leaves they read have finished
         cudaEvent_t ev;
-        TRY_CUDA(next_event(&ev));
-        TRY_CUDA(cudaEventRecord(ev, cs));
-        TRY_CUDA(cudaStreamWaitEvent(cstr, ev, 0));
+        TRY_SOLVE(next_event(&ev));
+        TRY_SOLVE(cudaEventRecord(ev, cs));
+        TRY_SOLVE(cudaStreamWaitEvent(cstr, ev, 0));
       }
       PhaseTimer side_pt(o.times, cstr);
       PhaseTimer* tm = urgent ? &pt : &side_pt;
       p2.items = items + ch.off; p2.n_items = ch.n; p2.max_k = ch.maxk;
       p2.pdl = urgent;
       cudaEvent_t ev = tm->begin();
-      TRY_CUDA(o.use_3xtf32 ? launch_prop_tc(p2, cstr) : launch_prop_simt(p2, cstr));
+      TRY_SOLVE(o.use_3xtf32 ? launch_prop_tc(p2, cstr) : launch_prop_simt(p2, cstr));
       tm->end(2, ev);
       if (!urgent) {
         pt.adopt(side_pt);
         cudaEvent_t done;
-        TRY_CUDA(next_event(&done));
-        TRY_CUDA(cudaEventRecord(done, cstr));
+        TRY_SOLVE(next_event(&done));
+        TRY_SOLVE(cudaEventRecord(done, cstr));
         pending.add(done, ch.dlo, ch.dhi);
       }
     }
   }
   {
     cudaEvent_t ev;
-    TRY_CUDA(next_event(&ev));
-    TRY_CUDA(cudaEventRecord(ev, cs));
+    TRY_SOLVE(next_event(&ev));
+    TRY_SOLVE(cudaEventRecord(ev, cs));
     if (bctx) {
       bctx->done = ev;
       bctx->st = st;
       return BAKRON_OK;
     }
-    TRY_CUDA(cudaStreamWaitEvent(s, ev, 0));
+    TRY_SOLVE(cudaStreamWaitEvent(s, ev, 0));
   }
   DevStatus h{};
   bakron_status r = finish(s, st, &h);
@@ -696,7 +819,7 @@ const char* bakron_status_string(int st) {
   }
 }
 
-int bakron_version(void) { return 10400; }
+int bakron_version(void) { return 20000; }
 
 int64_t bakron_kernel_launches(void) { return (int64_t)bakron::launches_so_far(); }
 
@@ -732,9 +855,21 @@ bakron_status bakron_schedule_export(int kind, int64_t M, int64_t N, int32_t* ou
       v.push_back((int32_t)s.chunks.size());
       v.push_back((int32_t)s.items.size());
       for (const Op& op : s.ops) {
-        const int32_t rec[7] = {op.kind, op.kind == 0 ? op.D : 0, op.kind == 0 ? op.I0 : 0,
-                                op.kind == 0 ? op.ntiles : 0, op.kind == 1 ? op.depth : 0,
-                                op.kind == 1 ? op.chunk0 : 0, op.kind == 1 ? op.nchunks : 0};
+        // leaf: (0, D, I0, ntiles, 0, 0, 0); near: (2, D, 0, 0, 0, chunk, 1);
+        // propagation: (1, last source, s0, s1, depth, chunk0, nchunks)
+        int32_t rec[7] = {op.kind, op.D, 0, 0, 0, 0, 0};
+        if (op.kind == 0) {
+          rec[2] = op.I0;
+          rec[3] = op.ntiles;
+        } else {
+          if (op.kind == 1) {
+            rec[2] = op.s0;
+            rec[3] = op.s1;
+            rec[4] = op.depth;
+          }
+          rec[5] = op.chunk0;
+          rec[6] = op.nchunks;
+        }
         v.insert(v.end(), rec, rec + 7);
       }
       chunks(s.chunks);
@@ -949,21 +1084,21 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   cudaStream_t cs = ss->crit;
   {
     cudaEvent_t ev;
-    TRY_CUDA(next_event(&ev));
-    TRY_CUDA(cudaEventRecord(ev, s));
-    TRY_CUDA(cudaStreamWaitEvent(cs, ev, 0));
+    TRY_SOLVE(next_event(&ev));
+    TRY_SOLVE(cudaEventRecord(ev, s));
+    TRY_SOLVE(cudaStreamWaitEvent(cs, ev, 0));
   }
-  TRY_CUDA(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
-  TRY_CUDA(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
+  TRY_SOLVE(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
+  TRY_SOLVE(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
-    TRY_CUDA(launch_check_finite(gr.scale, m * gr.ng, st, cs));
-    TRY_CUDA(launch_check_zero(gr.zero, m * gr.ng, qmin, qmax, st, cs));
-    TRY_CUDA(launch_pad_grid(gr.scale, gr.zero, m, gr.ng, sp, zp, L.Mp, cs));
-    TRY_CUDA(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
-    TRY_CUDA(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
-    TRY_CUDA(launch_transpose_split(UB, m, lbthi, lbtlo, L.Mp, cs));
+    TRY_SOLVE(launch_check_finite(gr.scale, m * gr.ng, st, cs));
+    TRY_SOLVE(launch_check_zero(gr.zero, m * gr.ng, qmin, qmax, st, cs));
+    TRY_SOLVE(launch_pad_grid(gr.scale, gr.zero, m, gr.ng, sp, zp, L.Mp, cs));
+    TRY_SOLVE(launch_pad_matrix(W, m, n, wt, L.Mp, L.Np, cs));
+    TRY_SOLVE(launch_transpose_split(UA, n, lathi, latlo, L.Np, cs));
+    TRY_SOLVE(launch_transpose_split(UB, m, lbthi, lbtlo, L.Mp, cs));
     pt.end(3, ev);
   }
   LeafArgs la{};
@@ -979,88 +1114,131 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   la.V = V; la.codes = codes; la.preround = preround;
   la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
   la.st = st;
+  // stage 1: Y^T = U_A^T E^T into the given buffer; stage 2: W~ -= U_B^T Y
+  auto stage1 = [&](float* yh, float* yl) {
+    PropArgs p{};
+    p.A_hi = lathi; p.A_lo = latlo; p.lda = L.Np; p.a_rows = L.Np;
+    p.B_hi = ehi; p.B_lo = elo; p.ldb = L.Np; p.b_rows = L.Mp;
+    p.out_hi = yh; p.out_lo = yl; p.ldo = L.Mp;
+    p.stage = 1;
+    p.st = st;
+    return p;
+  };
+  auto stage2 = [&](float* yh, float* yl) {
+    PropArgs p{};
+    p.A_hi = lbthi; p.A_lo = lbtlo; p.lda = L.Mp; p.a_rows = L.Mp;
+    p.B_hi = yh; p.B_lo = yl; p.ldb = L.Mp; p.b_rows = L.Np;
+    p.wt = wt; p.ldw = L.Np;
+    p.stage = 2;
+    p.st = st;
+    return p;
+  };
+  auto launch = [&](PropArgs pa, int off, int nit, int maxk, cudaStream_t str) {
+    pa.items = items + off; pa.n_items = nit; pa.max_k = maxk;
+    pa.pdl = str == cs;
+    return o.use_3xtf32 ? launch_prop_tc(pa, str) : launch_prop_simt(pa, str);
+  };
   PendingChunks pending;
-  for (const Op& op : sch.ops) {
-    if (op.kind == 0) {
-      TRY_CUDA(pending.order_before(cs, op.D, op.D + 1));
-      la.D = op.D;
-      la.I0 = op.I0;
-      // the first leaf reads the factors the kernel directly before it wrote;
-      // a leaf also waiting on deferred chunks (events) still waits for them
-      // in full, the relaxation covers only the previous kernel on this stream
-      la.pdl = op.D > 0;
-      cudaEvent_t ev = pt.begin();
-      TRY_CUDA(launch_leaf(la, op.ntiles, cs));
-      pt.end(0, ev);
-      continue;
-    }
-    float* yhi = (float*)(base + L.yhi[op.depth]);
-    float* ylo = (float*)(base + L.ylo[op.depth]);
-    PropArgs p1{};
-    p1.A_hi = lathi; p1.A_lo = latlo; p1.lda = L.Np; p1.a_rows = L.Np;
-    p1.B_hi = ehi; p1.B_lo = elo; p1.ldb = L.Np; p1.b_rows = L.Mp;
-    p1.out_hi = yhi; p1.out_lo = ylo; p1.ldo = L.Mp;
-    p1.stage = 1;
-    p1.st = st;
-    PropArgs p2{};
-    p2.A_hi = lbthi; p2.A_lo = lbtlo; p2.lda = L.Mp; p2.a_rows = L.Mp;
-    p2.B_hi = yhi; p2.B_lo = ylo; p2.ldb = L.Mp; p2.b_rows = L.Np;
-    p2.wt = wt; p2.ldw = L.Np;
-    p2.stage = 2;
-    p2.st = st;
-    auto launch = [&](PropArgs& pa, int off, int nit, int maxk, cudaStream_t str) {
-      pa.items = items + off; pa.n_items = nit; pa.max_k = maxk;
-      pa.pdl = str == cs;
-      return o.use_3xtf32 ? launch_prop_tc(pa, str) : launch_prop_simt(pa, str);
-    };
-    if (op.nchunks > 0)
-      TRY_CUDA(pending.order_before(cs, sch.chunks[op.chunk0].dlo,
-                                    sch.chunks[op.chunk0 + op.nchunks - 1].dhi));
-    cudaEvent_t ev_s1 = nullptr;
-    for (int c = 0; c < op.nchunks; ++c) {
-      const Chunk& ch = sch.chunks[op.chunk0 + c];
-      if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
-      const bool urgent = c == 0;
-      cudaStream_t cstr = urgent ? cs : ss->side[op.depth];
-      if (c == 1) TRY_CUDA(cudaStreamWaitEvent(cstr, ev_s1, 0));
-      PhaseTimer side_pt(o.times, cstr);
-      PhaseTimer* tm = urgent ? &pt : &side_pt;
-      if (ch.n1 > 0) {
-        cudaEvent_t ev = tm->begin();
-        TRY_CUDA(launch(p1, ch.off1, ch.n1, ch.maxk1, cstr));
-        tm->end(1, ev);
+  cudaEvent_t ev_leaf = nullptr;   // recorded after the leaf a propagation follows
+  auto enqueue = [&]() -> cudaError_t {
+    cudaError_t e;
+    for (const Op& op : sch.ops) {
+      if (op.kind == 2) {
+        // near products into diagonal op.D, after every deferred chunk that
+        // updates its tiles (a fixed order of the W~ updates)
+        const Chunk& ch = sch.chunks[op.chunk0];
+        if ((e = pending.order_before(cs, op.D, op.D + 1)) != cudaSuccess) return e;
+        if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
+        float* ynh = (float*)(base + L.ynhi);
+        float* ynl = (float*)(base + L.ynlo);
+        if (ch.n1 > 0) {
+          cudaEvent_t ev = pt.begin();
+          if ((e = launch(stage1(ynh, ynl), ch.off1, ch.n1, ch.maxk1, cs)) != cudaSuccess) return e;
+          pt.end(4, ev);
+        }
+        if (ch.n > 0) {
+          cudaEvent_t ev = pt.begin();
+          if ((e = launch(stage2(ynh, ynl), ch.off, ch.n, ch.maxk, cs)) != cudaSuccess) return e;
+          pt.end(4, ev);
+        }
+        continue;
       }
-      if (urgent && op.nchunks > 1) {
-        // the deferred chunks read the urgent stage-1 tiles too
-        TRY_CUDA(next_event(&ev_s1));
-        TRY_CUDA(cudaEventRecord(ev_s1, cs));
+      if (op.kind == 0) {
+        if ((e = pending.order_before(cs, op.D, op.D + 1)) != cudaSuccess) return e;
+        la.D = op.D;
+        la.I0 = op.I0;
+        // the first leaf reads the factors the kernel directly before it
+        // wrote; a leaf also waiting on deferred chunks (events) still waits
+        // for them in full, the relaxation covers only the previous kernel on
+        // this stream
+        la.pdl = op.D > 0;
+        cudaEvent_t ev = pt.begin();
+        if ((e = launch_leaf(la, op.ntiles, cs)) != cudaSuccess) return e;
+        pt.end(0, ev);
+        if ((e = next_event(&ev_leaf)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(ev_leaf, cs)) != cudaSuccess) return e;
+        continue;
       }
-      if (ch.n > 0) {
-        cudaEvent_t ev = tm->begin();
-        TRY_CUDA(launch(p2, ch.off, ch.n, ch.maxk, cstr));
-        tm->end(2, ev);
-      }
-      if (!urgent) {
-        pt.adopt(side_pt);
+      // propagation: starts after the leaf of its last source diagonal (the
+      // op directly before it); its first chunk on the depth's urgent
+      // stream, the others on the depth's side stream after the first
+      // chunk's stage 1 (they read its Y^T tiles too)
+      float* yhi = (float*)(base + L.yhi[op.depth]);
+      float* ylo = (float*)(base + L.ylo[op.depth]);
+      cudaStream_t us = ss->urg[op.depth], ds = ss->side[op.depth];
+      if ((e = cudaStreamWaitEvent(us, ev_leaf, 0)) != cudaSuccess) return e;
+      cudaEvent_t ev_s1 = nullptr;
+      for (int c = 0; c < op.nchunks; ++c) {
+        const Chunk& ch = sch.chunks[op.chunk0 + c];
+        if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
+        cudaStream_t cstr = c == 0 ? us : ds;
+        if (c == 1 && (e = cudaStreamWaitEvent(ds, ev_s1, 0)) != cudaSuccess) return e;
+        if (ch.n1 > 0) {
+          cudaEvent_t ev = pt.begin(cstr);
+          if ((e = launch(stage1(yhi, ylo), ch.off1, ch.n1, ch.maxk1, cstr)) != cudaSuccess) return e;
+          pt.end(1, ev, cstr);
+        }
+        if (c == 0 && op.nchunks > 1) {
+          if ((e = next_event(&ev_s1)) != cudaSuccess) return e;
+          if ((e = cudaEventRecord(ev_s1, us)) != cudaSuccess) return e;
+        }
+        if (ch.n > 0) {
+          // after the earlier updates of the same W~ tiles (fixed order)
+          if ((e = pending.order_before(cstr, ch.dlo, ch.dhi)) != cudaSuccess) return e;
+          cudaEvent_t ev = pt.begin(cstr);
+          if ((e = launch(stage2(yhi, ylo), ch.off, ch.n, ch.maxk, cstr)) != cudaSuccess) return e;
+          pt.end(2, ev, cstr);
+        }
         cudaEvent_t done;
-        TRY_CUDA(next_event(&done));
-        TRY_CUDA(cudaEventRecord(done, cstr));
+        if ((e = next_event(&done)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(done, cstr)) != cudaSuccess) return e;
         pending.add(done, ch.dlo, ch.dhi);
       }
     }
+    return cudaSuccess;
+  };
+  if (enqueue() != cudaSuccess) {
+    drain_solve_streams(ss);
+    return BAKRON_ERR_CUDA;
   }
-  // join back onto the caller's stream (every deferred chunk was waited for
-  // by the leaf of its diagonals, so the critical stream is last)
+  // join back onto the caller's stream (every chunk was waited for by the
+  // near products or the leaf of its diagonals, so the critical stream is
+  // last)
   {
     cudaEvent_t ev;
-    TRY_CUDA(next_event(&ev));
-    TRY_CUDA(cudaEventRecord(ev, cs));
+    if (next_event(&ev) != cudaSuccess || cudaEventRecord(ev, cs) != cudaSuccess) {
+      drain_solve_streams(ss);
+      return BAKRON_ERR_CUDA;
+    }
     if (bctx) {
       bctx->done = ev;
       bctx->st = st;
       return BAKRON_OK;
     }
-    TRY_CUDA(cudaStreamWaitEvent(s, ev, 0));
+    if (cudaStreamWaitEvent(s, ev, 0) != cudaSuccess) {
+      drain_solve_streams(ss);
+      return BAKRON_ERR_CUDA;
+    }
   }
   DevStatus h{};
   bakron_status r = finish(s, st, &h);

@@ -87,7 +87,7 @@ __global__ void mirror_crop_kernel(const float* __restrict__ P, int64_t kp, int6
 
 unsigned grid_1d(int64_t total, int per) {
   int64_t b = (total + per - 1) / per;
-  if (b > 152LL * 16) b = 152LL * 16;
+  if (b > (int64_t)sm_count() * 16) b = (int64_t)sm_count() * 16;
   return (unsigned)(b < 1 ? 1 : b);
 }
 

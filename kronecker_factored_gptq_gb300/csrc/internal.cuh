@@ -133,6 +133,10 @@ void set_no_host_alloc(bool on);
 cudaError_t ensure_smem_limit(const void* kernel, size_t bytes,
                               std::atomic<unsigned long long>& done);
 
+// Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount,
+// read once per device); grid-stride kernels cap their grids at a multiple of it.
+int sm_count();
+
 // Process-wide count of kernel launches made by the library.
 void count_launch(int k = 1);
 long long launches_so_far();

@@ -14,11 +14,28 @@ namespace {
 std::atomic<long long> g_launches{0};
 unsigned grid_for(int64_t total, int threads) {
   int64_t b = (total + threads - 1) / threads;
-  if (b > 152LL * 64) b = 152LL * 64;
+  if (b > (int64_t)sm_count() * 64) b = (int64_t)sm_count() * 64;
   if (b < 1) b = 1;
   return (unsigned)b;
 }
 }  // namespace
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  cached[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
 
 void count_launch(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }

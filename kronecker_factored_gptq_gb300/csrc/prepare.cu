@@ -400,7 +400,7 @@ __global__ void finalize_kernel(const float* __restrict__ G, const float* __rest
 
 unsigned grid_for(int64_t total) {
   int64_t b = (total + 255) / 256;
-  if (b > 152LL * 32) b = 152LL * 32;
+  if (b > (int64_t)sm_count() * 32) b = (int64_t)sm_count() * 32;
   return (unsigned)(b < 1 ? 1 : b);
 }
 }  // namespace

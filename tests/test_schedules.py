@@ -7,18 +7,22 @@ divide and conquer over anti-diagonals): the error of tile (I, J) reaches every 
 (I', J') with I' >= I, J' >= J, through Y[I][J'] = sum_J E[I][J] U_A[J][J']
 (stage 1) and W~[I'][J'] -= sum_I U_B[I][I']^T Y[I][J'] (stage 2).  The
 schedule must apply each (source, target) contribution exactly once, from a
-source whose leaf has run, before the leaf of the target.  One-sided solve
-(B = I): the same over column tiles.  Preparation: the blocked Cholesky's
-trailing updates and the recursive-doubling inverse.
+source whose leaf has run, before the leaf of the target: pairs on
+neighbouring tile diagonals through the near products issued between the two
+leaves, every other pair through a propagation that starts after the leaf of
+its last source.  One-sided solve (B = I): the same over column tiles.
+Preparation: the blocked Cholesky's trailing updates and the
+recursive-doubling inverse.
 
-The stream model mirrors the executor's rules in csrc/api.cu: leaves, the
-first chunk of each propagation and its waits on the critical stream, the
-other chunks on one side stream per recursion depth after the first chunk's
-stage 1, and a list of deferred chunks each waited for once, by the first
-leaf or propagation that touches its targets.  The checks then require every
-update of a W~ tile (so their fp32 order is fixed), every Y tile's writer
-and readers, and every E tile's producer and readers to be ordered by stream
-order and events.
+The stream model mirrors the executor's rules in csrc/api.cu: leaves and near
+products on the critical stream; a propagation's first chunk on its depth's
+urgent stream after the leaf before it, the other chunks on its depth's side
+stream after the first chunk's stage 1; every chunk's stage 2 after the
+chunks enqueued earlier that update any of the same diagonals, and every
+near product and leaf after the chunks that update its diagonal (each event
+waited for once).  The checks then require every update of a W~ tile (so
+their fp32 order is fixed), every Y tile's writer and readers, and every E
+tile's producer and readers to be ordered by stream order and events.
 """
 
 import numpy as np
@@ -87,7 +91,9 @@ class Streams:
 
 def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
     """Builds the stream model and returns (S, accesses) where accesses maps
-    ('W', tile) / ('Y', depth, tile) / ('E', tile) to [(node, 'r'|'w')]."""
+    ('W', tile) / ('Y', buffer, tile) / ('E', tile) to [(node, 'r'|'w')].
+    With wait_at_propagation False, propagation chunks skip the waits for
+    earlier chunks of the same diagonals (the sensitivity check)."""
     S = Streams()
     acc = {}
 
@@ -96,18 +102,39 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
 
     pending = []   # (event node, dlo, dhi)
 
-    def order_before(lo, hi):
+    def order_before(stream, lo, hi):
         keep = []
         for ev, dlo, dhi in pending:
-            if dlo < hi and dhi > lo:
-                S.wait("cs", ev)
-            else:
+            overlap = dlo < hi and dhi > lo
+            if overlap:
+                S.wait(stream, ev)
+            if not (overlap and lo <= dlo and dhi <= hi):
                 keep.append((ev, dlo, dhi))
         pending[:] = keep
 
-    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops:
+    def stage1(stream, buf, its):
+        n = S.node(stream)
+        for Jp, I, k0, k1 in its:
+            touch(("Y", buf, (I, Jp)), n, "w")
+            for J in range(k0, k1):
+                touch(("E", (I, J)), n, "r")
+        return n
+
+    def stage2(stream, buf, its):
+        n = S.node(stream)
+        for Ip, Jp, k0, k1 in its:
+            touch(("W", (Ip, Jp)), n, "w")
+            for I in range(k0, k1):
+                if one_sided:
+                    touch(("E", (Ip, I)), n, "r")
+                else:
+                    touch(("Y", buf, (I, Jp)), n, "r")
+        return n
+
+    ev_leaf = None
+    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops.tolist():
         if kind == 0:
-            order_before(D, D + 1)
+            order_before("cs", D, D + 1)
             n = S.node("cs")
             if one_sided:
                 tiles = [(I, D) for I in range(ntiles)]
@@ -116,34 +143,48 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
             for t in tiles:
                 touch(("W", t), n, "w")   # reads W~, the last of its updates
                 touch(("E", t), n, "w")
+            ev_leaf = S.record("cs")
             continue
-        if wait_at_propagation and nchunks > 0:
-            order_before(chunks[chunk0][0], chunks[chunk0 + nchunks - 1][1])
+        if kind == 2:
+            dlo, dhi, off1, n1, off, nn = chunks[chunk0].tolist()
+            order_before("cs", D, D + 1)
+            if n1 > 0:
+                stage1("cs", "near", items[off1:off1 + n1].tolist())
+            if nn > 0:
+                stage2("cs", "near", items[off:off + nn].tolist())
+            continue
+        if one_sided:
+            # one-sided path: first chunk on the critical stream, waits for the
+            # deferred chunks of the same columns before it
+            if wait_at_propagation and nchunks > 0:
+                order_before("cs", chunks[chunk0][0], chunks[chunk0 + nchunks - 1][1])
+            for c in range(nchunks):
+                dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
+                stream = "cs" if c == 0 else "side%d" % depth
+                if c == 1:
+                    S.wait(stream, S.record("cs"))
+                if nn > 0:
+                    stage2(stream, depth, items[off:off + nn].tolist())
+                if c > 0:
+                    pending.append((S.record(stream), dlo, dhi))
+            continue
+        us, ds = "urg%d" % depth, "side%d" % depth
+        S.wait(us, ev_leaf)
         ev_s1 = None
         for c in range(nchunks):
-            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c]
-            stream = "cs" if c == 0 else "side%d" % depth
+            dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
+            stream = us if c == 0 else ds
             if c == 1:
-                S.wait(stream, ev_s1)
+                S.wait(ds, ev_s1)
             if n1 > 0:
-                s1 = S.node(stream)
-                for Jp, I, k0, k1 in items[off1:off1 + n1]:
-                    touch(("Y", depth, (I, Jp)), s1, "w")
-                    for J in range(k0, k1):
-                        touch(("E", (I, J)), s1, "r")
-            if c == 0:
-                ev_s1 = S.record("cs")
+                stage1(stream, depth, items[off1:off1 + n1].tolist())
+            if c == 0 and nchunks > 1:
+                ev_s1 = S.record(us)
             if nn > 0:
-                s2 = S.node(stream)
-                for Ip, Jp, k0, k1 in items[off:off + nn]:
-                    touch(("W", (Ip, Jp)), s2, "w")
-                    for I in range(k0, k1):
-                        if one_sided:
-                            touch(("E", (Ip, I)), s2, "r")
-                        else:
-                            touch(("Y", depth, (I, Jp)), s2, "r")
-            if c > 0:
-                pending.append((S.record(stream), dlo, dhi))
+                if wait_at_propagation:
+                    order_before(stream, dlo, dhi)
+                stage2(stream, depth, items[off:off + nn].tolist())
+            pending.append((S.record(stream), dlo, dhi))
     return S, acc
 
 
@@ -176,22 +217,33 @@ def ordering_violations(S, acc):
 
 def contributions_solve(ops, chunks, items, M, N):
     """count[Ip, Jp, I, J]: times the error of tile (I, J) reaches (Ip, Jp);
-    also checks each contribution's source leaf precedes the propagation and
-    its target lies in the chunk's target range."""
+    also checks each contribution's source leaf precedes the products that
+    read it and its target lies in the chunk's target range and after them."""
     count = np.zeros((M, N, M, N), dtype=np.int32)
     last_leaf = -1   # leaves run in diagonal order
-    for kind, D, I0, ntiles, depth, chunk0, nchunks in ops.tolist():
+    for kind, D, a2, a3, depth, chunk0, nchunks in ops.tolist():
         if kind == 0:
             assert D == last_leaf + 1
             last_leaf = D
             continue
+        if kind == 2:
+            assert D == last_leaf + 1, "near products run right before their leaf"
+            assert nchunks == 1
+        else:
+            assert D == last_leaf, "a propagation starts right after its last source's leaf"
+            s0, s1 = a2, a3
+            assert s1 == D + 1
         yset = {}
         for c in range(nchunks):
             dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
+            if kind == 2:
+                assert (dlo, dhi) == (D, D + 1)
             for Jp, I, k0, k1 in items[off1:off1 + n1].tolist():
                 assert (I, Jp) not in yset, "Y tile computed twice in one propagation"
                 assert 0 <= k0 < k1 <= Jp + 1
                 assert I + k1 - 1 <= last_leaf, "stage 1 reads an unfinished source"
+                if kind == 1:
+                    assert s0 <= I + k0 and I + k1 - 1 < s1, "source outside the band"
                 yset[(I, Jp)] = (c, k0, k1)
             for Ip, Jp, k0, k1 in items[off:off + nn].tolist():
                 assert dlo <= Ip + Jp < dhi, "stage-2 target outside its chunk's range"
@@ -245,16 +297,42 @@ def test_solve_streams_order_every_tile_access(M, N):
 
 
 def test_solve_streams_without_the_propagation_wait_overlap():
-    """The checker is sensitive: with deferred chunks waited for only by the
-    leaf of their first target, a deeper propagation into the same diagonals
-    can update the same W~ tiles concurrently (seven diagonals suffice).  The
-    stage-2 updates are atomic adds, so that was correct, but the order of the
-    adds, and with it the fp32 rounding of W~, could change from run to run;
-    ordered updates make the solve bit-reproducible."""
+    """The checker is sensitive: without the waits of a propagation chunk for
+    the earlier chunks of the same diagonals, two propagations can update the
+    same W~ tiles concurrently.  The stage-2 updates are atomic adds, so that
+    was correct, but the order of the adds, and with it the fp32 rounding of
+    W~, could change from run to run; ordered updates make the solve
+    bit-reproducible."""
     ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, 4, 4))
     S, acc = model_solve(ops, chunks, items, wait_at_propagation=False)
     bad = ordering_violations(S, acc)
     assert bad and all(b[0][0] == "W" for b in bad)
+
+
+def test_solve_near_products_only_between_neighbours():
+    """Every pair of tiles on neighbouring diagonals goes through the near
+    products and only those; no propagation waits between two leaves on the
+    critical stream."""
+    M, N = 9, 7
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
+    # on the critical stream only near products and leaves alternate
+    crit = [int(k) for k in ops[:, 0] if k != 1]
+    assert crit == [0] + [2, 0] * (M + N - 2)
+    for kind, D, _, _, _, chunk0, nchunks in ops.tolist():
+        if kind != 2:
+            continue
+        dlo, dhi, off1, n1, off, nn = chunks[chunk0].tolist()
+        for Jp, I, k0, k1 in items[off1:off1 + n1].tolist():
+            assert k1 - k0 == 1 and I + k0 == D - 1, "near stage 1 reads diagonal D - 1 only"
+        for Ip, Jp, k0, k1 in items[off:off + nn].tolist():
+            assert Ip + Jp == D
+    # a propagation never reads a source one diagonal before one of its targets
+    for kind, D, s0, s1, depth, chunk0, nchunks in ops.tolist():
+        if kind != 1:
+            continue
+        for c in range(nchunks):
+            dlo = int(chunks[chunk0 + c][0])
+            assert dlo >= s1 + 1
 
 
 @pytest.mark.parametrize("M,N", [(1, 1), (3, 1), (1, 7), (4, 5), (9, 16), (6, 33), (64, 64), (32, 112)])

@@ -16,7 +16,7 @@ import pytest
 import oracle as O
 from kronecker_factored_gptq_gb300 import workloads as WL
 
-from _gpu_helpers import TOL, MAX_FRAC, shared_factors, to_dev
+from _gpu_helpers import check_parity, shared_factors, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +33,11 @@ def _noalloc_via_c_abi(kb, dW, dUA, dUB, ds, qmin, qmax, V, C):
 
 
 def test_noalloc_matches_quantize_on_consecutive_calls():
+    """Both calls run the same launch sequence as bakron_quantize on the same
+    inputs, and the solve is bit-reproducible, so codes and V must be equal
+    bit for bit; stale data left in the shared scratch array by the previous
+    call would show up as a difference.  The second (smaller) problem is also
+    checked directly against the oracle."""
     import torch
     from kronecker_factored_gptq_gb300 import bakron as kb
     # a larger problem first, then a smaller one: the second call finds the
@@ -42,17 +47,15 @@ def test_noalloc_matches_quantize_on_consecutive_calls():
         UA32, UB32 = shared_factors(w.A, w.damp_A, w.B, w.damp_B)
         s = O.row_scale(w.W, w.qmax)
         dW, dUA, dUB, ds = to_dev(w.W, UA32, UB32, s)
-        V_ref, C_ref, pre_ref = kb.bakron_quantize(dW, dUA, dUB, ds, w.qmin, w.qmax,
-                                                   want_preround=True)
+        V_ref, C_ref, _ = kb.bakron_quantize(dW, dUA, dUB, ds, w.qmin, w.qmax)
         V = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
         C = torch.full((m, n), 99, dtype=torch.int8, device="cuda")
         assert _noalloc_via_c_abi(kb, dW, dUA, dUB, ds, w.qmin, w.qmax, V, C) == kb.OK
-        c_ref = C_ref.cpu().numpy().astype(np.float64)
         c_new = C.cpu().numpy().astype(np.float64)
-        # the comparison rule of the other parity tests (near ties only, <= 0.1%)
-        r = O.compare_codes(c_new, c_ref, pre_ref.cpu().numpy(), s, w.qmin, w.qmax, TOL, MAX_FRAC)
-        assert r["ok"], r
-        np.testing.assert_array_equal(V.cpu().numpy(), (s[:, None] * c_new.astype(np.float32)))
+        np.testing.assert_array_equal(c_new, C_ref.cpu().numpy().astype(np.float64))
+        np.testing.assert_array_equal(V.cpu().numpy(), V_ref.cpu().numpy())
+        if m == 200:
+            check_parity(w.W, UA32, UB32, s, w.qmin, w.qmax, V.cpu().numpy(), c_new)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
