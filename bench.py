@@ -33,28 +33,79 @@ if ROOT not in sys.path:
 
 METRIC = "BaKron solve sec & TFLOP/s at 8192x8192 fp32 (% of GB300 TF32/FP32 peak)"
 UNIT = "TFLOP/s"
-# Dense peaks.  MEASURED_PEAKS.json holds the measured bf16 GEMM rate; the TF32
-# tensor peak is that times the nominal tf32/bf16 ratio (1.1 / 2.25).  The
-# FP32 FMA peak is 152 SMs x 128 lanes x 2 flops x the maximum SM clock.
-NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
-FP32_LANES = 152 * 128
+T = 128   # the solver's tile edge
 
 
-def load_peaks():
+def load_measured_peaks():
+    """HBM copy bandwidth and cuBLAS bf16 rates measured by the pool's driver
+    (MEASURED_PEAKS.json), else the recipe's fallback figures."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    d = {}
     if os.path.exists(p):
         d = json.load(open(p))
-        src = "measured"
-    else:
-        d = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-             "sm_max_mhz": 2070.0}
-        src = "fallback"
-    tf32 = d["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
-    tf32_s = d.get("bf16_tflops_sustained", d["bf16_tflops"]) * NOMINAL_TF32_OVER_BF16
-    fp32 = FP32_LANES * 2 * d.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-    return {"src": src, "tf32_tflops": tf32, "tf32_tflops_sustained": tf32_s,
-            "fp32_tflops": fp32, "hbm_gbs": d["hbm_gbs"]}
+        d["src"] = "measured (MEASURED_PEAKS.json)"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "src": "fallback"}
+
+
+def measure_peaks(kb, torch, dev, seconds=3.0):
+    """The two roofline denominators, measured on this GPU in this run:
+    TF32 tensor-core rate of cuBLAS (torch.matmul on 8192^3 fp32 operands
+    with TF32 allowed; best of 10 launches, and back to back for `seconds`)
+    and the FP32 FMA rate of the library's own probe (bakron_fma_probe)."""
+    stream = torch.cuda.current_stream()
+    out = {}
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        fl = 2.0 * n ** 3
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            torch.matmul(a, b, out=c)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        out["tf32_tflops"] = fl / best / 1e12
+        k = max(1, int(seconds / best))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            torch.matmul(a, b, out=c)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out["tf32_tflops_sustained"] = k * fl / (e0.elapsed_time(e1) / 1e3) / 1e12
+        del a, b, c
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+    sms = kb.sm_count()
+    blocks = sms * 8
+    buf = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    iters = 20000
+    kb.fma_probe(buf, blocks, 200)
+    torch.cuda.synchronize()
+    best = 0.0
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fl = kb.fma_probe(buf, blocks, iters)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, fl / (e0.elapsed_time(e1) / 1e3) / 1e12)
+    out["fp32_tflops"] = best
+    out["sms"] = sms
+    out["how"] = ("tf32: torch.matmul 8192^3 fp32 with allow_tf32 (cuBLAS), best of 10 and back to "
+                  "back for %.0f s; fp32: bakron_fma_probe, %d CTAs x 256 threads x 8 FMA chains, "
+                  "best of 5" % (seconds, blocks))
+    return out
 
 
 def traffic_per_launch(kernel_file, profile_file):
@@ -176,19 +227,34 @@ def flops_model(m, n):
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_sample(w, a):
-    """The fp64 oracle (prepare + BaKron solve) on the leading a x a
-    sub-problem of workload w, with the leading principal blocks of A and B.
-    Returns (seconds, flops under the mn(m+n) model)."""
+def oracle_solve(w, a, impl="rowacc"):
+    """The fp64 oracle (prepare + solve) on the leading a x a sub-problem of
+    workload w (the leading principal blocks of A and B; a >= m, n: the whole
+    problem).  impl "rowacc": the C row-accumulator form on all host cores;
+    "bakron": the numpy divide and conquer over anti-diagonals.  Returns
+    (prepare seconds, solve seconds, flops under the mn(m+n) model)."""
     import oracle as O
-    a = min(a, w.m, w.n)
+    m, n = min(a, w.m), min(a, w.n)
     t0 = time.perf_counter()
-    _, UA = O.prepare(w.A[:a, :a], w.damp_A)
-    _, UB = O.prepare(w.B[:a, :a], w.damp_B)
-    Wa = w.W[:a, :a]
+    _, UA = O.prepare(w.A[:n, :n], w.damp_A)
+    _, UB = O.prepare(w.B[:m, :m], w.damp_B)
+    t1 = time.perf_counter()
+    Wa = w.W[:m, :n]
     s = O.row_scale(Wa, w.qmax)
-    O.bakron(Wa, UA, UB, s, w.qmin, w.qmax)
-    return time.perf_counter() - t0, flops_model(a, a)
+    if impl == "rowacc":
+        O.rowacc(Wa, UA, UB, s, w.qmin, w.qmax)
+    else:
+        O.bakron(Wa, UA, UB, s, w.qmin, w.qmax)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, flops_model(m, n)
+
+
+def oracle_threads():
+    try:
+        from oracle import rowacc as R
+        return R.threads()
+    except Exception:
+        return os.cpu_count()
 
 
 def blas_threads():
@@ -199,6 +265,28 @@ def blas_threads():
         return os.cpu_count()
 
 
+# Oracle timing per workload: whole solves where the C oracle takes seconds,
+# a named leading sub-problem for the three largest shapes.
+ORACLE_SAMPLE = {"tiny64": None, "c1024": None, "c4096": None,
+                 "mlp4096x14336": 2048, "mlp14336x4096": 2048, "c8192": 2048}
+
+
+def oracle_report(w):
+    a = ORACLE_SAMPLE.get(w.name)
+    whole = a is None
+    a = max(w.m, w.n) if whole else a
+    tp, ts, fl = oracle_solve(w, a, "rowacc")
+    r = {"impl": "rowacc (C, fp64, OpenMP)", "threads": oracle_threads(),
+         "problem": "whole %dx%d" % (w.m, w.n) if whole else
+                    "leading %dx%d sub-problem" % (min(a, w.m), min(a, w.n)),
+         "prepare_s": tp, "solve_s": ts, "solve_tflops": fl / ts / 1e12}
+    if w.m * w.n <= 1024 * 1024:
+        tp2, ts2, fl2 = oracle_solve(w, a, "bakron")
+        r["numpy_bakron"] = {"prepare_s": tp2, "solve_s": ts2, "solve_tflops": fl2 / ts2 / 1e12,
+                             "blas_threads": blas_threads()}
+    return r
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -206,29 +294,117 @@ def run_reference(args, world, rank):
     w = WL.load(args.config, seed=args.seed)
     a = args.sample
     for _ in range(args.warmup):
-        oracle_sample(w, a)
+        oracle_solve(w, a)
     ts = []
     fl = 0.0
     for _ in range(args.steps):
-        t, f = oracle_sample(w, a)
-        ts.append(t)
+        tp, tsolve, f = oracle_solve(w, a)
+        ts.append(tp + tsolve)
         fl += f
     total = sum(ts)
     value = fl / total / 1e12
-    cores = blas_threads()
+    cores = oracle_threads()
+    sub = min(a, w.m, w.n)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "%s, leading %dx%d sub-problem per step" % (w.name, a, a),
-                   "m": a, "n": a},
+        "config": {"workload": "%s, leading %dx%d sub-problem per step" % (w.name, sub, sub),
+                   "m": sub, "n": sub},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "fp64 oracle prepare + BaKron solve of the leading %dx%d "
-                                   "sub-problem of %s, %d steps" % (a, a, w.name, args.steps)},
+                         "sample": "fp64 oracle (C row-accumulator solve, %d threads) prepare + "
+                                   "solve of the leading %dx%d sub-problem of %s, %d steps"
+                                   % (cores, sub, sub, w.name, args.steps)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ metrics
+
+def solve_metrics(torch, W, V, codes, scale, LA, LB, qmin, qmax, tol=1e-4):
+    """fp64 metrics of a solve output on the GPU (measurement, not the solve):
+    E = L_B (W - V) L_A^T, the proxy loss ||E||_F^2 (= vec(V - W)^T (A (x) B)
+    vec(V - W)), and every rounding decision replayed from the output's own
+    history, w~ = V + E / (l^B l^A^T) (the GPTQ identity W - V = U^T e):
+    codes that differ from the replay, and how many of those are near ties
+    (within `tol` grid units of a rounding boundary inside the clamp range)."""
+    dt = torch.float64
+    LA64, LB64 = LA.to(dt), LB.to(dt)
+    E = LB64 @ (W.to(dt) - V.to(dt)) @ LA64.T
+    loss = float((E * E).sum())
+    wt = V.to(dt) + E / torch.outer(torch.diagonal(LB64), torch.diagonal(LA64))
+    del E
+    s32 = scale.to(torch.float32)[:, None]
+    rep = torch.round(wt.to(torch.float32) / s32).to(dt)
+    if qmin is not None:
+        rep = rep.clamp(min=float(qmin), max=float(qmax))
+    mism = rep != codes.to(dt)
+    t = wt / scale.to(dt)[:, None]
+    k = torch.floor(t)
+    near = (t - (k + 0.5)).abs() < tol
+    if qmin is not None:
+        near &= (k >= qmin) & (k + 1 <= qmax)
+    n_m = int(mism.sum())
+    bad = int((mism & ~near).sum())
+    return {"proxy_loss": loss, "cert_mismatch": n_m, "cert_not_near_tie": bad}
+
+
+def config_report(kb, torch, dev, w, reps, peaks):
+    """Solve and prepare times, TFLOP/s on the mn(m+n) model, fractions of
+    the measured peaks, proxy loss, certificate counts and the Corollary 3.4
+    bound on an unclamped unit-step run, for one workload."""
+    stream = torch.cuda.current_stream()
+    m, n = w.m, w.n
+    dW = torch.from_numpy(w.W).to(dev)
+    dA = torch.from_numpy(w.A).to(dev)
+    dB = torch.from_numpy(w.B).to(dev)
+    solver = kb.Solver(m, n, qmin=w.qmin, qmax=w.qmax)
+    solver.rowscale(dW)
+    solver.prepare(dA, w.damp_A, dB, w.damp_B)
+    solver.quantize(dW)
+    torch.cuda.synchronize()
+    tp, tq = [], []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        solver.rowscale(dW)
+        solver.prepare(dA, w.damp_A, dB, w.damp_B)
+        e[1].record(stream)
+        solver.quantize(dW)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        tp.append(e[0].elapsed_time(e[1]) / 1e3)
+        tq.append(e[1].elapsed_time(e[2]) / 1e3)
+    solve_s, prep_s = statistics.median(tq), statistics.median(tp)
+    fl = flops_model(m, n)
+    r = {"m": m, "n": n, "bits": w.bits, "solve_s": solve_s, "prepare_s": prep_s,
+         "solve_tflops": fl / solve_s / 1e12,
+         "solve_frac_of_tf32_peak": fl / solve_s / 1e12 / peaks["tf32_tflops"],
+         "solve_frac_of_fp32_peak": fl / solve_s / 1e12 / peaks["fp32_tflops"],
+         "reps": reps}
+    _, _, LA, LB, _ = kb.bakron_prepare(dA, w.damp_A, dB, w.damp_B, want_L=True)
+    r.update(solve_metrics(torch, dW, solver.V, solver.codes, solver.scale, LA, LB, w.qmin, w.qmax))
+    # Corollary 3.4 on an unclamped unit-step grid, input 10 W, same factors
+    ones = torch.ones(m, dtype=torch.float32, device=dev)
+    W10 = 10.0 * dW
+    Vu, cu, _ = kb.bakron_quantize(W10, solver.UA, solver.UB, ones, kb.INT32_MIN, kb.INT32_MAX,
+                                   workspace=solver.ws_q)
+    u = solve_metrics(torch, W10, Vu, cu, ones, LA, LB, None, None)
+    dt = torch.float64
+    lA2 = float((torch.diagonal(LA.to(dt)) ** 2).sum())
+    lB2 = float((torch.diagonal(LB.to(dt)) ** 2).sum())
+    trA = float(torch.trace(dA.to(dt))) * (1.0 + w.damp_A)
+    trB = float(torch.trace(dB.to(dt))) * (1.0 + w.damp_B)
+    r["cor34_unclamped"] = {"proxy_loss": u["proxy_loss"], "bound_tight": 0.25 * lA2 * lB2,
+                            "bound_trace": 0.25 * trA * trB,
+                            "holds": u["proxy_loss"] <= 0.25 * lA2 * lB2 <= 0.25 * trA * trB * (1 + 1e-5),
+                            "cert_mismatch": u["cert_mismatch"],
+                            "cert_not_near_tie": u["cert_not_near_tie"]}
+    del solver, dW, dA, dB, W10, Vu, cu, LA, LB
+    torch.cuda.empty_cache()
+    return r
 
 
 # ------------------------------------------------------------------ ours
@@ -298,8 +474,9 @@ def run_ours(args, world, rank, local):
     # slower than the headline pass and is reported separately.
     opts.times = kb.ctypes.pointer(times)
     solver.opts = opts
-    phase = {"leaf_ms": 0.0, "prop1_ms": 0.0, "prop2_ms": 0.0, "other_ms": 0.0, "prop_flops": 0.0,
-             "leaf_launches": 0, "prop_launches": 0, "other_launches": 0}
+    phase = {"leaf_ms": 0.0, "prop1_ms": 0.0, "prop2_ms": 0.0, "near_ms": 0.0, "other_ms": 0.0,
+             "prop_flops": 0.0, "leaf_launches": 0, "prop_launches": 0, "near_launches": 0,
+             "other_launches": 0}
     torch.cuda.synchronize()
     barrier(world)
     r_start = torch.cuda.Event(enable_timing=True)
@@ -319,42 +496,66 @@ def run_ours(args, world, rank, local):
     solve_ms = [e[1].elapsed_time(e[2]) for e in evs]
     fl = flops_model(m, n)
     value = world * args.steps * fl / total_s / 1e12
-    peaks = load_peaks()
+    peaks = measure_peaks(kb, torch, dev)
+    mp = load_measured_peaks()
 
-    # roofline of the dominant kernel class (by device time in the timed region)
-    prop_ms = phase["prop1_ms"] + phase["prop2_ms"]
+    # Roofline of the dominant kernel class by event-summed device time in the
+    # roofline pass.  The propagation product (prop_tc_kernel) counts in
+    # algorithmic units: the method's mn(m+n) flops less the work done inside
+    # the leaves' tiles (2 T^3 per tile, the in-tile row-accumulator form),
+    # divided by the event-summed time of every propagation launch (the
+    # off-path propagations and the near products between leaves), against the
+    # TF32 rate measured in this run (sustained: the kernel runs inside a
+    # seconds-long loop of steps).  The executed (dense 128-tile products) and
+    # issued (3 MMAs per product with the 3xTF32 split) fractions stand beside
+    # it.
+    steps = args.steps
+    tiles = -(-m // T) * -(-n // T)
+    prop_ms = (phase["prop1_ms"] + phase["prop2_ms"] + phase["near_ms"]) / steps
+    leaf_ms = phase["leaf_ms"] / steps
+    prop_launches = (phase["prop_launches"] + phase["near_launches"]) / steps
     use_tc = opts.use_3xtf32 == 1
-    if prop_ms >= phase["leaf_ms"]:
+    alg_prop = fl - 2.0 * T ** 3 * tiles
+    executed = phase["prop_flops"] / steps
+    if prop_ms >= leaf_ms:
         kernel = "prop_tc_kernel (tcgen05 3xTF32)" if use_tc else "prop_simt_kernel (fp32 FMA)"
-        per_launch_flops = phase["prop_flops"] / max(1, phase["prop_launches"])
-        per_launch_ms = prop_ms / max(1, phase["prop_launches"])
-        issued = 3.0 if use_tc else 1.0
-        achieved = issued * per_launch_flops / (per_launch_ms / 1e3) / 1e12
+        per_launch = alg_prop / max(1.0, prop_launches)
+        per_launch_ms = prop_ms / max(1.0, prop_launches)
+        achieved = alg_prop / (prop_ms / 1e3) / 1e12
         peak = peaks["tf32_tflops_sustained"] if use_tc else peaks["fp32_tflops"]
         bound = "tensor" if use_tc else "alu"
+        launches_per_step = prop_launches
+        share = prop_ms * steps / (instr_s * 1e3)
+        extra = {"executed_flops_per_solve": executed,
+                 "executed_frac": executed / (prop_ms / 1e3) / 1e12 / peak,
+                 "issued_frac": (3.0 if use_tc else 1.0) * executed / (prop_ms / 1e3) / 1e12 / peak,
+                 "algorithmic_flops_per_solve": alg_prop,
+                 "counting": "achieved = (m n (m+n) - 2 T^3 tiles) / event-summed propagation time; "
+                             "executed: dense 128-tile products; issued: x3 (3xTF32)"}
     else:
         kernel = "leaf_kernel"
-        T = 128
-        tiles = -(-m // T) * -(-n // T)
-        per_launch_flops = 2.0 * T ** 3 * tiles * args.steps / max(1, phase["leaf_launches"])
-        per_launch_ms = phase["leaf_ms"] / max(1, phase["leaf_launches"])
-        achieved = per_launch_flops / (per_launch_ms / 1e3) / 1e12
+        per_launch = 2.0 * T ** 3 * tiles / max(1.0, phase["leaf_launches"] / steps)
+        per_launch_ms = leaf_ms / max(1.0, phase["leaf_launches"] / steps)
+        achieved = 2.0 * T ** 3 * tiles / (leaf_ms / 1e3) / 1e12
         peak = peaks["fp32_tflops"]
         bound = "alu"
+        launches_per_step = phase["leaf_launches"] / steps
+        share = leaf_ms * steps / (instr_s * 1e3)
+        extra = {"counting": "2 T^3 flops per tile (in-tile row-accumulator form)"}
     roofline = {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_src": peaks["src"] + (" (bf16 x 1.1/2.25, sustained)" if bound == "tensor" else
-                                             " (152 SMs x 128 FP32 lanes x 2 x max SM clock)"),
+                "peak_src": "measured in this run (%s)" % ("TF32 cuBLAS, sustained" if bound == "tensor"
+                                                          else "bakron_fma_probe"),
+                "algorithmic_flops_per_launch": per_launch, "avg_launch_ms": per_launch_ms,
                 "traffic": (traffic_per_launch("kronecker_factored_gptq_gb300/csrc/prop_tc.cu",
-                                               "profiles/prop_tc_kernel_c8192_traffic.md")
+                                               "profiles/prop_tc_kernel_c4096_traffic.md")
                             if kernel != "leaf_kernel" and use_tc else None),
                 "traffic_unit": "bytes per launch (ncu dram read + write, see profiles/)",
-                "launches_per_step": (phase["leaf_launches"] if kernel == "leaf_kernel"
-                                      else phase["prop_launches"]) / args.steps,
-                "share_of_timed_region": (phase["leaf_ms"] if kernel == "leaf_kernel" else prop_ms)
-                / (instr_s * 1e3),
+                "launches_per_step": launches_per_step,
+                "share_of_timed_region": share,
                 "timed_in": "roofline pass: %d steps with per-launch events, %.2f ms per step"
-                            % (args.steps, 1e3 * instr_s / args.steps)}
+                            % (steps, 1e3 * instr_s / steps)}
+    roofline.update(extra)
 
     # End to end through the public API from pinned host buffers.  Copies run
     # on two copy streams, double-buffered: the inputs of step k+1 go up
@@ -501,12 +702,31 @@ def run_ours(args, world, rank, local):
                  "batched_tflops": fl_b / (statistics.median(bat) / 1e3) / 1e12}
         del probs, wsb
 
+    # Every workload: solve / prepare times, fractions of the measured peaks,
+    # proxy loss, certificate counts and Corollary 3.4 (GPU, fp64 metrics),
+    # and the fp64 oracle timed on the host cores (whole problems where the C
+    # oracle takes seconds, a named leading sub-problem for the largest).
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {}
+        del solver, dA, dB
+        torch.cuda.empty_cache()
+        for name in WL.CONFIGS:
+            wc = w if name == args.config else WL.load(name, seed=args.seed, device=dev)
+            reps = 3 if wc.m * wc.n >= 8192 * 4096 else 5
+            r = config_report(kb, torch, dev, wc, reps, peaks)
+            if not args.no_cpu_baseline:
+                r["oracle"] = oracle_report(wc)
+            per_config[name] = r
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t, f = oracle_sample(w, args.sample)
-        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-               "sample": "fp64 oracle prepare + BaKron solve of the leading %dx%d sub-problem of "
-                         "the workload (%.1f s)" % (min(args.sample, m, n), min(args.sample, m, n), t)}
+        tp, ts, f = oracle_solve(w, args.sample)
+        sub = min(args.sample, m, n)
+        cpu = {"value": f / (tp + ts) / 1e12, "unit": UNIT, "cores": oracle_threads(),
+               "kind": "oracle",
+               "sample": "fp64 oracle prepare + solve (C row-accumulator form) of the leading "
+                         "%dx%d sub-problem of the workload (%.1f s)" % (sub, sub, tp + ts)}
 
     if rank != 0:
         return
@@ -526,10 +746,13 @@ def run_ours(args, world, rank, local):
         "solve_frac_of_tf32_peak": fl / (solve_med / 1e3) / 1e12 / peaks["tf32_tflops"],
         "solve_frac_of_fp32_peak": fl / (solve_med / 1e3) / 1e12 / peaks["fp32_tflops"],
         "prepare_s": statistics.median(prep_ms) / 1e3,
+        "peaks": dict(peaks, hbm_gbs=mp.get("hbm_gbs"), bf16_tflops=mp.get("bf16_tflops"),
+                      hbm_bf16_src=mp.get("src")),
         "phases_ms_per_step": {k: (v / args.steps if k.endswith("_ms") else v)
                                for k, v in phase.items()},
         "executed_prop_flops_per_solve": phase["prop_flops"] / args.steps,
         "roofline": roofline,
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -551,14 +774,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c8192")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--sample", type=int, default=1024,
-                    help="edge of the leading sub-problem the CPU oracle times")
+    ap.add_argument("--sample", type=int, default=None,
+                    help="edge of the leading sub-problem the CPU oracle times (default 4096 for "
+                         "the CPU baseline beside the GPU arm, 2048 per step of --impl reference)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload table (solve times, metrics, oracle timings)")
     ap.add_argument("--simt", action="store_true", help="fp32 FMA propagation instead of tcgen05")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the context timings (one-sided GPTQ, factor accumulation)")
     args = ap.parse_args()
+    if args.sample is None:
+        args.sample = 2048 if args.impl == "reference" else 4096
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; the other ranks exit at
         # once, so no process group is needed

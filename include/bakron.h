@@ -13,14 +13,17 @@
  * - Pointers named "host" are host memory; every other pointer is DEVICE
  *   memory on the current CUDA device, owned by the caller.  The caller
  *   passes a workspace of at least the size the matching *_workspace_size
- *   call reports; the library allocates no other per-call memory.  The one
- *   exception is its schedules: the first call for a problem shape on a
- *   device builds the shape's work lists (16 bytes per 128-tile product,
- *   e.g. 0.8 MB for an 8192 x 8192 factor) and keeps one copy of each in
- *   mapped pinned host memory and one in device memory until the process
- *   exits, so that later calls read them in place.  bakron_quantize_noalloc
- *   allocates nothing.  Inputs are read-only; outputs must not alias inputs,
- *   each other or the workspace.
+ *   call reports.  The library allocates no device memory and no pinned
+ *   host memory, and keeps none between calls; it never synchronises the
+ *   whole device.  What it keeps are host-side descriptions of the
+ *   schedules of the problem shapes it has seen (ordinary host memory, the
+ *   work lists of 16 bytes per 128-tile product), and, per device, the
+ *   streams and events its calls reuse, created by the first call.  The work
+ *   lists reach the device inside kernel parameters, written into the
+ *   workspace on every call, or once into a caller-owned plan
+ *   (bakron_plan_init) that later calls read in place.  Inputs are
+ *   read-only; outputs must not alias inputs, each other, the workspace or a
+ *   plan.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *   enqueued on it; every compute call then synchronises the stream and reads
  *   back a device status word, so the returned status is final.  Outputs are
@@ -85,6 +88,9 @@ typedef struct {
                                CTA skips its first grid-barrier arrival, so
                                the others time out (BAKRON_ERR_TIMEOUT) */
   bakron_phase_times* times; /* host; NULL = no per-phase timing */
+  const void* plan;         /* device, nullable: the problem shape's work-list
+                               plan written by bakron_plan_init; NULL = write
+                               the work lists into the workspace on each call */
 } bakron_opts;
 
 /* Fill `opts` with the defaults above. */
@@ -140,6 +146,23 @@ bakron_status bakron_schedule_export(int kind, int64_t M, int64_t N, int32_t* ou
  * m x n problem (written to *bytes, host).  Pure host arithmetic. */
 bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opts,
                                     size_t* bytes);
+
+/* Work-list plan of a problem shape in caller-owned device memory.  A
+ * solve's work lists depend only on the shape's 128-tile grid (M = ceil(m /
+ * 128), N = ceil(n / 128)).  Without a plan each bakron_quantize call writes
+ * them into its workspace (about 0.9 MB at 8192 x 8192, a few dozen small
+ * launches); with bakron_opts.plan set to a plan of the same tile grid the
+ * call reads them in place.  bakron_plan_size: the plan's bytes (host
+ * arithmetic).  bakron_plan_init: writes the plan of the m x n shape into
+ * `plan` (device, 16-byte aligned, plan_bytes >= bakron_plan_size) on
+ * `stream` and synchronises it.  The plan serves the two-sided and the
+ * one-sided (UB NULL) solves of every shape with the same tile grid; a call
+ * given a plan of another grid returns BAKRON_ERR_INVALID_ARG (a header
+ * check on the device; every item is also bounds-checked before use).  The
+ * plan is only read: calls may share one plan concurrently. */
+bakron_status bakron_plan_size(int64_t m, int64_t n, size_t* bytes);
+bakron_status bakron_plan_init(int64_t m, int64_t n, void* plan, size_t plan_bytes,
+                               void* stream);
 
 /* Workspace bytes bakron_prepare needs for factors of order n and m
  * (either may be 0 when that factor is not prepared).  Pure host arithmetic. */
@@ -314,6 +337,18 @@ bakron_status bakron_quantize_noalloc(const float* W, int64_t m, int64_t n,
                                       const float* UA, const float* UB,
                                       const float* scale, int qmin, int qmax,
                                       float* V, int8_t* codes, void* stream);
+
+/* Measurement utilities (not part of the solve).
+ * bakron_fma_probe: enqueues `blocks` CTAs of 256 threads on `stream`, each
+ * thread running 8 independent chains of 16 * iters fp32 fused multiply-adds
+ * (2 flops each: blocks * 256 * iters * 256 flops in all), and writes one
+ * float per thread to out (device, blocks * 256 floats).  Returns after the
+ * launch, without synchronising; time it with events on `stream`.  It is the
+ * denominator of the FP32 (SIMT) roofline measured on the device at hand.
+ * bakron_sm_count: streaming multiprocessors of the current device
+ * (cudaDevAttrMultiProcessorCount), 1 if it cannot be read. */
+bakron_status bakron_fma_probe(float* out, int64_t blocks, int iters, void* stream);
+int bakron_sm_count(void);
 
 #ifdef __cplusplus
 }

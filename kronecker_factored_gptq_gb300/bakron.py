@@ -26,7 +26,8 @@ EXPORTS = ["bakron_default_opts", "bakron_status_string", "bakron_version", "bak
            "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
            "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
            "bakron_grid_params", "bakron_quantize_grid", "bakron_batch_workspace_size",
-           "bakron_quantize_batch", "bakron_schedule_export"]
+           "bakron_quantize_batch", "bakron_schedule_export", "bakron_fma_probe", "bakron_sm_count",
+           "bakron_plan_size", "bakron_plan_init"]
 FACTORS_KFAC = 0
 FACTORS_SHAMPOO = 1
 
@@ -45,7 +46,7 @@ class PhaseTimes(ctypes.Structure):
 class Opts(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int), ("leaf_width", ctypes.c_int), ("use_3xtf32", ctypes.c_int),
                 ("spin_budget_cycles", ctypes.c_longlong), ("fault_inject", ctypes.c_int),
-                ("times", ctypes.POINTER(PhaseTimes))]
+                ("times", ctypes.POINTER(PhaseTimes)), ("plan", ctypes.c_void_p)]
 
 
 class Problem(ctypes.Structure):
@@ -101,11 +102,16 @@ def lib():
     L.bakron_factors_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
     L.bakron_factors.argtypes = [vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, sz, vp]
     L.bakron_schedule_export.argtypes = [ctypes.c_int, i64, i64, vp, i64, ctypes.POINTER(i64)]
+    L.bakron_fma_probe.argtypes = [vp, i64, ctypes.c_int, vp]
+    L.bakron_plan_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
+    L.bakron_plan_init.argtypes = [i64, i64, vp, sz, vp]
+    L.bakron_sm_count.restype = ctypes.c_int
     for f in ("bakron_schedule_export", "bakron_workspace_size", "bakron_prepare_workspace_size", "bakron_rowscale",
               "bakron_prepare", "bakron_quantize", "bakron_quantize_antidiag",
               "bakron_quantize_noalloc", "bakron_factors_workspace_size", "bakron_factors",
               "bakron_grid_params", "bakron_quantize_grid", "bakron_batch_workspace_size",
-              "bakron_quantize_batch"):
+              "bakron_quantize_batch", "bakron_fma_probe", "bakron_plan_size",
+              "bakron_plan_init"):
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
@@ -114,6 +120,24 @@ def lib():
 def kernel_launches():
     """Kernels the library has launched in this process so far."""
     return int(lib().bakron_kernel_launches())
+
+
+def sm_count():
+    """Streaming multiprocessors of the current CUDA device."""
+    return int(lib().bakron_sm_count())
+
+
+def fma_probe(out, blocks, iters):
+    """Enqueue the FP32 FMA throughput probe on the current stream (see
+    bakron_fma_probe); ``out`` is a float32 CUDA tensor of blocks * 256
+    elements.  Returns the flops it performs."""
+    import torch
+    assert out.dtype == torch.float32 and out.is_cuda and out.numel() >= blocks * 256
+    st = lib().bakron_fma_probe(ctypes.c_void_p(out.data_ptr()), int(blocks), int(iters),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if st != OK:
+        raise BakronError(st, "bakron_fma_probe")
+    return 2.0 * blocks * 256 * iters * 128
 
 
 SCHEDULE_SOLVE = 0
@@ -181,6 +205,26 @@ def workspace_size(m, n, opts=None):
     _check(lib().bakron_workspace_size(m, n, ctypes.byref(opts) if opts else None, ctypes.byref(b)),
            "bakron_workspace_size")
     return b.value
+
+
+def plan_size(m, n):
+    b = ctypes.c_size_t(0)
+    _check(lib().bakron_plan_size(m, n, ctypes.byref(b)), "bakron_plan_size")
+    return b.value
+
+
+def bakron_plan_init(m, n, plan=None, stream=None):
+    """The work-list plan of the m x n shape in a device buffer (uint8 tensor,
+    allocated here when ``plan`` is None); pass it as ``opts.plan``."""
+    torch = _torch()
+    nb = plan_size(m, n)
+    if plan is None:
+        plan = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    elif plan.numel() * plan.element_size() < nb:
+        raise ValueError("plan buffer too small: need %d bytes" % nb)
+    _check(lib().bakron_plan_init(m, n, ctypes.c_void_p(plan.data_ptr()), nb, _stream(stream)),
+           "bakron_plan_init")
+    return plan
 
 
 def prepare_workspace_size(n, m):
@@ -449,8 +493,8 @@ def bakron_factors(X=None, G=None, mode=FACTORS_KFAC, want_A=True, want_B=True, 
 class Solver:
     """The whole path on one GPU: row grid, factor preparation, solve.
 
-    Workspaces and outputs are allocated once per shape and reused, so
-    repeated solves of one shape allocate nothing.
+    Workspaces, the shape's work-list plan and the outputs are allocated once
+    per shape and reused, so repeated solves of one shape allocate nothing.
     """
 
     def __init__(self, m, n, bits=None, qmin=None, qmax=None, opts=None, stream=None):
@@ -461,9 +505,10 @@ class Solver:
             self.qmin = -(self.qmax + 1)
         else:
             self.qmin, self.qmax = qmin, qmax
-        self.opts = opts
+        self.opts = opts if opts is not None else default_opts()
         self.stream = stream
         dev = "cuda"
+        self.plan = bakron_plan_init(m, n, stream=stream)
         self.ws_q = torch.empty(workspace_size(m, n, opts), dtype=torch.uint8, device=dev)
         self.ws_p = torch.empty(prepare_workspace_size(n, m), dtype=torch.uint8, device=dev)
         self.scale = torch.empty(m, dtype=torch.float32, device=dev)
@@ -481,6 +526,8 @@ class Solver:
         return self.UA, self.UB
 
     def quantize(self, W, UA=None, UB=None, scale=None, want_preround=False):
+        if self.opts is not None and not self.opts.plan:
+            self.opts.plan = self.plan.data_ptr()
         return bakron_quantize(W, self.UA if UA is None else UA, self.UB if UB is None else UB,
                                self.scale if scale is None else scale, self.qmin, self.qmax,
                                want_preround=want_preround, opts=self.opts, workspace=self.ws_q,

@@ -337,6 +337,32 @@ const RowsSchedule& get_rows_schedule(int M, int N) {
   return cache.emplace(key, std::move(s)).first->second;
 }
 
+// The work lists of a solve on stream s: read in place from the caller's
+// plan (after a header check that sets BAKRON_ERR_INVALID_ARG on a mismatch),
+// or written into the workspace region ws_dst (kernel parameters, see
+// fill_items).
+cudaError_t stage_schedule(const void* plan, bool two_sided, int M, int N, WorkItem* ws_dst,
+                           DevStatus* st, cudaStream_t s, const WorkItem** out) {
+  const Schedule& sch = get_schedule(M, N);
+  const RowsSchedule& rs = get_rows_schedule(M, N);
+  if (plan) {
+    cudaError_t e = launch_plan_check(plan, M, N, (int64_t)sch.items.size(), (int64_t)rs.items.size(),
+                                      st, s);
+    if (e != cudaSuccess) return e;
+    const WorkItem* base = (const WorkItem*)((const char*)plan + kPlanHeaderBytes);
+    *out = two_sided ? base : base + sch.items.size();
+    return cudaSuccess;
+  }
+  *out = ws_dst;
+  return two_sided ? fill_items(sch.items.data(), sch.items.size(), ws_dst, s)
+                   : fill_items(rs.items.data(), rs.items.size(), ws_dst, s);
+}
+
+size_t plan_bytes(int M, int N) {
+  return kPlanHeaderBytes +
+         sizeof(WorkItem) * (get_schedule(M, N).items.size() + get_rows_schedule(M, N).items.size());
+}
+
 constexpr int kMaxDepth = 24;
 
 struct QLayout {
@@ -698,7 +724,8 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     TRY_SOLVE(cudaStreamWaitEvent(cs, ev, 0));
   }
   TRY_SOLVE(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
-  TRY_SOLVE(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
+  TRY_SOLVE(stage_schedule(o.plan, false, (int)L.M, (int)L.N, (WorkItem*)(base + L.sched), st, cs,
+                           &items));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();
@@ -803,6 +830,7 @@ void bakron_default_opts(bakron_opts* o) {
   o->spin_budget_cycles = 4000000000LL;
   o->fault_inject = 0;
   o->times = nullptr;
+  o->plan = nullptr;
 }
 
 const char* bakron_status_string(int st) {
@@ -906,6 +934,48 @@ bakron_status bakron_workspace_size(int64_t m, int64_t n, const bakron_opts* opt
     const QLayout q = quantize_layout(m, n);
     const ALayout a = antidiag_layout(m, n);
     *bytes = std::max(q.total, a.total);
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
+}
+
+bakron_status bakron_plan_size(int64_t m, int64_t n, size_t* bytes) {
+  try {
+    if (!bytes || !sizes_ok(m, n)) return BAKRON_ERR_INVALID_ARG;
+    *bytes = plan_bytes((int)((m + T - 1) / T), (int)((n + T - 1) / T));
+    return BAKRON_OK;
+  } catch (...) {
+    return BAKRON_ERR_INVALID_ARG;   // host allocation failure
+  }
+}
+
+bakron_status bakron_plan_init(int64_t m, int64_t n, void* plan, size_t plan_bytes_given,
+                               void* stream) {
+  try {
+    if (!plan || !sizes_ok(m, n) || ((uintptr_t)plan & 15)) return BAKRON_ERR_INVALID_ARG;
+    const int M = (int)((m + T - 1) / T), N = (int)((n + T - 1) / T);
+    if (plan_bytes_given < plan_bytes(M, N)) return BAKRON_ERR_INVALID_ARG;
+    const Schedule& sch = get_schedule(M, N);
+    const RowsSchedule& rs = get_rows_schedule(M, N);
+    // the header as the first 16 work-item slots, then both lists
+    std::vector<WorkItem> all(kPlanHeaderBytes / sizeof(WorkItem) + sch.items.size() +
+                              rs.items.size());
+    PlanHeader h{};
+    h.magic = kPlanMagic;
+    h.version = kPlanVersion;
+    h.M = M;
+    h.N = N;
+    h.n_solve = (long long)sch.items.size();
+    h.n_rows = (long long)rs.items.size();
+    h.off_solve = (long long)(kPlanHeaderBytes / sizeof(WorkItem));
+    h.off_rows = h.off_solve + h.n_solve;
+    std::memcpy(all.data(), &h, sizeof(h));
+    std::copy(sch.items.begin(), sch.items.end(), all.begin() + h.off_solve);
+    std::copy(rs.items.begin(), rs.items.end(), all.begin() + h.off_rows);
+    cudaStream_t s = (cudaStream_t)stream;
+    TRY_CUDA(fill_items(all.data(), all.size(), (WorkItem*)plan, s));
+    TRY_CUDA(cudaStreamSynchronize(s));
     return BAKRON_OK;
   } catch (...) {
     return BAKRON_ERR_INVALID_ARG;   // host allocation failure
@@ -1089,7 +1159,8 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
     TRY_SOLVE(cudaStreamWaitEvent(cs, ev, 0));
   }
   TRY_SOLVE(cudaMemsetAsync(st, 0, sizeof(DevStatus), cs));
-  TRY_SOLVE(stage_items(sch.items.data(), sch.items.size(), (WorkItem*)(base + L.sched), cs, &items));
+  TRY_SOLVE(stage_schedule(o.plan, true, (int)L.M, (int)L.N, (WorkItem*)(base + L.sched), st, cs,
+                           &items));
   PhaseTimer pt(o.times, cs);
   {
     cudaEvent_t ev = pt.begin();

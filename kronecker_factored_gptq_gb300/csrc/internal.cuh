@@ -64,6 +64,14 @@ struct WorkItem {
   int r, c, k0, k1;
 };
 
+// True when a work item lies inside the operands of a product launch: every
+// tile it reads or writes exists.  Items come from the library's schedules,
+// or from a caller's plan, which could belong to another shape; a kernel
+// refuses an item that fails this (BAKRON_ERR_INVALID_ARG) instead of
+// running it.
+struct PropArgs;
+__device__ __forceinline__ bool item_in_bounds(const WorkItem& it, const PropArgs& p);
+
 struct PropArgs {
   // C[r][c] = sum_k A[r][k] * B[c][k], A and B row-major with leading
   // dimensions lda/ldb, each given as an (hi, lo) pair whose sum is exact.
@@ -99,6 +107,12 @@ struct LeafArgs {
   int pdl;    // launch as a programmatic dependent of the previous kernel
 };
 
+__device__ __forceinline__ bool item_in_bounds(const WorkItem& it, const PropArgs& p) {
+  return it.r >= 0 && it.c >= 0 && it.k0 >= 0 && it.k1 > it.k0 &&
+         (int64_t)(it.r + 1) * kTile <= p.a_rows && (int64_t)(it.c + 1) * kTile <= p.b_rows &&
+         (int64_t)it.k1 * kTile <= p.lda && (int64_t)it.k1 * kTile <= p.ldb;
+}
+
 // Launch `k` on `s`, as a programmatic dependent of the previous kernel in
 // the stream when `pdl` is set.
 template <typename... KArgs, typename... Args>
@@ -117,15 +131,25 @@ cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
 }
 
-// Copy a cached host work list into the workspace (see misc.cu); the
-// no-allocation entry point sets the thread flag for the length of its call.
-// Device address of a host-built work list for kernels on stream s: its
-// device-resident copy (made by the first call, later calls wait for it), or
-// ws_dst after copying the list there (calls that must not allocate, and
-// calls during stream capture before the resident copy exists).
-cudaError_t stage_items(const WorkItem* src, size_t count, WorkItem* ws_dst, cudaStream_t s,
-                        const WorkItem** out);
-void set_no_host_alloc(bool on);
+// Write `count` host work items to device memory at dst, in stream order on
+// s, as the parameters of copy kernels (see misc.cu).
+cudaError_t fill_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s);
+
+// A work-list plan in caller-owned device memory (bakron_plan_init): this
+// header, padded to kPlanHeaderBytes, then the two-sided solve's items, then
+// the one-sided solve's items.
+constexpr unsigned long long kPlanMagic = 0x4e414c504e4f524bULL;
+constexpr int kPlanVersion = 1;
+constexpr size_t kPlanHeaderBytes = 256;
+struct PlanHeader {
+  unsigned long long magic;
+  int version, M, N, pad;
+  long long n_solve, n_rows;      // items of each list
+  long long off_solve, off_rows;  // their offsets in items from the plan's start
+};
+static_assert(sizeof(PlanHeader) <= kPlanHeaderBytes, "plan header");
+cudaError_t launch_plan_check(const void* plan, int M, int N, int64_t n_solve, int64_t n_rows,
+                              DevStatus* st, cudaStream_t s);
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per device: `done` is the call site's own flag word (bit d set

@@ -4,6 +4,7 @@
 #include <map>
 #include <mutex>
 
+#include <algorithm>
 #include <cstring>
 
 #include "internal.cuh"
@@ -251,34 +252,35 @@ cudaError_t launch_check_finite(const float* x, int64_t count, DevStatus* st, cu
 }
 
 // ------------------------------------------------------ work-item staging
-// The host-built work lists of a cached schedule never change, so each list
-// gets one device-resident copy per device, made by the first call that needs
-// it and read in place by every later call.  The first call stages the list in
-// mapped pinned host memory and copies it with a kernel that reads it over the
-// host link (a DMA copy would queue on the host-to-device copy engine behind
-// any large transfer the caller has in flight, such as the next problem's
-// inputs), then records an event that later calls on other streams wait for.
-// Calls that must not allocate (thread flag) copy into the caller's
-// workspace with a plain asynchronous copy; calls made while their stream is
-// being captured into a graph copy into the workspace with the kernel.
-__global__ void copy_items_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = src[i];
+// The host-built work lists reach the device as kernel parameters: each
+// launch of fill_items_kernel carries up to kFillItems items in its
+// parameter block and writes them into device memory the caller owns (the
+// workspace, or a plan).  Parameters travel with the launch itself, so the
+// copy allocates nothing, needs no pinned staging buffer, does not queue on
+// the copy engine behind the caller's own transfers, and can be captured
+// into a CUDA graph like any other launch.
+constexpr int kFillItems = 2000;   // 32000 bytes, under the 32764-byte parameter limit
+struct FillBlock {
+  WorkItem it[kFillItems];
+};
+
+__global__ void __launch_bounds__(256) fill_items_kernel(const __grid_constant__ FillBlock b,
+                                                         WorkItem* __restrict__ dst, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = b.it[i];
 }
 
-namespace {
-thread_local bool t_no_host_alloc = false;
-struct Staged {
-  void* host = nullptr;         // mapped pinned copy of the list
-  const void* mapped = nullptr; // its device address
-  void* resident = nullptr;     // device-resident copy (null while capturing)
-  cudaEvent_t ready = nullptr;  // recorded after the resident copy was made
-  size_t bytes = 0;
-};
-}  // namespace
-
-void set_no_host_alloc(bool on) { t_no_host_alloc = on; }
+cudaError_t fill_items(const WorkItem* src, size_t count, WorkItem* dst, cudaStream_t s) {
+  static thread_local FillBlock blk;
+  for (size_t off = 0; off < count; off += kFillItems) {
+    const int n = (int)std::min<size_t>(kFillItems, count - off);
+    std::memcpy(blk.it, src + off, sizeof(WorkItem) * n);
+    count_launch();
+    fill_items_kernel<<<1, 256, 0, s>>>(blk, dst + off, n);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t ensure_smem_limit(const void* kernel, size_t bytes,
                               std::atomic<unsigned long long>& done) {
@@ -292,79 +294,22 @@ cudaError_t ensure_smem_limit(const void* kernel, size_t bytes,
   return e;
 }
 
-cudaError_t stage_items(const WorkItem* src, size_t count, WorkItem* ws_dst, cudaStream_t s,
-                        const WorkItem** out) {
-  *out = ws_dst;
-  if (count == 0) return cudaSuccess;
-  const size_t bytes = sizeof(WorkItem) * count;
-  if (t_no_host_alloc) return cudaMemcpyAsync(ws_dst, src, bytes, cudaMemcpyHostToDevice, s);
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(s, &cap);
-  if (e != cudaSuccess) return e;
-  const bool capturing = cap != cudaStreamCaptureStatusNone;
-  static std::mutex mu;
-  static std::map<std::pair<const void*, int>, Staged> cache;   // (list, device)
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  const int64_t n16 = (int64_t)(bytes / 16);
-  std::lock_guard<std::mutex> lk(mu);
-  Staged& st = cache[std::make_pair((const void*)src, dev)];
-  if (st.bytes != bytes) {
-    // the cached lists never change or move; a list seen with another size
-    // is a new list at a reused address (the old copies are released once
-    // the device is idle)
-    if (st.host || st.resident) {
-      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return e;
-      if (st.host) cudaFreeHost(st.host);
-      if (st.resident) cudaFree(st.resident);
-      if (st.ready) cudaEventDestroy(st.ready);
-    }
-    st = Staged{};
-    void* h = nullptr;
-    if ((e = cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess)
-      return e;
-    std::memcpy(h, src, bytes);
-    void* d = nullptr;
-    if ((e = cudaHostGetDevicePointer(&d, h, 0)) != cudaSuccess) {
-      cudaFreeHost(h);
-      return e;
-    }
-    st.host = h;
-    st.mapped = d;
-    st.bytes = bytes;
-  }
-  if (!st.resident && !capturing) {
-    void* r = nullptr;
-    if ((e = cudaMalloc(&r, bytes)) != cudaSuccess) return e;
-    cudaEvent_t ev = nullptr;
-    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
-      cudaFree(r);
-      return e;
-    }
-    count_launch();
-    copy_items_kernel<<<grid_for(n16, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(st.mapped),
-                                                          reinterpret_cast<uint4*>(r), n16);
-    if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaEventRecord(ev, s)) != cudaSuccess) {
-      // nothing was queued that reads r, or the copy is queued but unusable:
-      // release after the stream is done with it
-      cudaStreamSynchronize(s);
-      cudaFree(r);
-      cudaEventDestroy(ev);
-      return e;
-    }
-    st.resident = r;
-    st.ready = ev;
-    *out = reinterpret_cast<const WorkItem*>(r);
-    return cudaSuccess;
-  }
-  if (st.resident) {
-    *out = reinterpret_cast<const WorkItem*>(st.resident);
-    return cudaStreamWaitEvent(s, st.ready, 0);
-  }
-  // capturing before any resident copy exists: copy into the workspace
+// A plan's header check: BAKRON_ERR_INVALID_ARG unless the plan was written
+// by bakron_plan_init for this tile grid (the kernels that read its items
+// also bounds-check every item, so a wrong plan cannot make them access
+// memory outside their matrices).
+__global__ void plan_check_kernel(const PlanHeader* __restrict__ h, int M, int N, int64_t n_solve,
+                                  int64_t n_rows, DevStatus* st) {
+  if (threadIdx.x != 0) return;
+  if (h->magic != kPlanMagic || h->version != kPlanVersion || h->M != M || h->N != N ||
+      h->n_solve != n_solve || h->n_rows != n_rows)
+    set_status(st, BAKRON_ERR_INVALID_ARG);
+}
+
+cudaError_t launch_plan_check(const void* plan, int M, int N, int64_t n_solve, int64_t n_rows,
+                              DevStatus* st, cudaStream_t s) {
   count_launch();
-  copy_items_kernel<<<grid_for(n16, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(st.mapped),
-                                                        reinterpret_cast<uint4*>(ws_dst), n16);
+  plan_check_kernel<<<1, 32, 0, s>>>(static_cast<const PlanHeader*>(plan), M, N, n_solve, n_rows, st);
   return cudaGetLastError();
 }
 

@@ -69,10 +69,6 @@ extern "C" bakron_status bakron_quantize_noalloc(const float* W, int64_t m, int6
   if (need > kNoAllocBytes) return BAKRON_ERR_INVALID_ARG;
   void* ws = nullptr;
   if (scratch_for_current_device(&ws) != cudaSuccess) return BAKRON_ERR_CUDA;
-  // no pinned staging of the work lists either: a plain copy
-  set_no_host_alloc(true);
-  const bakron_status r = bakron_quantize(W, m, n, UA, UB, scale, qmin, qmax, V, codes, nullptr,
-                                          nullptr, ws, kNoAllocBytes, stream);
-  set_no_host_alloc(false);
-  return r;
+  return bakron_quantize(W, m, n, UA, UB, scale, qmin, qmax, V, codes, nullptr, nullptr, ws,
+                         kNoAllocBytes, stream);
 }

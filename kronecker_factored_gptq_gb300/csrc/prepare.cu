@@ -515,7 +515,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   BK_TRY(ensure_smem_limit((const void*)split_diag_kernel, sizeof(float) * NB * PP, done[1]));
   const PrepItems& P = prep_items(kp);
   const WorkItem* items = a.items;
-  BK_TRY(stage_items(P.items.data(), P.items.size(), a.items, s, &items));
+  BK_TRY(fill_items(P.items.data(), P.items.size(), a.items, s));
   count_launch();
   diag_mean_kernel<<<1, 256, 0, s>>>(a.X, k, a.damp, a.scal);
   BK_TRY(cudaGetLastError());

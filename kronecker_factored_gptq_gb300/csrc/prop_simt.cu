@@ -17,6 +17,10 @@ __global__ void __launch_bounds__(256) prop_simt_kernel(PropArgs p) {
   __shared__ __align__(16) float As[BK][BM + PAD];
   __shared__ __align__(16) float Bs[BK][BN + PAD];
   const WorkItem it = p.items[blockIdx.x];
+  if (!item_in_bounds(it, p)) {
+    if (threadIdx.x == 0) set_status(p.st, BAKRON_ERR_INVALID_ARG);
+    return;
+  }
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
   const int64_t r0 = (int64_t)it.r * BM, c0 = (int64_t)it.c * BN;

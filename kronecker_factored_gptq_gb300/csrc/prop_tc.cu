@@ -155,6 +155,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[blockIdx.x];
+  if (!item_in_bounds(it, p)) {   // uniform over the CTA: nothing set up yet
+    if (threadIdx.x == 0) set_status(st, BAKRON_ERR_INVALID_ARG);
+    return;
+  }
   const int nk = (it.k1 - it.k0) * SPC;     // K slices
   const int nc = it.k1 - it.k0;             // accumulation chunks (K tiles)
   // 1024-byte aligned stage ring

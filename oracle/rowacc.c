@@ -32,6 +32,9 @@
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -96,9 +99,114 @@ long long rowacc_solve(const double* W, const double* UA, const double* UB, cons
   return overrides;
 }
 
+/* The same solve, traversed by blocks of `rb` consecutive rows instead of by
+ * anti-diagonals, for speed at the full workload sizes (the arithmetic per
+ * entry is the one above).  A block takes its columns left to right; column
+ * j of block b starts once block b - 1 has finished column j (a progress
+ * counter per block), which, by induction over the blocks above, puts every
+ * entry to the top-left of (i, j) before it: the order Theorem 3.2 allows.
+ * Inside a block, the entries of column j go top to bottom; each pushes its
+ * finished row accumulator R_i(j) into the block's later rows at once, and
+ * into the rows below the block together with the block's other rows (one
+ * pass over S(j, .)); the row updates R_i(j'') += E_ij U_A[j, j''] of the
+ * block's rows share one pass over row j of U_A.  The rows of R and U_B a
+ * block works on stay in its thread's cache, so memory traffic drops by
+ * about `rb` against the anti-diagonal traversal.  Only the grouping of the
+ * column sums S(j, i) changes (sums of each block's contributions are added
+ * to S in one step), so the result agrees with rowacc_solve up to fp64
+ * rounding.  Blocks are dealt to threads in turn; each thread takes its
+ * blocks in increasing order and every wait is on a lower block, so the
+ * waits always end. */
+long long rowacc_solve_blocked(const double* W, const double* UA, const double* UB, const float* s,
+                               int64_t m, int64_t n, int clamp, double qmin, double qmax,
+                               const double* guide, double guide_tol, double* codes,
+                               double* preround, double* E, int rb) {
+  if (rb < 1) rb = 1;
+  if (rb > 64) rb = 64;
+  const int64_t nb = (m + rb - 1) / rb;
+  double* R = (double*)calloc((size_t)(m * n), sizeof(double));   /* R[i][j] */
+  double* S = (double*)calloc((size_t)(n * m), sizeof(double));   /* S[j][i] */
+  int64_t* done = (int64_t*)calloc((size_t)nb, sizeof(int64_t));  /* columns finished per block */
+  if (!R || !S || !done) {
+    free(R);
+    free(S);
+    free(done);
+    return -1;
+  }
+  long long overrides = 0;
+#pragma omp parallel reduction(+ : overrides)
+  {
+    int nt = 1, t = 0;
+#ifdef _OPENMP
+    nt = omp_get_num_threads();
+    t = omp_get_thread_num();
+#endif
+    double sl[64], ev[64], rf[64];
+    for (int64_t b = t; b < nb; b += nt) {
+      const int64_t i0 = b * rb, i1 = i0 + rb < m ? i0 + rb : m;
+      const int rows = (int)(i1 - i0);
+      for (int64_t j = 0; j < n; ++j) {
+        if (b > 0)
+          while (__atomic_load_n(&done[b - 1], __ATOMIC_ACQUIRE) < j + 1) {
+          }
+        double* Sj = S + j * m;
+        for (int r = 0; r < rows; ++r) sl[r] = Sj[i0 + r];
+        const double ua = UA[j * n + j];
+        for (int r = 0; r < rows; ++r) {
+          const int64_t i = i0 + r;
+          const double x = W[i * n + j] - sl[r] - UB[i * m + i] * R[i * n + j];
+          const float tq = (float)x / s[i];
+          double c = (double)rintf(tq);
+          if (clamp) {
+            if (c < qmin) c = qmin;
+            if (c > qmax) c = qmax;
+          }
+          if (guide && near_tie(x, (double)s[i], clamp, qmin, qmax, guide_tol)) {
+            const double g = guide[i * n + j];
+            if (g != c) ++overrides;
+            c = g;
+          }
+          const double lB = 1.0 / UB[i * m + i], lA = 1.0 / ua;
+          const double e = (x - (double)s[i] * c) * lB * lA;
+          codes[i * n + j] = c;
+          preround[i * n + j] = x;
+          E[i * n + j] = e;
+          ev[r] = e;
+          rf[r] = R[i * n + j] + e * ua;   /* R_i(j), final */
+          R[i * n + j] = rf[r];
+          for (int r2 = r + 1; r2 < rows; ++r2) sl[r2] += rf[r] * UB[i * m + i0 + r2];
+        }
+        /* row updates of the block's rows for the later columns */
+        const double* uaj = UA + j * n;
+        for (int r = 0; r < rows; ++r) {
+          double* Ri = R + (i0 + r) * n;
+          const double e = ev[r];
+          for (int64_t jj = j + 1; jj < n; ++jj) Ri[jj] += e * uaj[jj];
+        }
+        /* the block's finished accumulators into the rows below it */
+        for (int64_t c0 = i1; c0 < m; c0 += 64) {
+          const int len = m - c0 < 64 ? (int)(m - c0) : 64;
+          double acc[64];
+          for (int k = 0; k < len; ++k) acc[k] = 0.0;
+          for (int r = 0; r < rows; ++r) {
+            const double f = rf[r];
+            const double* ub = UB + (i0 + r) * m + c0;
+            for (int k = 0; k < len; ++k) acc[k] += f * ub[k];
+          }
+          for (int k = 0; k < len; ++k) Sj[c0 + k] += acc[k];
+        }
+        __atomic_store_n(&done[b], j + 1, __ATOMIC_RELEASE);
+      }
+    }
+  }
+  free(R);
+  free(S);
+  free(done);
+  return overrides;
+}
+
 /* Threads the parallel loop may use (0: the OpenMP default). */
 #ifdef _OPENMP
-#include <omp.h>
 int rowacc_threads(int want) {
   if (want > 0) omp_set_num_threads(want);
   return omp_get_max_threads();

@@ -35,6 +35,8 @@ def _load():
         lib.rowacc_solve.restype = ctypes.c_longlong
         lib.rowacc_solve.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                      ctypes.c_double, ctypes.c_double, P, ctypes.c_double, P, P, P]
+        lib.rowacc_solve_blocked.restype = ctypes.c_longlong
+        lib.rowacc_solve_blocked.argtypes = lib.rowacc_solve.argtypes + [ctypes.c_int]
         lib.rowacc_threads.restype = ctypes.c_int
         lib.rowacc_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -50,10 +52,13 @@ def _ptr(a):
     return ctypes.c_void_p(a.ctypes.data)
 
 
-def rowacc(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
+def rowacc(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4, rows_per_block=0):
     """GPTQ output for W (m x n) with update factors UA (n x n), UB (m x m) and
     the per-row grid ``s`` (fp32 scales, codes clamped to [qmin, qmax]; both
     None: no clamp).  ``guide``: codes taken at the solver's own near ties.
+    ``rows_per_block`` 0: anti-diagonal traversal (``rowacc_solve``); k > 0:
+    blocks of k rows (``rowacc_solve_blocked``, the same arithmetic per entry,
+    column sums grouped by block; for the full workload sizes).
     Returns a :class:`SolveResult` (codes, preround, V = s c, E)."""
     lib = _load()
     W = np.ascontiguousarray(W, dtype=np.float64)
@@ -68,10 +73,13 @@ def rowacc(W, UA, UB, s, qmin=None, qmax=None, guide=None, guide_tol=1e-4):
     codes = np.empty((m, n))
     pre = np.empty((m, n))
     E = np.empty((m, n))
-    over = lib.rowacc_solve(_ptr(W), _ptr(UA), _ptr(UB), _ptr(s32), m, n, int(clamp),
-                            float(qmin) if clamp else 0.0, float(qmax) if clamp else 0.0,
-                            None if g is None else _ptr(g), float(guide_tol), _ptr(codes),
-                            _ptr(pre), _ptr(E))
+    args = [_ptr(W), _ptr(UA), _ptr(UB), _ptr(s32), m, n, int(clamp),
+            float(qmin) if clamp else 0.0, float(qmax) if clamp else 0.0,
+            None if g is None else _ptr(g), float(guide_tol), _ptr(codes), _ptr(pre), _ptr(E)]
+    if rows_per_block > 0:
+        over = lib.rowacc_solve_blocked(*args, int(rows_per_block))
+    else:
+        over = lib.rowacc_solve(*args)
     if over < 0:
         raise MemoryError("rowacc: scratch allocation failed")
     V = s32.astype(np.float64)[:, None] * codes

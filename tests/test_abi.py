@@ -110,3 +110,41 @@ def test_size_limits(L):
     assert L.bakron_schedule_export(0, 2048, 1024, None, 0, ctypes.byref(n)) == 1
     assert L.bakron_schedule_export(2, 513, 1, None, 0, ctypes.byref(n)) == 1
     assert L.bakron_schedule_export(2, 16, 1, None, 0, ctypes.byref(n)) == 0 and n.value > 0
+
+
+def test_plan_size_and_invalid_plan_arguments(L):
+    """The plan holds a header and both solves' work lists (16 bytes per
+    128-tile product) of the shape's tile grid; shapes with the same grid
+    share it.  Bad arguments return before any CUDA call."""
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    b = ctypes.c_size_t(0)
+    assert L.bakron_plan_size(8192, 8192, ctypes.byref(b)) == 0
+    n = (len(kb.schedule_export(kb.SCHEDULE_SOLVE, 64, 64)) and
+         int(kb.schedule_export(kb.SCHEDULE_SOLVE, 64, 64)[2]) +
+         int(kb.schedule_export(kb.SCHEDULE_ROWS, 64, 64)[2]))
+    assert b.value == 256 + 16 * n
+    assert kb.plan_size(8100, 8192) == kb.plan_size(8192, 8192)
+    assert L.bakron_plan_size(0, 8, ctypes.byref(b)) == 1
+    assert L.bakron_plan_size(8, 8, None) == 1
+    fake = ctypes.c_void_p(0x1000)
+    assert L.bakron_plan_init(8, 8, None, 1 << 20, None) == 1
+    assert L.bakron_plan_init(8, 8, ctypes.c_void_p(0x1004), 1 << 20, None) == 1   # unaligned
+    assert L.bakron_plan_init(8, 8, fake, 16, None) == 1                           # too small
+
+
+ALLOC_CALLS = ("cudaMalloc", "cudaMallocAsync", "cudaMallocManaged", "cudaHostAlloc",
+               "cudaMallocHost", "cudaFree", "cudaFreeHost", "cudaFreeAsync",
+               "cudaDeviceSynchronize")
+
+
+def test_library_source_allocates_no_device_or_pinned_memory():
+    """The ownership rule of the header: the library allocates no device or
+    pinned host memory, keeps none between calls and never synchronises the
+    whole device; every buffer is the caller's (workspace, plan, outputs)."""
+    csrc = os.path.join(ROOT, "kronecker_factored_gptq_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if not f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            continue
+        txt = re.sub(r"//[^\n]*|/\*.*?\*/", "", open(os.path.join(csrc, f)).read(), flags=re.S)
+        for call in ALLOC_CALLS:
+            assert not re.search(r"\b%s\s*\(" % call, txt), "%s calls %s" % (f, call)

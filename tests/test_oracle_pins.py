@@ -538,3 +538,26 @@ def test_rowacc_guide_takes_a_planted_near_tie():
     assert g.codes[0, 0] == 1.0 and g.overrides >= 1
     ref = O.antidiag(W, p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], guide=guide)
     np.testing.assert_array_equal(g.codes, ref.codes)
+
+
+@pytest.mark.parametrize("m,n,rb", [(5, 7, 3), (33, 20, 8), (37, 100, 16), (129, 77, 8)])
+def test_rowacc_row_blocks_equal_antidiagonal_traversal(m, n, rb):
+    """The row-blocked traversal of the C solver (the one the full-size
+    comparisons use) against its anti-diagonal traversal: same codes, and the
+    same pre-rounding values up to the regrouped column sums; with one row
+    per block the two are the same computation, bit for bit."""
+    from oracle.rowacc import rowacc
+    p = problem(m, n, seed=m + 3 * n)
+    a = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"])
+    b = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], rows_per_block=rb)
+    np.testing.assert_array_equal(b.codes, a.codes)
+    np.testing.assert_allclose(b.preround, a.preround, rtol=0, atol=1e-13)
+    one = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], rows_per_block=1)
+    np.testing.assert_array_equal(one.preround, a.preround)
+    ones = np.ones(m, np.float32)
+    u = rowacc(12 * p["W"], p["UA"], p["UB"], ones, rows_per_block=rb)
+    ua = O.antidiag(12 * p["W"], p["UA"], p["UB"], ones)
+    np.testing.assert_array_equal(u.codes, ua.codes)
+    g = rowacc(p["W"], p["UA"], p["UB"], p["s"], p["qmin"], p["qmax"], guide=a.codes, rows_per_block=rb)
+    np.testing.assert_array_equal(g.codes, a.codes)
+    assert g.overrides == 0
