@@ -52,6 +52,9 @@ namespace bakron {
 namespace {
 
 constexpr int T = kTile;
+// Source diagonals the near products reach back (D - kNear .. D - 1); the
+// propagations cover every pair further apart.
+constexpr int kNear = BAKRON_NEAR_DIAGONALS;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -160,12 +163,14 @@ Op build_prop(Schedule& s, int S0, int S1, int T0, int T1, int depth) {
   return op;
 }
 
-// Near products into the tiles of diagonal D from their left and upper
-// neighbours (diagonal D - 1): stage-1 items write Y^T[J, I] (from the left
-// neighbour, K = tile column J - 1) and Y^T[J, I - 1] (from the upper
-// neighbour, K = tile column J, the triangular diagonal block of U_A); the
-// stage-2 item of (I, J) sums U_B^T[I, I''] Y^T[J, I''] over I'' in
-// {I - 1, I}, whichever exist.
+// Near products into the tiles of diagonal D from every tile at most kNear
+// diagonals before it (D - kNear .. D - 1), in the row-accumulator form:
+// for a target (I, J) and each row I'' = I - k (k = 0 .. kNear) the stage-1
+// item writes Y^T[J, I''] over the source columns J' of row I'' with
+// D - kNear <= I'' + J' < D and J' <= J (k = 0: J - kNear .. J - 1; k >= 1:
+// J - kNear + k .. J); the stage-2 item of (I, J) sums U_B^T[I, I''] Y^T[J, I'']
+// over those rows.  Targets of one diagonal sit in distinct columns J, so the
+// Y^T tiles of one launch are distinct.
 Op build_near(Schedule& s, int D) {
   const int M = s.M, N = s.N;
   Op op{};
@@ -180,16 +185,20 @@ Op build_near(Schedule& s, int D) {
   c.off1 = (int)s.items.size();
   for (int I = I0; I <= I1; ++I) {
     const int J = D - I;
-    if (J >= 1) s.items.push_back(WorkItem{J, I, J - 1, J});
-    if (I >= 1) s.items.push_back(WorkItem{J, I - 1, J, J + 1});
+    for (int k = 0; k <= kNear && I - k >= 0; ++k) {
+      const int j0 = std::max(0, k == 0 ? J - kNear : J - kNear + k);
+      const int j1 = k == 0 ? J : J + 1;   // exclusive
+      if (j1 <= j0) continue;
+      s.items.push_back(WorkItem{J, I - k, j0, j1});
+      c.flops1 += 2.0 * T * T * T * (j1 - j0);
+      c.maxk1 = std::max(c.maxk1, j1 - j0);
+    }
   }
   c.n1 = (int)s.items.size() - c.off1;
-  c.maxk1 = c.n1 > 0 ? 1 : 0;
-  c.flops1 = 2.0 * T * T * T * c.n1;
   c.off = (int)s.items.size();
   for (int I = I0; I <= I1; ++I) {
     const int J = D - I;
-    const int k0 = I >= 1 ? I - 1 : I, k1 = J >= 1 ? I + 1 : I;
+    const int k0 = std::max(0, I - kNear), k1 = J >= 1 ? I + 1 : I;
     if (k1 <= k0) continue;
     s.items.push_back(WorkItem{I, J, k0, k1});
     c.flops += 2.0 * T * T * T * (k1 - k0);
@@ -206,7 +215,7 @@ void build_rec(Schedule& s, int D0, int D1, int depth, std::vector<Op>& prop_aft
   if (D1 - D0 <= 1) return;
   const int Dm = (D0 + D1) / 2;
   build_rec(s, D0, Dm, depth + 1, prop_after);
-  const int S0 = std::max(D0 - 1, 0), S1 = Dm - 1;
+  const int S0 = std::max(D0 - kNear, 0), S1 = Dm - kNear;
   if (S1 > S0) prop_after[S1 - 1] = build_prop(s, S0, S1, Dm, D1, depth);
   build_rec(s, Dm, D1, depth + 1, prop_after);
 }

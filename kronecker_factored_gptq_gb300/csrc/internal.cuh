@@ -13,6 +13,14 @@ namespace bakron {
 
 constexpr int kTile = 128;          // tile edge T of the solver
 
+// Tile anti-diagonals the near products of the solve reach back: the errors of
+// diagonals D - BAKRON_NEAR_DIAGONALS .. D - 1 reach diagonal D on the
+// critical stream right before its leaf, every older diagonal's through a
+// propagation that runs beside the leaves in between.
+#ifndef BAKRON_NEAR_DIAGONALS
+#define BAKRON_NEAR_DIAGONALS 1
+#endif
+
 // Largest problems the entry points accept: at most kMaxTiles 128-tiles of W
 // (m n <= 2^34 elements, 64 GiB in fp32) and factor orders up to kMaxOrder.
 // The host work lists then stay below a few hundred MB, and no single GPU

@@ -309,30 +309,31 @@ def test_solve_streams_without_the_propagation_wait_overlap():
     assert bad and all(b[0][0] == "W" for b in bad)
 
 
-def test_solve_near_products_only_between_neighbours():
-    """Every pair of tiles on neighbouring diagonals goes through the near
-    products and only those; no propagation waits between two leaves on the
-    critical stream."""
-    M, N = 9, 7
+@pytest.mark.parametrize("M,N", [(9, 7), (4, 4), (16, 13)])
+def test_solve_near_products_reach_a_fixed_depth(M, N):
+    """The near products issued between leaf D - 1 and leaf D read the
+    diagonals D - h .. D - 1 (h the same for every D) and write only diagonal
+    D; every propagation's sources are at least h + 1 diagonals before its
+    first target, so it can start h leaves early; no propagation sits
+    between two leaves on the critical stream."""
     ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
-    # on the critical stream only near products and leaves alternate
     crit = [int(k) for k in ops[:, 0] if k != 1]
     assert crit == [0] + [2, 0] * (M + N - 2)
+    depth = set()
     for kind, D, _, _, _, chunk0, nchunks in ops.tolist():
         if kind != 2:
             continue
         dlo, dhi, off1, n1, off, nn = chunks[chunk0].tolist()
-        for Jp, I, k0, k1 in items[off1:off1 + n1].tolist():
-            assert k1 - k0 == 1 and I + k0 == D - 1, "near stage 1 reads diagonal D - 1 only"
+        src = [I + J for Jp, I, k0, k1 in items[off1:off1 + n1].tolist() for J in range(k0, k1)]
+        assert src and max(src) <= D - 1
+        depth.add(D - min(src))
         for Ip, Jp, k0, k1 in items[off:off + nn].tolist():
             assert Ip + Jp == D
-    # a propagation never reads a source one diagonal before one of its targets
-    for kind, D, s0, s1, depth, chunk0, nchunks in ops.tolist():
-        if kind != 1:
-            continue
-        for c in range(nchunks):
-            dlo = int(chunks[chunk0 + c][0])
-            assert dlo >= s1 + 1
+    h = max(depth)
+    assert h >= 1 and all(d == min(h, D) for d, D in zip(sorted(depth), sorted(depth)))
+    for kind, D, s0, s1, _, chunk0, nchunks in ops.tolist():
+        if kind == 1:
+            assert all(int(chunks[chunk0 + c][0]) >= s1 + h for c in range(nchunks))
 
 
 @pytest.mark.parametrize("M,N", [(1, 1), (3, 1), (1, 7), (4, 5), (9, 16), (6, 33), (64, 64), (32, 112)])
