@@ -52,6 +52,14 @@ namespace bakron {
 namespace {
 
 constexpr int T = kTile;
+// Propagation lanes (a Y^T buffer pair and three streams each).
+constexpr int kMaxDepth = 24;
+// A propagation chunk whose first target is at most this many leaves after
+// the propagation's start runs at middle priority, a later one at the lowest.
+#ifndef BAKRON_MID_SLACK
+#define BAKRON_MID_SLACK 15
+#endif
+constexpr int kMidSlack = BAKRON_MID_SLACK;
 // Source diagonals the near products reach back (D - kNear .. D - 1); the
 // propagations cover every pair further apart.
 constexpr int kNear = BAKRON_NEAR_DIAGONALS;
@@ -74,7 +82,7 @@ struct Op {
                            // its last source diagonal (after whose leaf it starts)
   int I0, ntiles;          // leaf: first row tile and tile count
   int s0, s1;              // propagation: source diagonals [s0, s1)
-  int depth;               // propagation: recursion depth (Y buffer, streams)
+  int depth;               // propagation: its lane (Y^T buffer and streams)
   int chunk0, nchunks;     // near: one chunk; propagation: its chunks
 };
 
@@ -210,29 +218,82 @@ Op build_near(Schedule& s, int D) {
 }
 
 // The propagations of the recursion, each filed under its last source
-// diagonal (at most one per diagonal: every split point is distinct).
-void build_rec(Schedule& s, int D0, int D1, int depth, std::vector<Op>& prop_after) {
+// diagonal.  A wide source band is split into parts of about kSplitWidth
+// diagonals, propagated separately: the pairs are partitioned by source, so
+// each still reaches every target once, and each part starts right after the
+// leaf of its own last source.  The first part of the top-level band can
+// then run beside dozens of leaves instead of one; the price is the
+// stage-2 work repeated per part.
+#ifndef BAKRON_SPLIT_WIDTH
+#define BAKRON_SPLIT_WIDTH 0
+#endif
+constexpr int kSplitWidth = BAKRON_SPLIT_WIDTH;   // 0: no split
+
+void build_rec(Schedule& s, int D0, int D1, int depth, std::vector<std::vector<Op>>& prop_after,
+               bool split) {
   if (D1 - D0 <= 1) return;
   const int Dm = (D0 + D1) / 2;
-  build_rec(s, D0, Dm, depth + 1, prop_after);
+  build_rec(s, D0, Dm, depth + 1, prop_after, split);
   const int S0 = std::max(D0 - kNear, 0), S1 = Dm - kNear;
-  if (S1 > S0) prop_after[S1 - 1] = build_prop(s, S0, S1, Dm, D1, depth);
-  build_rec(s, Dm, D1, depth + 1, prop_after);
+  if (S1 > S0) {
+    const int w = S1 - S0;
+    const int width = kSplitWidth > 0 ? kSplitWidth : 1;
+    const int parts = split && kSplitWidth > 0 ? std::min(4, std::max(1, (w + width / 2) / width)) : 1;
+    for (int p = 0; p < parts; ++p) {
+      const int a = S0 + (int)((int64_t)w * p / parts), b = S0 + (int)((int64_t)w * (p + 1) / parts);
+      if (b > a) prop_after[b - 1].push_back(build_prop(s, a, b, Dm, D1, depth));
+    }
+  }
+  build_rec(s, Dm, D1, depth + 1, prop_after, split);
 }
 
-void build_schedule(Schedule& s) {
-  const int ND = s.M + s.N - 1;
-  std::vector<Op> prop_after(ND, Op{-1});
-  build_rec(s, 0, ND, 0, prop_after);
-  for (int D = 0; D < ND; ++D) {
-    if (D >= 1) s.ops.push_back(build_near(s, D));
-    Op leaf{};
-    leaf.kind = 0;
-    leaf.D = D;
-    leaf.I0 = std::max(0, D - s.N + 1);
-    leaf.ntiles = std::min(D, s.M - 1) - leaf.I0 + 1;
-    s.ops.push_back(leaf);
-    if (prop_after[D].kind == 1) s.ops.push_back(prop_after[D]);
+// Y^T buffer and stream pair of each propagation ("lane", kept in Op.depth):
+// the lowest lane whose previous propagation has finished.  A propagation's
+// chunks all complete before the leaf of the last chunk's first target, and
+// a propagation starts after the leaf of its last source, so a lane is free
+// for a propagation starting after leaf D once its previous one's last chunk
+// targets a diagonal <= D.  Returns false if more than kMaxLanes are needed.
+bool assign_lanes(Schedule& s, int max_lanes) {
+  std::vector<int> free_at;   // per lane: first leaf after which it is free
+  int top = 0;
+  for (Op& op : s.ops) {
+    if (op.kind != 1) continue;
+    int lane = -1;
+    for (int l = 0; l < (int)free_at.size(); ++l)
+      if (free_at[l] <= op.D) { lane = l; break; }
+    if (lane < 0) {
+      lane = (int)free_at.size();
+      if (lane >= max_lanes) return false;
+      free_at.push_back(0);
+    }
+    op.depth = lane;
+    free_at[lane] = s.chunks[op.chunk0 + op.nchunks - 1].dlo;
+    top = std::max(top, lane);
+  }
+  s.max_depth = top;
+  return true;
+}
+
+void build_schedule(Schedule& s, int max_lanes) {
+  for (int split = 1; split >= 0; --split) {
+    s.items.clear();
+    s.ops.clear();
+    s.chunks.clear();
+    s.max_depth = 0;
+    const int ND = s.M + s.N - 1;
+    std::vector<std::vector<Op>> prop_after(ND);
+    build_rec(s, 0, ND, 0, prop_after, split != 0);
+    for (int D = 0; D < ND; ++D) {
+      if (D >= 1) s.ops.push_back(build_near(s, D));
+      Op leaf{};
+      leaf.kind = 0;
+      leaf.D = D;
+      leaf.I0 = std::max(0, D - s.N + 1);
+      leaf.ntiles = std::min(D, s.M - 1) - leaf.I0 + 1;
+      s.ops.push_back(leaf);
+      for (const Op& op : prop_after[D]) s.ops.push_back(op);
+    }
+    if (assign_lanes(s, max_lanes)) return;
   }
 }
 
@@ -279,7 +340,7 @@ const Schedule& get_schedule(int M, int N) {
   Schedule s;
   s.M = M;
   s.N = N;
-  build_schedule(s);
+  build_schedule(s, kMaxDepth);
   return cache.emplace(key, std::move(s)).first->second;
 }
 
@@ -371,8 +432,6 @@ size_t plan_bytes(int M, int N) {
   return kPlanHeaderBytes +
          sizeof(WorkItem) * (get_schedule(M, N).items.size() + get_rows_schedule(M, N).items.size());
 }
-
-constexpr int kMaxDepth = 24;
 
 struct QLayout {
   int64_t M, N, Mp, Np;
@@ -523,14 +582,15 @@ cudaError_t prep_events(PrepStreams* ps, size_t n) {
 }
 
 // Streams of the solve, per device, created once: a high-priority critical
-// stream (leaves, near products; the one-sided path's urgent chunks), per
-// recursion depth an urgent stream (the first chunk of a propagation, what
-// the next leaves wait for) just below it in priority and a low-priority side
-// stream (the other chunks), plus a pool of reusable events.  Calls are
+// stream (leaves, near products; the one-sided path's urgent chunks) and per
+// propagation lane an urgent stream (the chunk the next leaf waits for) just
+// below it in priority, a middle-priority and a lowest-priority stream (the
+// chunks due later), plus a pool of reusable events.  Calls are
 // synchronous, so the pool is reused per call.
 struct SolveStreams {
   cudaStream_t crit = nullptr;
   cudaStream_t urg[kMaxDepth] = {};
+  cudaStream_t mid[kMaxDepth] = {};
   cudaStream_t side[kMaxDepth] = {};
   std::vector<cudaEvent_t> events;
   std::mutex mu;
@@ -555,22 +615,26 @@ cudaError_t solve_streams(SolveStreams** out, int slot = 0) {
     // greater priority = smaller number; urgent chunks one step below the
     // critical stream when the device has the levels
     const int urg = hi < lo ? hi + 1 : hi;
-    cudaStream_t c = nullptr, u[kMaxDepth] = {}, sd[kMaxDepth] = {};
+    const int mid = (urg + lo) / 2;
+    cudaStream_t c = nullptr, u[kMaxDepth] = {}, md[kMaxDepth] = {}, sd[kMaxDepth] = {};
     e = cudaStreamCreateWithPriority(&c, cudaStreamNonBlocking, hi);
     for (int d = 0; d < kMaxDepth && e == cudaSuccess; ++d) {
       e = cudaStreamCreateWithPriority(&u[d], cudaStreamNonBlocking, urg);
+      if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&md[d], cudaStreamNonBlocking, mid);
       if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&sd[d], cudaStreamNonBlocking, lo);
     }
     if (e != cudaSuccess) {
       if (c) cudaStreamDestroy(c);
       for (int d = 0; d < kMaxDepth; ++d) {
         if (u[d]) cudaStreamDestroy(u[d]);
+        if (md[d]) cudaStreamDestroy(md[d]);
         if (sd[d]) cudaStreamDestroy(sd[d]);
       }
       return e;
     }
     for (int d = 0; d < kMaxDepth; ++d) {
       ss.urg[d] = u[d];
+      ss.mid[d] = md[d];
       ss.side[d] = sd[d];
     }
     ss.crit = c;
@@ -586,6 +650,7 @@ void drain_solve_streams(SolveStreams* ss) {
   cudaStreamSynchronize(ss->crit);
   for (int d = 0; d < kMaxDepth; ++d) {
     cudaStreamSynchronize(ss->urg[d]);
+    cudaStreamSynchronize(ss->mid[d]);
     cudaStreamSynchronize(ss->side[d]);
   }
 }
@@ -1265,24 +1330,38 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
       // chunk's stage 1 (they read its Y^T tiles too)
       float* yhi = (float*)(base + L.yhi[op.depth]);
       float* ylo = (float*)(base + L.ylo[op.depth]);
-      cudaStream_t us = ss->urg[op.depth], ds = ss->side[op.depth];
-      if ((e = cudaStreamWaitEvent(us, ev_leaf, 0)) != cudaSuccess) return e;
-      cudaEvent_t ev_s1 = nullptr;
+      // Each chunk goes to a stream of the propagation's lane chosen by its
+      // slack, the leaves between the propagation's start (after leaf op.D)
+      // and its first target: the next leaf's chunk to the urgent stream, the
+      // chunks due within kMidSlack leaves to a middle-priority stream, the
+      // rest to the lowest; so far-off chunks of a large propagation cannot
+      // hold the SMs that a near deadline needs.  A chunk's stage 2 reads the
+      // Y^T tiles of every earlier chunk's stage 1: it waits for those on
+      // other streams.
+      cudaStream_t lane_str[3] = {ss->urg[op.depth], ss->mid[op.depth], ss->side[op.depth]};
+      bool started[3] = {false, false, false};
+      cudaEvent_t s1_ev[3] = {nullptr, nullptr, nullptr};   // latest stage 1 per stream
       for (int c = 0; c < op.nchunks; ++c) {
         const Chunk& ch = sch.chunks[op.chunk0 + c];
         if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
-        cudaStream_t cstr = c == 0 ? us : ds;
-        if (c == 1 && (e = cudaStreamWaitEvent(ds, ev_s1, 0)) != cudaSuccess) return e;
+        const int slack = ch.dlo - op.D - 1;
+        const int k = slack <= 1 ? 0 : (slack <= kMidSlack ? 1 : 2);
+        cudaStream_t cstr = lane_str[k];
+        if (!started[k]) {
+          if ((e = cudaStreamWaitEvent(cstr, ev_leaf, 0)) != cudaSuccess) return e;
+          started[k] = true;
+        }
         if (ch.n1 > 0) {
           cudaEvent_t ev = pt.begin(cstr);
           if ((e = launch(stage1(yhi, ylo), ch.off1, ch.n1, ch.maxk1, cstr)) != cudaSuccess) return e;
           pt.end(1, ev, cstr);
-        }
-        if (c == 0 && op.nchunks > 1) {
-          if ((e = next_event(&ev_s1)) != cudaSuccess) return e;
-          if ((e = cudaEventRecord(ev_s1, us)) != cudaSuccess) return e;
+          if ((e = next_event(&s1_ev[k])) != cudaSuccess) return e;
+          if ((e = cudaEventRecord(s1_ev[k], cstr)) != cudaSuccess) return e;
         }
         if (ch.n > 0) {
+          for (int k2 = 0; k2 < 3; ++k2)
+            if (k2 != k && s1_ev[k2] && (e = cudaStreamWaitEvent(cstr, s1_ev[k2], 0)) != cudaSuccess)
+              return e;
           // after the earlier updates of the same W~ tiles (fixed order)
           if ((e = pending.order_before(cstr, ch.dlo, ch.dhi)) != cudaSuccess) return e;
           cudaEvent_t ev = pt.begin(cstr);

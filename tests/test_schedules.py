@@ -15,12 +15,12 @@ Preparation: the blocked Cholesky's trailing updates and the
 recursive-doubling inverse.
 
 The stream model mirrors the executor's rules in csrc/api.cu: leaves and near
-products on the critical stream; a propagation's first chunk on its depth's
-urgent stream after the leaf before it, the other chunks on its depth's side
-stream after the first chunk's stage 1; every chunk's stage 2 after the
-chunks enqueued earlier that update any of the same diagonals, and every
-near product and leaf after the chunks that update its diagonal (each event
-waited for once).  The checks then require every update of a W~ tile (so
+products on the critical stream; a propagation's chunks on its lane's urgent,
+middle or lowest-priority stream by their slack, each stream starting after
+the leaf before the propagation; every chunk's stage 2 after the earlier
+chunks' stage 1 on the other streams and after the chunks enqueued earlier
+that update any of the same diagonals, and every near product and leaf after
+the chunks that update its diagonal.  The checks then require every update of a W~ tile (so
 their fp32 order is fixed), every Y tile's writer and readers, and every E
 tile's producer and readers to be ordered by stream order and events.
 """
@@ -87,6 +87,9 @@ class Streams:
 
     def before(self, a, b):
         return bool((self.anc[b] >> a) & 1)
+
+
+MID_SLACK = 15   # the executor's middle-priority bound (csrc/api.cu, kMidSlack)
 
 
 def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
@@ -168,19 +171,26 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
                 if c > 0:
                     pending.append((S.record(stream), dlo, dhi))
             continue
-        us, ds = "urg%d" % depth, "side%d" % depth
-        S.wait(us, ev_leaf)
-        ev_s1 = None
+        # the chunk's stream by its slack (leaves between the propagation's
+        # start, after leaf D, and its first target), as the executor does
+        streams = ["urg%d" % depth, "mid%d" % depth, "side%d" % depth]
+        started = [False, False, False]
+        s1ev = [None, None, None]
         for c in range(nchunks):
             dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
-            stream = us if c == 0 else ds
-            if c == 1:
-                S.wait(ds, ev_s1)
+            slack = dlo - D - 1
+            k = 0 if slack <= 1 else (1 if slack <= MID_SLACK else 2)
+            stream = streams[k]
+            if not started[k]:
+                S.wait(stream, ev_leaf)
+                started[k] = True
             if n1 > 0:
                 stage1(stream, depth, items[off1:off1 + n1].tolist())
-            if c == 0 and nchunks > 1:
-                ev_s1 = S.record(us)
+                s1ev[k] = S.record(stream)
             if nn > 0:
+                for k2 in range(3):
+                    if k2 != k and s1ev[k2] is not None:
+                        S.wait(stream, s1ev[k2])
                 if wait_at_propagation:
                     order_before(stream, dlo, dhi)
                 stage2(stream, depth, items[off:off + nn].tolist())
