@@ -36,13 +36,11 @@
 // Every mbarrier wait is bounded (clock64 budget); on expiry the CTA records
 // BAKRON_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs (with a
 // bound again), frees TMEM and returns.
-#include <cuda.h>
-
-#include <mutex>
-
-#include "internal.cuh"
+#include "tc_common.cuh"
 
 namespace bakron {
+
+using namespace tc;
 
 namespace {
 constexpr int BM = 128, BN = 128, BKF = 32;      // tile rows, cols, K slice (floats)
@@ -55,92 +53,9 @@ constexpr int SPC = kTile / BKF;                 // K slices per accumulation ch
 constexpr int NTHREADS = 256;
 constexpr int SPITCH = BN + 4;                   // epilogue staging pitch (floats)
 static_assert(4 * 32 * SPITCH * 4 <= STAGES * STAGE_BYTES, "epilogue staging fits the ring");
-constexpr long long kBudget = 400000000LL;       // ~0.2 s of SM clock per wait
 
-// instruction descriptor, kind::tf32: D fp32, A/B tf32, both K-major, M=N=128
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = tc::idesc_tf32(BM, BN);
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait; false on timeout or when another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if (clock64() - t0 > kBudget) return false;
-  }
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (SBO), start address in 16-byte units.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
-  d |= (uint64_t)1 << 46;             // descriptor version
-  d |= (uint64_t)2 << 61;             // 128-byte swizzle
-  return d;
-}
-__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_before_sync() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after_sync() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 }  // namespace
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -257,9 +172,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int j = 0; j < BKF / 8; ++j) {
         const uint64_t o = (uint64_t)(j * 32 >> 4);  // 8 tf32 = 32 bytes along K
         const uint32_t acc = (first && j == 0) ? 0u : 1u;
-        mma_tf32(tm_main, ahi + o, bhi + o, acc);
-        mma_tf32(tm_corr, ahi + o, blo + o, acc);
-        mma_tf32(tm_corr, alo + o, bhi + o, 1u);
+        mma_tf32(tm_main, ahi + o, bhi + o, kIdesc, acc);
+        mma_tf32(tm_corr, ahi + o, blo + o, kIdesc, acc);
+        mma_tf32(tm_corr, alo + o, bhi + o, kIdesc, 1u);
       }
       mma_commit(smem_u32(&bar_empty[s]));
       if ((i % SPC) == SPC - 1) mma_commit(smem_u32(&acc_full[b]));
@@ -382,6 +297,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+namespace tc {
 namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -402,8 +318,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// rows x cols fp32 row-major matrix with leading dimension ld (floats);
-// box = 32 columns (128 bytes) x 128 rows, 128-byte swizzle.
+}  // namespace
+
+bool encode_available() { return encode_fn() != nullptr; }
+
 bool make_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ld) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -415,7 +333,7 @@ bool make_map(CUtensorMap* m, const float* ptr, int64_t rows, int64_t ld) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-}  // namespace
+}  // namespace tc
 
 bool prop_tc_supported() {
   static std::atomic<int> cached{-1};
@@ -425,7 +343,7 @@ bool prop_tc_supported() {
   bool ok = cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
-            major == 10 && minor == 3 && encode_fn() != nullptr;
+            major == 10 && minor == 3 && tc::encode_available();
   if (!ok) (void)cudaGetLastError();
   cached.store(ok ? 1 : 0, std::memory_order_release);
   return ok;
