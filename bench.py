@@ -766,6 +766,28 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_solve(args):
+    """One warm-up step of the configuration, then one solve inside the NVTX
+    range "solve" (for ncu's --nvtx-include "solve/"); prints one line."""
+    import torch
+    from kronecker_factored_gptq_gb300 import bakron as kb
+    from kronecker_factored_gptq_gb300 import workloads as WL
+    if not os.path.exists(kb.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    w = WL.load(args.config, seed=args.seed, device="cuda")
+    dW, dA, dB = (torch.from_numpy(x).cuda() for x in (w.W, w.A, w.B))
+    solver = kb.Solver(w.m, w.n, bits=w.bits)
+    solver.solve(dW, dA, w.damp_A, dB, w.damp_B)
+    torch.cuda.synchronize()
+    n0 = kb.kernel_launches()
+    torch.cuda.nvtx.range_push("solve")
+    solver.quantize(dW)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    print(json.dumps({"profile_solve": w.name, "launches": kb.kernel_launches() - n0}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -784,7 +806,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the context timings (one-sided GPTQ, factor accumulation)")
+    ap.add_argument("--profile-solve", action="store_true",
+                    help="profiling helper: one warm-up step, then one solve in the NVTX range "
+                         "'solve'; no benchmark line")
     args = ap.parse_args()
+    if args.profile_solve:
+        run_profile_solve(args)
+        return
     if args.sample is None:
         args.sample = 2048 if args.impl == "reference" else 4096
     if args.impl == "reference":
