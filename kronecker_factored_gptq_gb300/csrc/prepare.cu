@@ -420,11 +420,20 @@ namespace {
 // Largest launch of the inverse's products while the chain runs.
 constexpr int kInvChunk = 1 << 20;
 
+// Trailing updates far from the chain are applied kSyrkBatch panels at a
+// time (one product of K = kSyrkBatch tiles instead of kSyrkBatch products of
+// one tile each); see prep_items.
+#ifndef BAKRON_SYRK_BATCH
+#define BAKRON_SYRK_BATCH 4
+#endif
+constexpr int kSyrkBatch = BAKRON_SYRK_BATCH;
+
 struct PrepItems {
   std::vector<WorkItem> items;
   // per kb: the urgent tile (kb+1, kb+1) at syrk_off, then syrk_n1 tiles of
-  // column kb+1 and tile (kb+2, kb+2), then syrk_n2 other tiles
-  std::vector<int> syrk_off, syrk_n1, syrk_n2;
+  // column kb+1 and tile (kb+2, kb+2), then syrk_n2 other tiles (longest K
+  // first), syrk_k2 the longest K of those
+  std::vector<int> syrk_off, syrk_n1, syrk_n2, syrk_k2;
   // recursive doubling of G^{-1}: per level (block size B = 2^level) and per
   // pair of neighbouring blocks [p0, p0 + B), [p0 + B, e2) (p = p0 / 2B), the
   // items of T = (G21 Ginv11)^T and of Ginv21 = -Ginv22 T^T
@@ -449,11 +458,25 @@ const PrepItems& prep_items(int64_t kp) {
     for (int r = kb + 2; r < nb; ++r) P.items.push_back(WorkItem{r, kb + 1, kb, kb + 1});
     if (kb + 2 < nb) P.items.push_back(WorkItem{kb + 2, kb + 2, kb, kb + 1});
     P.syrk_n1.push_back((int)(P.items.size() - s1));
+    // S2: panel kb into the tiles of columns kb+2 .. cmax one by one (the
+    // columns the chain reaches within the next batch); the tiles of columns
+    // beyond cmax take the panels of batch b = kb / kSyrkBatch together, once
+    // its last panel is done (at kb = (b+1) kSyrkBatch - 1), at least
+    // kSyrkBatch steps before the chain needs them.  Every (tile, panel)
+    // pair once: panel j reaches column c >= j + 2 singly if
+    // c <= (j / kSyrkBatch + 2) kSyrkBatch, else in its batch.
     const size_t s2 = P.items.size();
+    const int bt = kb / kSyrkBatch;
+    const int cmax = (bt + 2) * kSyrkBatch;
+    const bool batch_end = (kb + 1) % kSyrkBatch == 0;
+    if (batch_end)
+      for (int r = cmax + 1; r < nb; ++r)
+        for (int c = cmax + 1; c <= r; ++c) P.items.push_back(WorkItem{r, c, bt * kSyrkBatch, kb + 1});
     for (int r = kb + 3; r < nb; ++r)
-      for (int c = kb + 2; c <= r; ++c)
+      for (int c = kb + 2; c <= std::min(r, cmax); ++c)
         if (!(r == kb + 2 && c == kb + 2)) P.items.push_back(WorkItem{r, c, kb, kb + 1});
     P.syrk_n2.push_back((int)(P.items.size() - s2));
+    P.syrk_k2.push_back(batch_end && cmax + 1 < nb ? kSyrkBatch : 1);
   }
   for (int B = 1; B < nb; B *= 2) {
     P.pairs.emplace_back();
@@ -528,7 +551,8 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
   // Lookahead stream: the rest of step kb's panel, then S1(kb) = the
   // trailing tiles of column kb+1 and tile (kb+2, kb+2) (what step kb+1
   // reads).  Bulk stream (lowest priority): S2(kb) = the other trailing
-  // tiles, needed two steps later.  Every tile receives its updates in a
+  // tiles, needed two or more steps later (the far ones in batches of
+  // kSyrkBatch panels, see prep_items).  Every tile receives its updates in a
   // fixed order (S2 of earlier steps, then S1, then the urgent update), so
   // the result is the same bit for bit on every run: S1(kb) waits for
   // S2(kb-1), and step kb's urgent part waits for S1(kb-1).  Events per
@@ -633,14 +657,14 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
                            a.Clo + off + r0 * kp);
     };
     // trailing update C22 -= P P^T over syrk items [i0, i0 + n) (tensor cores)
-    auto syrk = [&](int i0, int n, cudaStream_t str, bool pdl) -> cudaError_t {
+    auto syrk = [&](int i0, int n, cudaStream_t str, bool pdl, int maxk = 1) -> cudaError_t {
       if (n <= 0) return cudaSuccess;
       PropArgs q{};
       q.pdl = pdl;
       q.A_hi = a.Chi; q.A_lo = a.Clo; q.lda = kp; q.a_rows = kp;
       q.B_hi = a.Chi; q.B_lo = a.Clo; q.ldb = kp; q.b_rows = kp;
       q.wt = a.C; q.ldw = kp;
-      q.items = items + i0; q.n_items = n; q.max_k = 1;
+      q.items = items + i0; q.n_items = n; q.max_k = maxk;
       q.stage = 2;
       q.st = a.st;
       return launch_prop_tc(q, str);
@@ -661,7 +685,7 @@ cudaError_t run_prepare_factor(const PrepareFactorArgs& a, cudaStream_t s) {
     BK_TRY(cudaEventRecord(ev_s1, a.side));
     // bulk stream: S2(kb) (reads the panel rows below kb+1 only)
     BK_TRY(cudaStreamWaitEvent(a.bulk, ev_pan, 0));
-    BK_TRY(syrk(PI.syrk_off[kb] + 1 + PI.syrk_n1[kb], PI.syrk_n2[kb], a.bulk, false));
+    BK_TRY(syrk(PI.syrk_off[kb] + 1 + PI.syrk_n1[kb], PI.syrk_n2[kb], a.bulk, false, PI.syrk_k2[kb]));
     BK_TRY(cudaEventRecord(ev_s2, a.bulk));
     // inverse stream: block kb's inverse, the pairs it closes, then the
     // pairs whose first range it ends (their panels are final at ev_pan)

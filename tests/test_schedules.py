@@ -373,6 +373,14 @@ def test_rows_schedule(M, N):
 
 @pytest.mark.parametrize("nb", [1, 2, 3, 5, 8, 13, 17, 64, 112])
 def test_prepare_trailing_updates_once_in_groups(nb):
+    """Right-looking blocked Cholesky: every trailing tile (r, c) receives
+    every panel j < c exactly once, after panel j is done (step >= j) and
+    before the chain needs the tile (the step that reads column c is c - 1:
+    the urgent tile and the lookahead group of step j are exactly what
+    steps j + 1 and j + 2 read).  Panels reach a far tile singly or in a
+    batch of consecutive panels (one product over their K range), applied
+    at a step >= the batch's last panel and at least two steps before the
+    tile's column is read."""
     syrk, levels, items = parse_prepare(kb.schedule_export(kb.SCHEDULE_PREPARE, nb))
     seen = {}
     for j in range(nb):
@@ -380,19 +388,26 @@ def test_prepare_trailing_updates_once_in_groups(nb):
         grp = [items[off:off + 1] if j + 1 < nb else items[off:off]]
         grp.append(items[off + 1:off + 1 + n1])
         grp.append(items[off + 1 + n1:off + 1 + n1 + n2])
-        urgent, s1, s2 = ({(int(r), int(c)) for r, c, k0, k1 in g} for g in grp)
-        for g in grp:
-            for r, c, k0, k1 in g:
-                assert (k0, k1) == (j, j + 1), "one panel per trailing update"
-                key = (int(r), int(c), j)
-                assert key not in seen
-                seen[key] = True
-        # the urgent tile is what the next diagonal block reads, the
-        # lookahead group what the next step's panel reads
+        urgent, s1 = ({(int(r), int(c)) for r, c, k0, k1 in g} for g in grp[:2])
+        for gi, g in enumerate(grp):
+            for r, c, k0, k1 in g.tolist():
+                assert 0 <= k0 < k1 <= j + 1, "a panel that is not done yet"
+                if gi < 2:
+                    assert (k0, k1) == (j, j + 1), "one panel per urgent / lookahead update"
+                else:
+                    assert k1 - k0 == 1 or k1 == j + 1, "a batch ends with this step's panel"
+                    assert c - 1 >= j + 2 or k1 - k0 == 1, "a batched tile is read two steps later"
+                for p in range(k0, k1):
+                    key = (r, c, p)
+                    assert key not in seen, key
+                    seen[key] = True
         assert urgent == ({(j + 1, j + 1)} if j + 1 < nb else set())
         want1 = {(r, j + 1) for r in range(j + 2, nb)} | ({(j + 2, j + 2)} if j + 2 < nb else set())
         assert s1 == want1
-        assert s2 == {(r, c) for r in range(j + 3, nb) for c in range(j + 2, r + 1)}
+        # the bulk group never touches what the urgent or lookahead groups of
+        # this step hold, nor a column the chain already passed
+        for r, c, k0, k1 in grp[2].tolist():
+            assert c >= j + 2 and (r, c) != (j + 2, j + 2)
     want = {(r, c, j) for c in range(nb) for r in range(c, nb) for j in range(c)}
     assert set(seen) == want
 
