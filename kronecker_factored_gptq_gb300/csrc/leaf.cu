@@ -36,10 +36,13 @@
 // registers; r(a-1, b), completed by the row above in the previous step,
 // arrives by a warp shuffle; the older r(a', b) of the rows above are read
 // from shared memory (rT[b][a'], 16-byte loads); the pending r(a, b'') of the lane's own
-// row live in a register window FR[j] = r(a, b0 + j), b0 = 4 kb - a, shifted
-// by four registers every four steps (the step loop is unrolled by four, so
-// every register index is static); the diagonal-major copy
-// Dg[b][t] = Ua(b, b + t) makes the row update a run of 16-byte loads.
+// row live in registers FR[j] = r(a, j - a) (the step loop is unrolled
+// completely, so every register index is static and a register lives only
+// between the steps that use it); the diagonal-major copy
+// Dg[b][t] = Ua(b, b + t) makes the row update a run of 16-byte loads.  With
+// the step d static, the work of a step is cut to what its active lanes
+// (rows d - S + 1 .. d) can use: the row update to t <= 2 S - 2 - d, the
+// look-ahead to the rows a' <= d - 1.
 #include "internal.cuh"
 
 namespace bakron {
@@ -55,7 +58,7 @@ template <int S>
 struct Cfg {
   static constexpr int NB = T / S;          // blocks per tile edge
   static constexpr int BPW = 32 / S;        // blocks per warp in a sweep
-  static constexpr int NF = S + 3;          // row-accumulator window
+  static constexpr int NF = 2 * S - 1;      // row accumulators, by step index
   static constexpr int PX = T + 4;          // tile pitch
   static constexpr int PP = S + 1;          // P^T block pitch
   static constexpr int PR = S + 4;          // rT pitch (16-byte rows)
@@ -73,7 +76,8 @@ struct Cfg {
   static constexpr int OFF_UA = OFF_D + NB * S * PD;
   static constexpr int OFF_UB = OFF_UA + NUA * S * PU;
   static constexpr int OFF_LA = OFF_UB + NUB * S * PU;
-  static constexpr int OFF_CS = OFF_LA + T;                  // NB x [S][PC] int8 codes
+  static constexpr int OFF_LB = OFF_LA + T;
+  static constexpr int OFF_CS = OFF_LB + T;                  // NB x [S][PC] int8 codes
   static constexpr int SMEM_FLOATS = OFF_CS + NB * S * PC / 4;
   static constexpr size_t SMEM = sizeof(float) * (size_t)SMEM_FLOATS;
   // block products: one warp, OPT outputs per lane (RPT rows x CPT columns)
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   float* UaO = smem + K::OFF_UA;  // NUA x [S][PU]: Ua(SJ+b, SJ2+b2) at [b2][b]
   float* UbB = smem + K::OFF_UB;  // NUB x [S][PU]: Ub(SI+a, SI2+a2) at [a2][a]
   float* lA = smem + K::OFF_LA;   // [T]: 1 / Ua(b, b)
+  float* lB = smem + K::OFF_LB;   // [T]: 1 / Ub(a, a)
   signed char* CS = reinterpret_cast<signed char*>(smem + K::OFF_CS);  // NB x [S][PC] codes
 
   const int tid = threadIdx.x;
@@ -278,6 +283,9 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   if (tid < T) {
     const int J = tid / S, b = tid % S;
     lA[tid] = 1.f / stage[J * S * PU + b * PU + b];
+  } else if (tid < 2 * T) {
+    const int I = (tid - T) / S, r = (tid - T) % S;
+    lB[tid - T] = 1.f / UbB[K::ub_idx(I, I) * S * PU + r * PU + r];
   }
   __syncthreads();
   for (int idx = tid; idx < NB * (NB - 1) * S * PP; idx += NTHR) Pt[idx] = 0.f;
@@ -293,12 +301,35 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   const float fqmin = (float)a.qmin, fqmax = (float)a.qmax;
   bool nonfinite = false, out_of_range = false;
 
+  // Grid scale and zero point of the row and block this thread sweeps at
+  // level kk (lane = (sub, row) of block slot BPW warp + sub; a slot past
+  // the level's blocks takes the level's first block, an in-bounds address).
+  // The padded grid is written at the start of the solve, like the factors,
+  // and is read one level ahead so the load latency stays off the sweeps.
+  auto grid_at = [&](int kk, float& sc, float& zc) {
+    const int Imn = level_imin(kk, NB), nb = level_imax(kk, NB) - Imn + 1;
+    const int slot = warp * BPW + lane / S;
+    const int I = Imn + (slot < nb ? slot : 0);
+    const int64_t gi = i0 + S * I + lane % S;
+    int64_t grp = (j0 + S * (kk - I)) / a.group;
+    if (grp > a.ngroups - 1) grp = a.ngroups - 1;
+    sc = a.scale[gi * a.ngroups + grp];
+    zc = a.zero[gi * a.ngroups + grp];
+  };
+  float sc_next = 1.f, zc_next = 0.f;
+  if (warp < 1) grid_at(0, sc_next, zc_next);
+
   for (int k = 0; k < 2 * NB - 1; ++k) {
     if (k == 2 * NB - 2) grid_dep_launch();   // the next kernel may start setting up
     const int Imin = level_imin(k, NB), Imax = level_imax(k, NB);
     const int nblk = Imax - Imin + 1;
     const int nsw = (nblk + BPW - 1) / BPW;    // sweep warps of this level
     float* rTk = rT0 + (k & 1) * NB * RT_SLOT;
+    const float sc = sc_next, zc = zc_next;
+    if (k + 1 < 2 * NB - 1) {
+      const int nbn = level_imax(k + 1, NB) - level_imin(k + 1, NB) + 1;
+      if (warp < (nbn + BPW - 1) / BPW) grid_at(k + 1, sc_next, zc_next);
+    }
 
     if (warp < nsw) {
       // ---- B. block sweeps: lane = (sub, row), block Imin + BPW warp + sub
@@ -321,7 +352,7 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       // step before this row needs it, is kept out of the look-ahead sum
       const float ub1 = row > 0 ? Ubd[row * PU + row - 1] : 0.f;
       const float ubaa = Ubd[row * PU + row];
-      const float lB = 1.f / ubaa;
+      const float lBa = lB[S * I + row];
       const int64_t gi = i0 + S * I + row;
       const bool row_real = live && gi < a.m;
       float* rs = rTk + slot * RT_SLOT;
@@ -329,14 +360,13 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       const float* lAj = lA + S * J;
       float* Xrow = X + (S * I + row) * PX + S * J;
       const int64_t jb0 = j0 + S * J;
-      // the block's columns lie in one group of the grid (groups are whole
-      // multiples of 32 columns, or the whole row)
-      int64_t grp = jb0 / a.group;
-      if (grp > a.ngroups - 1) grp = a.ngroups - 1;
-      const float sc = a.scale[gi * a.ngroups + grp];
-      const float zc = a.zero[gi * a.ngroups + grp];
+      // sc, zc: the block's columns lie in one group of the grid (groups are
+      // whole multiples of 32 columns, or the whole row)
       // centred code c = clamp(rint(x / s), qmin - z, qmax - z); stored c + z
       const float clo = fqmin - zc, chi = fqmax - zc;
+      // a code is c + z with c in [clo, chi]; rounding is monotone, so the
+      // codes of this row lie in [clo + z, chi + z]
+      out_of_range |= live && ((clo + zc < -128.f) || (chi + zc > 127.f));
       const float rinv = 1.f / sc;
       signed char* csr = CS + slot * S * PC + row * PC;
       float FR[NF];
@@ -345,74 +375,73 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       float pp = 0.f;   // column sum over rows a' < a - 1 for this step's column
       float rlast = 0.f;  // r(a, .) completed by this lane in the previous step
 
-      for (int kb = 0; kb * 4 < NSTEP; ++kb) {
 #pragma unroll
-        for (int sg = 0; sg < 4; ++sg) {
-          const int d = kb * 4 + sg;
-          if (d >= NSTEP) break;
-          // straight-line step: inactive lanes compute on safe addresses and
-          // their results are masked (e = 0, stores predicated)
-          const int b = d - row;
-          const bool act = live && (unsigned)b < (unsigned)S;
-          const int bb = act ? b : 0;
-          const float xin = Xrow[bb];
-          const float la = lAj[bb];
-          // r(a-1, b): the row above completed column b in the previous step
-          // (lane 0 of a block multiplies it by ub1 = 0)
-          const float rprev = __shfl_up_sync(0xffffffffu, rlast, 1);
-          // look-ahead: the column sum of the NEXT step (column b + 1) over
-          // rows a' < a - 1, all completed by the previous step; it is off
-          // this step's dependency chain
-          const int bn = b + 1;
-          const float* rc = rs + ((unsigned)bn < (unsigned)S ? bn : S) * PR;
-          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+      for (int d = 0; d < NSTEP; ++d) {
+        // straight-line step: inactive lanes compute on safe addresses and
+        // their results are masked (e = 0, stores predicated)
+        const int b = d - row;
+        const bool act = live && (unsigned)b < (unsigned)S;
+        const int bb = act ? b : 0;
+        const float xin = Xrow[bb];
+        const float la = lAj[bb];
+        // r(a-1, b): the row above completed column b in the previous step
+        // (lane 0 of a block multiplies it by ub1 = 0)
+        const float rprev = __shfl_up_sync(0xffffffffu, rlast, 1);
+        // look-ahead: the column sum of the NEXT step (column b + 1) over
+        // rows a' < a - 1, all completed by the previous step; it is off this
+        // step's dependency chain.  A lane active next step has a <= d + 1,
+        // so only the rows a' <= d - 1 can count (ub is zero past a - 2).
+        const int bn = b + 1;
+        const float* rc = rs + ((unsigned)bn < (unsigned)S ? bn : S) * PR;
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
-          for (int c = 0; c < S / 4; ++c) {
+        for (int c = 0; c < S / 4; ++c) {
+          if (d + 1 < NSTEP && 4 * c <= d - 1) {
             const float4 v = *reinterpret_cast<const float4*>(rc + 4 * c);
             p0 = fmaf(ub[4 * c + 0], v.x, p0);
             p1 = fmaf(ub[4 * c + 1], v.y, p1);
             p2 = fmaf(ub[4 * c + 2], v.z, p2);
             if (c < S / 4 - 1) p3 = fmaf(ub[4 * c + 3], v.w, p3);
           }
-          // row b of the diagonal-major Ua, read before this step's stores
-          const float4* dr = reinterpret_cast<const float4*>(Dj + bb * PD);
-          float4 dv[PD / 4];
-#pragma unroll
-          for (int c = 0; c < PD / 4; ++c) dv[c] = dr[c];
-          const float x = xin - fmaf(ub1, rprev, pp) - ubaa * FR[sg];
-          pp = (p0 + p1) + (p2 + p3);
-          // rounding decision on x * fl(1/s): within 2^-23 relative of x / s,
-          // so it can differ from the correctly rounded quotient only within
-          // 2e-5 grid units of a rounding boundary
-          float c = rintf(x * rinv);
-          c = fminf(fmaxf(c, clo), chi);
-          const float e = act ? (x - sc * c) * lB * la : 0.f;
-          const float code = c + zc;
-          nonfinite |= act && !isfinite(x);
-          out_of_range |= act && ((code < -128.f) || (code > 127.f));
-          FR[sg] = fmaf(e, dv[0].x, FR[sg]);
-          rlast = FR[sg];
-          if (act) {
-            Xrow[b] = e;
-            csr[b] = (signed char)(int)fminf(fmaxf(code, -128.f), 127.f);
-            rs[b * PR + row] = FR[sg];
-          }
-          if (PRE && act && row_real && jb0 + b < a.n) a.preround[gi * a.n + jb0 + b] = x;
-          // pending accumulators of this row: FR[sg + t] += e Ua(b, b + t)
-#pragma unroll
-          for (int c = 0; c < PD / 4; ++c) {
-            const float4 v = dv[c];
-            if (4 * c + 0 >= 1 && sg + 4 * c + 0 < NF) FR[sg + 4 * c + 0] = fmaf(e, v.x, FR[sg + 4 * c + 0]);
-            if (4 * c + 1 >= 1 && sg + 4 * c + 1 < NF) FR[sg + 4 * c + 1] = fmaf(e, v.y, FR[sg + 4 * c + 1]);
-            if (4 * c + 2 >= 1 && sg + 4 * c + 2 < NF) FR[sg + 4 * c + 2] = fmaf(e, v.z, FR[sg + 4 * c + 2]);
-            if (4 * c + 3 >= 1 && sg + 4 * c + 3 < NF) FR[sg + 4 * c + 3] = fmaf(e, v.w, FR[sg + 4 * c + 3]);
-          }
-          __syncwarp();
         }
+        // row b of the diagonal-major Ua (its S entries; the row's pad is
+        // zero), read before this step's stores; entries t > 2 S - 2 - d
+        // reach only columns past the block
+        const float4* dr = reinterpret_cast<const float4*>(Dj + bb * PD);
+        float4 dv[S / 4];
 #pragma unroll
-        for (int j = 0; j < NF - 4; ++j) FR[j] = FR[j + 4];
+        for (int c = 0; c < S / 4; ++c)
+          if (4 * c <= 2 * S - 2 - d) dv[c] = dr[c];
+        const float x = xin - fmaf(ub1, rprev, pp) - ubaa * FR[d];
+        pp = (p0 + p1) + (p2 + p3);
+        // rounding decision on x * fl(1/s): within 2^-23 relative of x / s,
+        // so it can differ from the correctly rounded quotient only within
+        // 2e-5 grid units of a rounding boundary
+        float c = rintf(x * rinv);
+        c = fminf(fmaxf(c, clo), chi);
+        const float e = act ? (x - sc * c) * lBa * la : 0.f;
+        const float code = c + zc;
+        nonfinite |= act && !isfinite(x);
+        FR[d] = fmaf(e, dv[0].x, FR[d]);
+        rlast = FR[d];
+        if (act) {
+          Xrow[b] = e;
+          csr[b] = (signed char)(int)fminf(fmaxf(code, -128.f), 127.f);
+          rs[b * PR + row] = FR[d];
+        }
+        if (PRE && act && row_real && jb0 + b < a.n) a.preround[gi * a.n + jb0 + b] = x;
+        // pending accumulators of this row: FR[d + t] += e Ua(b, b + t)
 #pragma unroll
-        for (int j = NF - 4; j < NF; ++j) FR[j] = 0.f;
+        for (int c = 0; c < S / 4; ++c) {
+          if (4 * c <= 2 * S - 2 - d) {
+            const float4 v = dv[c];
+            if (4 * c + 0 >= 1 && 4 * c + 0 <= 2 * S - 2 - d) FR[d + 4 * c + 0] = fmaf(e, v.x, FR[d + 4 * c + 0]);
+            if (4 * c + 1 <= 2 * S - 2 - d) FR[d + 4 * c + 1] = fmaf(e, v.y, FR[d + 4 * c + 1]);
+            if (4 * c + 2 <= 2 * S - 2 - d) FR[d + 4 * c + 2] = fmaf(e, v.z, FR[d + 4 * c + 2]);
+            if (4 * c + 3 <= 2 * S - 2 - d) FR[d + 4 * c + 3] = fmaf(e, v.w, FR[d + 4 * c + 3]);
+          }
+        }
+        __syncwarp();
       }
       // codes and V of this block row: one contiguous run per lane
       if (row_real) {
