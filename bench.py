@@ -767,8 +767,9 @@ def run_ours(args, world, rank, local):
 
 
 def run_profile_solve(args):
-    """One warm-up step of the configuration, then one solve inside the NVTX
-    range "solve" (for ncu's --nvtx-include "solve/"); prints one line."""
+    """One warm-up step of the configuration, then one factor preparation in
+    the NVTX range "prepare" and one solve in the range "solve" (for ncu's
+    --nvtx-include); prints one line."""
     import torch
     from kronecker_factored_gptq_gb300 import bakron as kb
     from kronecker_factored_gptq_gb300 import workloads as WL
@@ -780,6 +781,10 @@ def run_profile_solve(args):
     solver = kb.Solver(w.m, w.n, bits=w.bits)
     solver.solve(dW, dA, w.damp_A, dB, w.damp_B)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("prepare")
+    solver.prepare(dA, w.damp_A, dB, w.damp_B)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     n0 = kb.kernel_launches()
     torch.cuda.nvtx.range_push("solve")
     solver.quantize(dW)
@@ -807,8 +812,8 @@ def main():
     ap.add_argument("--no-context", action="store_true",
                     help="skip the context timings (one-sided GPTQ, factor accumulation)")
     ap.add_argument("--profile-solve", action="store_true",
-                    help="profiling helper: one warm-up step, then one solve in the NVTX range "
-                         "'solve'; no benchmark line")
+                    help="profiling helper: one warm-up step, then one preparation and one solve "
+                         "in the NVTX ranges 'prepare' and 'solve'; no benchmark line")
     args = ap.parse_args()
     if args.profile_solve:
         run_profile_solve(args)
