@@ -13,22 +13,24 @@
 // scaled errors.  For blocks (I, J):
 //   P[I,J] = sum_{J'' < J} E[I,J''] Ua[J'',J]        (row accumulator, left part)
 //   R[I,J] = P[I,J] + E[I,J] Ua[J,J]                 (complete row accumulator)
-//   x0[I,J] = W~[I,J] - sum_{I' < I} Ub[I',I]^T R[I',J] - Ub[I,I]^T P[I,J]
+//   x0[I,J] = W~[I,J] - sum_{I' < I} Ub[I',I]^T R[I',J]
 // where W~ already holds every update from earlier tile anti-diagonals.  x0
-// is what the block sweep starts from; the sweep applies the updates between
-// entries of the block itself in the same row-accumulator form:
-//   x(a,b) = x0(a,b) - sum_{a' < a} Ub(a',a) r(a',b) - Ub(a,a) r_part(a,b),
-//   r(a,b) = sum_{b' <= b} e(a,b') Ua(b',b),  r_part: the sum over b' < b.
+// is what the block sweep starts from; the sweep applies the rest, the
+// updates from the block's own rows, in the row-accumulator form
+//   x(a,b) = x0(a,b) - sum_{a' < a} Ub(a',a) R(a',b) - Ub(a,a) R_part(a,b),
+//   R(a,b) = P(a,b) + sum_{b' <= b} e(a,b') Ua(b',b),  R_part: the sum over
+//   b' < b (the Ub[I,I]^T P[I,J] part of the block's own rows rides in the
+//   accumulators, which start from P).
 //
 // Schedule, level k (blocks with I + J = k), two CTA barriers per level:
-//   B(k):   the sweep warps run the block sweeps of level k (then R = P + r,
-//           codes and V); four other warps meanwhile apply the pushes of
-//           level k-1 that later levels need but level k+1 does not:
+//   B(k):   the sweep warps run the block sweeps of level k (R, codes and
+//           V); four other warps meanwhile apply the pushes of level k-1
+//           that later levels need but level k+1 does not:
 //           P[I,J'] += E[I,J] Ua[J,J'] for J' >= J + 2 and
 //           W~[I',J] -= Ub[I,I']^T R[I,J] for I' >= I + 2;
-//   prep(k+1): one warp per block (I,J) of level k+1 completes its x0 with
-//           the pushes from its two neighbours on level k, then
-//           W~[I,J] -= Ub[I,I]^T P[I,J] (triangular).
+//   prep(k+1): the pushes from the two neighbours on level k into each block
+//           (I,J) of level k+1, P[I,J] += E[I,J-1] Ua[J-1,J] and
+//           W~[I,J] -= Ub[I-1,I]^T R[I-1,J], one warp per product.
 // R of level k lives in one of two slot sets (level parity), because the
 // deferred pushes read it while level k+1 writes its own.
 //
@@ -203,8 +205,11 @@ __device__ __forceinline__ void deferred_pushes(int kp, int wk, int nwork, float
 }  // namespace
 
 // PRE: also write the pre-rounding values (a.preround), a debug output kept
-// out of the default instantiation for its register cost
-template <int S, bool PRE>
+// out of the default instantiation for its register cost.  CHK: check every
+// code against the int8 range; without it the grid guarantees the range
+// (qmin >= -128, qmax <= 127 and integer zero points in [qmin, qmax], so a
+// code c + z with c clamped to [qmin - z, qmax - z] lies in [qmin, qmax]).
+template <int S, bool PRE, bool CHK>
 __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   using K = Cfg<S>;
   constexpr int NB = K::NB, BPW = K::BPW, NF = K::NF, PX = K::PX, PP = K::PP, PR = K::PR,
@@ -364,16 +369,18 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
       // whole multiples of 32 columns, or the whole row)
       // centred code c = clamp(rint(x / s), qmin - z, qmax - z); stored c + z
       const float clo = fqmin - zc, chi = fqmax - zc;
-      // a code is c + z with c in [clo, chi]; rounding is monotone, so the
-      // codes of this row lie in [clo + z, chi + z]
-      out_of_range |= live && ((clo + zc < -128.f) || (chi + zc > 127.f));
       const float rinv = 1.f / sc;
       signed char* csr = CS + slot * S * PC + row * PC;
       float FR[NF];
 #pragma unroll
       for (int j = 0; j < NF; ++j) FR[j] = 0.f;
       float pp = 0.f;   // column sum over rows a' < a - 1 for this step's column
-      float rlast = 0.f;  // r(a, .) completed by this lane in the previous step
+      float rlast = 0.f;  // R(a, .) completed by this lane in the previous step
+      // P(a, b) of the block (zero in block column 0) enters the accumulator
+      // FR[a + b] one step before the lane reaches column b (row 0: here)
+      const bool hasP = live && J >= 1;
+      const float* Pa = Pt + K::p_idx(I, J >= 1 ? J : 1) * S * PP + row;   // P(a, b) at Pa[b PP]
+      if (hasP && row == 0) FR[0] = Pa[0];
 
 #pragma unroll
       for (int d = 0; d < NSTEP; ++d) {
@@ -384,6 +391,13 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         const int bb = act ? b : 0;
         const float xin = Xrow[bb];
         const float la = lAj[bb];
+        // P(a, b + 1) for the next column's accumulator
+        float pnext = 0.f;
+        if (d + 1 < NSTEP) {
+          const bool pin = hasP && (unsigned)(b + 1) < (unsigned)S;
+          pnext = Pa[(pin ? b + 1 : 0) * PP];
+          pnext = pin ? pnext : 0.f;
+        }
         // r(a-1, b): the row above completed column b in the previous step
         // (lane 0 of a block multiplies it by ub1 = 0)
         const float rprev = __shfl_up_sync(0xffffffffu, rlast, 1);
@@ -422,6 +436,8 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         const float e = act ? (x - sc * c) * lBa * la : 0.f;
         const float code = c + zc;
         nonfinite |= act && !isfinite(x);
+        if (CHK) out_of_range |= act && ((code < -128.f) || (code > 127.f));
+        if (d + 1 < NSTEP) FR[d + 1] += pnext;
         FR[d] = fmaf(e, dv[0].x, FR[d]);
         rlast = FR[d];
         if (act) {
@@ -483,12 +499,6 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           }
         }
       }
-      // R^T = P^T + r^T in place (lane = block row a owns column a)
-      if (live && J >= 1) {
-        const float* pb = Pt + K::p_idx(I, J) * S * PP;
-#pragma unroll 8
-        for (int b = 0; b < S; ++b) rs[b * PR + row] += pb[b * PP + row];
-      }
     } else if (k >= 1 && warp < nsw + NDEF) {
       // ---- deferred pushes of level k-1 into levels >= k+1, on NDEF of the
       // other warps (more would take issue and shared-memory bandwidth from
@@ -498,24 +508,23 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
     }
     __syncthreads();
 
-    // ---- prep(k+1): x0 of the blocks of level k+1, one warp per block
+    // ---- prep(k+1): the neighbours' pushes into the blocks of level k+1,
+    // one warp per product (the two products of a block write different
+    // arrays)
     if (k + 1 < 2 * NB - 1) {
       const int kn = k + 1;
       const int Inmin = level_imin(kn, NB), Inmax = level_imax(kn, NB);
       const int nn = Inmax - Inmin + 1;
-      for (int w = warp; w < nn; w += NWARP) {
-        const int I = Inmin + w, J = kn - I;
-        float* Xb = X + (S * I) * PX + S * J;
-        if (J >= 1)   // P[I,J] += E[I,J-1] Ua[J-1,J]  (the left neighbour, level k)
-          block_product<S, false, true>(UaO + K::ua_idx(J - 1, J) * S * PU, X + (S * I) * PX + S * (J - 1),
-                                  PX, Pt + K::p_idx(I, J) * S * PP, PP, 1.f, lane);
-        if (I >= 1)   // W~[I,J] -= Ub[I-1,I]^T R[I-1,J]  (the upper neighbour, level k)
+      for (int t = warp; t < 2 * nn; t += NWARP) {
+        const int I = Inmin + (t >> 1), J = kn - I;
+        if ((t & 1) == 0) {
+          if (J >= 1)   // P[I,J] += E[I,J-1] Ua[J-1,J]  (the left neighbour, level k)
+            block_product<S, false, true>(UaO + K::ua_idx(J - 1, J) * S * PU, X + (S * I) * PX + S * (J - 1),
+                                    PX, Pt + K::p_idx(I, J) * S * PP, PP, 1.f, lane);
+        } else if (I >= 1) {   // W~[I,J] -= Ub[I-1,I]^T R[I-1,J]  (the upper neighbour, level k)
           block_product<S, false, true>(UbB + K::ub_idx(I - 1, I) * S * PU,
-                                  rTk + (I - 1 - Imin) * RT_SLOT, PR, Xb, PX, -1.f, lane);
-        __syncwarp();
-        if (J >= 1)   // W~[I,J] -= Ub[I,I]^T P[I,J]
-          block_product<S, true, false>(UbB + K::ub_idx(I, I) * S * PU, Pt + K::p_idx(I, J) * S * PP, PP,
-                                 Xb, PX, -1.f, lane);
+                                  rTk + (I - 1 - Imin) * RT_SLOT, PR, X + (S * I) * PX + S * J, PX, -1.f, lane);
+        }
       }
       __syncthreads();
     }
@@ -546,15 +555,18 @@ constexpr int kLeafBlock = 16;
 
 cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s) {
   constexpr int S = kLeafBlock;
-  static std::atomic<unsigned long long> done[2];
+  static std::atomic<unsigned long long> done[3];
   constexpr size_t smem = Cfg<S>::SMEM;
-  cudaError_t e = ensure_smem_limit((const void*)leaf_kernel<S, false>, smem, done[0]);
-  if (e == cudaSuccess) e = ensure_smem_limit((const void*)leaf_kernel<S, true>, smem, done[1]);
+  cudaError_t e = ensure_smem_limit((const void*)leaf_kernel<S, false, false>, smem, done[0]);
+  if (e == cudaSuccess) e = ensure_smem_limit((const void*)leaf_kernel<S, false, true>, smem, done[1]);
+  if (e == cudaSuccess) e = ensure_smem_limit((const void*)leaf_kernel<S, true, true>, smem, done[2]);
   if (e != cudaSuccess) return e;
   count_launch();
   if (a.preround)
-    return launch_kernel(leaf_kernel<S, true>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
-  return launch_kernel(leaf_kernel<S, false>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
+    return launch_kernel(leaf_kernel<S, true, true>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
+  if (a.qmin < -128 || a.qmax > 127)
+    return launch_kernel(leaf_kernel<S, false, true>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
+  return launch_kernel(leaf_kernel<S, false, false>, dim3(n_tiles), dim3(NTHR), smem, s, a.pdl != 0, a);
 }
 
 }  // namespace bakron
