@@ -64,9 +64,9 @@ typedef enum {
  * split. */
 typedef struct {
   double leaf_ms;         /* leaf sweeps (anti-diagonal steps inside tiles) */
-  double prop1_ms;        /* propagation stage 1: Y^T = U_A^T E_P^T (off the
-                             critical stream) */
-  double prop2_ms;        /* propagation stage 2: W~_Q -= U_B^T Y */
+  double prop1_ms;        /* propagation stage 1: row accumulators
+                             R^T += U_A^T E^T (off the critical stream) */
+  double prop2_ms;        /* propagation stage 2: W~ -= U_B^T R */
   double other_ms;        /* padding, factor transposition/split */
   double prop_flops;      /* executed propagation flops (both stages) */
   int64_t leaf_launches;
@@ -131,9 +131,14 @@ int64_t bakron_kernel_launches(void);
  *                          chunk0, nchunks
  *       ROWS leaf          0, J (column tile), 0, M, depth, 0, 0
  *       ROWS propagation   1, 0, 0, 0, depth, chunk0, nchunks;
- *     n_chunks records of 6 values dlo, dhi (target range), off1, n1
- *     (stage-1 items), off, n (stage-2 items; ROWS has no stage-1 items);
- *     the items.
+ *     n_chunks records of 6 values dlo, dhi (the tile anti-diagonals the
+ *     chunk writes), off1, n1 (stage-1 items), off, n (stage-2 items; ROWS
+ *     has no stage-1 items); the items.  SOLVE items of 4 values: stage 1
+ *     (J', I, k0, k1): the row accumulator tile R^T[J', I] += the products
+ *     of the error tiles E[I, k0 .. k1-1]; stage 2 (I', J', k0, k1): W~[I', J']
+ *     -= the products of R^T[J', k0 .. k1-1] (near stage 2 reads R of rows
+ *     I'-1 and I').  A propagation follows the near products of the diagonal
+ *     after its last source.
  *   PREPARE: nb, n_items, n_levels; nb records syrk_off, n1, n2 (the
  *     trailing updates of step kb: the urgent tile, n1 lookahead tiles, n2
  *     bulk tiles); per doubling level n_pairs then n_pairs records t_off,

@@ -7,36 +7,42 @@
 // second half).  The recursion runs over TILE anti-diagonals D = I + J of
 // 128 x 128 tiles; every tile order with D increasing rounds an entry after
 // all entries to its top-left, which Theorem 3.2 says leaves the result
-// unchanged.  The error of a tile reaches a later tile in two ways:
+// unchanged.
 //
-//  * near products: the tiles of diagonal D - 1 that touch a tile (I, J) of
-//    diagonal D, its left and upper neighbours, reach it through
-//      W~[I, J] -= U_B^T[I, I] (U_A^T[J, J-1] E[I, J-1]^T)^T
-//               +  U_B^T[I, I-1] (U_A^T[J, J] E[I-1, J]^T)^T,
-//    two stage-1 and one stage-2 product per tile, run on the critical
-//    stream between leaf D - 1 and leaf D;
-//  * propagation: every other (source, target) pair is two or more
-//    diagonals apart.  rec(D0, D1) with D1 - D0 >= 2 and Dm = (D0 + D1) / 2
-//    runs rec(D0, Dm), then propagates the sources [max(D0 - 1, 0), Dm - 1)
-//    into the targets [Dm, D1), then rec(Dm, D1).  A pair (s, t) with
-//    t - s >= 2 is propagated by the one node whose split separates s + 1
-//    from t; pairs with t - s = 1 never are (they are the near products).
-//    The propagation's last source is diagonal Dm - 2, so it starts after
-//    leaf Dm - 2 and runs beside leaf Dm - 1: no propagation sits between
-//    two leaves on the critical stream.
+// The error reaches later tiles in the row-accumulator form: with
+//   R[I, J'] = sum_{J <= J'} E[I, J] U_A[J, J']       (row I's accumulator)
+// target (I', J') receives  W~[I', J'] -= sum_{I < I'} U_B[I, I']^T R[I, J']
+// + U_B[I', I']^T R^-[I', J'], R^- the sum over J < J' only.  The library
+// keeps R (transposed, R^T[J', I], in fp32 and split for the tensor cores)
+// for the whole solve and builds it incrementally, so each row update
+// E[I, J] U_A[J, J'] and each push of a complete R[I, J'] into a target is
+// computed once:
 //
-// A propagation is two stages over lists of dense 128-tile products (the
-// triangular diagonal blocks of the factors carry their zeros):
-//   stage 1: for every row tile I with source tiles:
-//            Y^T[J', I] = sum_{J in sources of row I, J <= J'} U_A^T[J', J] E[I, J]^T
-//   stage 2: for every target tile (I', J'):
-//            W~[I', J'] -= sum_{I <= I'} U_B^T[I', I] Y^T[J', I]^T
-// Both stages are split by the target tile anti-diagonal they serve into
-// chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...: the first chunk is what
-// leaf Dm needs and runs on a high-priority stream, the others on a
-// low-priority stream; every leaf waits for the chunks covering its
-// diagonal.  A stage-1 item Y^T[J', I] is first read by targets on diagonal
-// max(Dm, I + J'), so it belongs to the chunk holding that diagonal.
+//  * near products, on the critical stream between leaf D - 1 and leaf D,
+//    for each target (I, J) of diagonal D: stage 1 adds the row updates
+//    from diagonal D - 1 into R, E[I, J-1] U_A[J-1, J] into R[I, J] (now
+//    R^-[I, J]) and the own term E[I-1, J] U_A[J, J] into R[I-1, J] (now
+//    complete); stage 2 applies U_B[I-1, I]^T R[I-1, J] + U_B[I, I]^T R[I, J];
+//  * propagation: rec(D0, D1) with D1 - D0 >= 2 and Dm = (D0 + D1) / 2 runs
+//    rec(D0, Dm), then, for the sources [max(D0 - 1, 0), Dm - 1) and the
+//    targets [Dm, D1): stage 1, the row updates from the source tiles E[I, J]
+//    into the R tiles (I, J') of the target band; stage 2, the pushes of the
+//    complete R tiles (I, J') of the source band into the targets (I', J')
+//    below them; then rec(Dm, D1).  A (source, target) pair of either kind
+//    with t - s >= 2 is handled by the one node whose split separates s + 1
+//    from t; pairs with t - s = 1 are the near products.  The propagation
+//    starts after the near products of diagonal Dm - 1 (the own terms that
+//    complete the R tiles of diagonal Dm - 2), beside leaf Dm - 1: no
+//    propagation sits between two leaves on the critical stream.
+//
+// Both stages are lists of dense 128-tile products (the triangular diagonal
+// blocks of the factors carry their zeros):
+//   stage 1: R^T[J', I] += sum_{J in the band, row I} U_A^T[J', J] E[I, J]^T
+//   stage 2: W~[I', J'] -= sum_{I in the band, column J'} U_B^T[I', I] R^T[J', I]^T
+// split by the tile anti-diagonal of the R tile (stage 1) or target (stage
+// 2) into chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...: every chunk is
+// due at the near products of its first diagonal, which wait for it; the
+// chunk due next runs on a high-priority stream, the later ones lower.
 #include <algorithm>
 #include <climits>
 #include <cstring>
@@ -52,7 +58,7 @@ namespace bakron {
 namespace {
 
 constexpr int T = kTile;
-// Propagation lanes (a Y^T buffer pair and three streams each).
+// Propagation lanes (three streams each).
 constexpr int kMaxDepth = 24;
 // A propagation chunk whose first target is at most this many leaves after
 // the propagation's start runs at middle priority, a later one at the lowest.
@@ -60,9 +66,9 @@ constexpr int kMaxDepth = 24;
 #define BAKRON_MID_SLACK 15
 #endif
 constexpr int kMidSlack = BAKRON_MID_SLACK;
-// Source diagonals the near products reach back (D - kNear .. D - 1); the
+// Source diagonals the near products reach back (diagonal D - 1); the
 // propagations cover every pair further apart.
-constexpr int kNear = BAKRON_NEAR_DIAGONALS;
+constexpr int kNear = 1;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -82,7 +88,7 @@ struct Op {
                            // its last source diagonal (after whose leaf it starts)
   int I0, ntiles;          // leaf: first row tile and tile count
   int s0, s1;              // propagation: source diagonals [s0, s1)
-  int depth;               // propagation: its lane (Y^T buffer and streams)
+  int depth;               // propagation: its lane (streams)
   int chunk0, nchunks;     // near: one chunk; propagation: its chunks
 };
 
@@ -124,61 +130,56 @@ Op build_prop(Schedule& s, int S0, int S1, int T0, int T1, int depth) {
     while (bounds[c].second <= d) ++c;
     return c;
   };
-  // stage 1 items, bucketed by the first target diagonal that reads them
-  std::vector<std::vector<WorkItem>> s1(bounds.size());
-  std::vector<double> f1(bounds.size(), 0.0);
+  std::vector<std::vector<WorkItem>> s1(bounds.size()), s2(bounds.size());
+  // stage 1: R tile (I, J') of the target band += the source tiles of row I
+  // (all at least two columns left of J')
   for (int I = 0; I < M; ++I) {
     const int jlo = std::max(S0 - I, 0), jhi = std::min(S1 - I, N);
     if (jlo >= jhi) continue;
-    for (int Jp = jlo; Jp < std::min(T1 - I, N); ++Jp) {
-      const int lo = std::max(I, T0 - Jp), hi = std::min(M - 1, T1 - 1 - Jp);
-      if (lo > hi) continue;  // no target in column Jp at or below row I
-      const int k1 = std::min(jhi, Jp + 1);
-      const int c = chunk_of(std::max(T0, I + Jp));
-      s1[c].push_back(WorkItem{Jp, I, jlo, k1});
-      f1[c] += 2.0 * T * T * T * (k1 - jlo);
+    for (int Jp = std::max(T0 - I, 0); Jp < std::min(T1 - I, N); ++Jp) {
+      const int c = chunk_of(I + Jp);
+      s1[c].push_back(WorkItem{Jp, I, jlo, jhi});
+    }
+  }
+  // stage 2: target (I', J') of the target band -= the complete R tiles of
+  // column J' in the source band (all at least two rows above I')
+  for (int Jp = 0; Jp < N; ++Jp) {
+    const int ilo = std::max(S0 - Jp, 0), ihi = std::min(S1 - Jp, M);
+    if (ilo >= ihi) continue;
+    for (int Ip = std::max(T0 - Jp, 0); Ip < std::min(T1 - Jp, M); ++Ip) {
+      const int c = chunk_of(Ip + Jp);
+      s2[c].push_back(WorkItem{Ip, Jp, ilo, ihi});
     }
   }
   for (size_t ci = 0; ci < bounds.size(); ++ci) {
     Chunk c{};
     c.dlo = bounds[ci].first;
     c.dhi = bounds[ci].second;
-    c.off1 = (int)s.items.size();
-    for (const WorkItem& w : s1[ci]) {
-      s.items.push_back(w);
-      c.maxk1 = std::max(c.maxk1, w.k1 - w.k0);
-    }
-    sort_items(s.items, c.off1);
-    c.n1 = (int)s.items.size() - c.off1;
-    c.flops1 = f1[ci];
-    c.off = (int)s.items.size();
-    for (int Ip = 0; Ip < M; ++Ip) {
-      for (int Jp = std::max(c.dlo - Ip, 0); Jp < std::min(c.dhi - Ip, N); ++Jp) {
-        // source rows I <= Ip whose Y^T[Jp, I] is not empty
-        const int ilo = std::max(std::max(0, S0 - Jp), S0 - N + 1);
-        const int ihi = std::min(std::min(Ip, S1 - 1), M - 1);
-        if (ilo > ihi) continue;
-        s.items.push_back(WorkItem{Ip, Jp, ilo, ihi + 1});
-        c.flops += 2.0 * T * T * T * (ihi + 1 - ilo);
-        c.maxk = std::max(c.maxk, ihi + 1 - ilo);
+    auto take = [&](const std::vector<WorkItem>& src, int& off, int& n, int& maxk, double& flops) {
+      off = (int)s.items.size();
+      for (const WorkItem& w : src) {
+        s.items.push_back(w);
+        maxk = std::max(maxk, w.k1 - w.k0);
+        flops += 2.0 * T * T * T * (w.k1 - w.k0);
       }
-    }
-    sort_items(s.items, c.off);
-    c.n = (int)s.items.size() - c.off;
+      sort_items(s.items, off);
+      n = (int)s.items.size() - off;
+    };
+    take(s1[ci], c.off1, c.n1, c.maxk1, c.flops1);
+    take(s2[ci], c.off, c.n, c.maxk, c.flops);
     s.chunks.push_back(c);
   }
   op.nchunks = (int)s.chunks.size() - op.chunk0;
   return op;
 }
 
-// Near products into the tiles of diagonal D from every tile at most kNear
-// diagonals before it (D - kNear .. D - 1), in the row-accumulator form:
-// for a target (I, J) and each row I'' = I - k (k = 0 .. kNear) the stage-1
-// item writes Y^T[J, I''] over the source columns J' of row I'' with
-// D - kNear <= I'' + J' < D and J' <= J (k = 0: J - kNear .. J - 1; k >= 1:
-// J - kNear + k .. J); the stage-2 item of (I, J) sums U_B^T[I, I''] Y^T[J, I'']
-// over those rows.  Targets of one diagonal sit in distinct columns J, so the
-// Y^T tiles of one launch are distinct.
+// Near products into the tiles of diagonal D from diagonal D - 1, in the
+// row-accumulator form: for a target (I, J) the stage-1 items add
+// E[I, J-1] U_A[J-1, J] into R^T[J, I] and E[I-1, J] U_A[J, J] into
+// R^T[J, I-1] (source columns J - 1 and J); the stage-2 item of (I, J) sums
+// U_B^T[I, I''] R^T[J, I''] over the rows I'' = I - 1, I.  Targets of one
+// diagonal sit in distinct columns J, so the R tiles of one launch are
+// distinct.
 Op build_near(Schedule& s, int D) {
   const int M = s.M, N = s.N;
   Op op{};
@@ -247,8 +248,8 @@ void build_rec(Schedule& s, int D0, int D1, int depth, std::vector<std::vector<O
   build_rec(s, Dm, D1, depth + 1, prop_after, split);
 }
 
-// Y^T buffer and stream pair of each propagation ("lane", kept in Op.depth):
-// the lowest lane whose previous propagation has finished.  A propagation's
+// Streams of each propagation ("lane", kept in Op.depth): the lowest lane
+// whose previous propagation has finished.  A propagation's
 // chunks all complete before the leaf of the last chunk's first target, and
 // a propagation starts after the leaf of its last source, so a lane is free
 // for a propagation starting after leaf D once its previous one's last chunk
@@ -284,14 +285,18 @@ void build_schedule(Schedule& s, int max_lanes) {
     std::vector<std::vector<Op>> prop_after(ND);
     build_rec(s, 0, ND, 0, prop_after, split != 0);
     for (int D = 0; D < ND; ++D) {
-      if (D >= 1) s.ops.push_back(build_near(s, D));
+      // the propagations whose last source is diagonal D - 1 follow the near
+      // products of diagonal D, which complete that diagonal's R tiles
+      if (D >= 1) {
+        s.ops.push_back(build_near(s, D));
+        for (const Op& op : prop_after[D - 1]) s.ops.push_back(op);
+      }
       Op leaf{};
       leaf.kind = 0;
       leaf.D = D;
       leaf.I0 = std::max(0, D - s.N + 1);
       leaf.ntiles = std::min(D, s.M - 1) - leaf.I0 + 1;
       s.ops.push_back(leaf);
-      for (const Op& op : prop_after[D]) s.ops.push_back(op);
     }
     if (assign_lanes(s, max_lanes)) return;
   }
@@ -308,20 +313,25 @@ void build_schedule(Schedule& s, int max_lanes) {
 // writer's own event (or through the stream, for the leaf and the near
 // products, which are the last writers of their diagonal).  A chunk that
 // reaches past [lo, hi) stays listed for the writers of its other diagonals.
+// The critical stream waits for a listed chunk once: its later work follows
+// that wait in stream order, and a kernel launched with no event wait in
+// front of it can start early (programmatic dependent launch).
 struct PendingChunks {
   struct Item {
     cudaEvent_t ev;
     int dlo, dhi;
+    bool crit_waited;
   };
   std::vector<Item> v;
-  void add(cudaEvent_t ev, int dlo, int dhi) { v.push_back(Item{ev, dlo, dhi}); }
-  cudaError_t order_before(cudaStream_t cs, int lo, int hi) {
+  void add(cudaEvent_t ev, int dlo, int dhi) { v.push_back(Item{ev, dlo, dhi, false}); }
+  cudaError_t order_before(cudaStream_t cs, int lo, int hi, bool critical = false) {
     size_t w = 0;
     for (size_t i = 0; i < v.size(); ++i) {
       const bool overlap = v[i].dlo < hi && v[i].dhi > lo;
-      if (overlap) {
+      if (overlap && !(critical && v[i].crit_waited)) {
         const cudaError_t e = cudaStreamWaitEvent(cs, v[i].ev, 0);
         if (e != cudaSuccess) return e;
+        if (critical) v[i].crit_waited = true;
       }
       if (!(overlap && v[i].dlo >= lo && v[i].dhi <= hi)) v[w++] = v[i];
     }
@@ -435,10 +445,7 @@ size_t plan_bytes(int M, int N) {
 
 struct QLayout {
   int64_t M, N, Mp, Np;
-  int ndepth;
-  size_t status, sched, scale, zero, wt, ehi, elo, ynhi, ynlo, yhi[kMaxDepth], ylo[kMaxDepth], lathi,
-      latlo, lbthi,
-      lbtlo, total;
+  size_t status, sched, scale, zero, wt, ehi, elo, racc, rhi, rlo, lathi, latlo, lbthi, lbtlo, total;
 };
 
 QLayout quantize_layout(int64_t m, int64_t n) {
@@ -448,7 +455,6 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   L.Mp = L.M * T;
   L.Np = L.N * T;
   const Schedule& s = get_schedule((int)L.M, (int)L.N);
-  L.ndepth = s.ops.size() > 1 ? s.max_depth + 1 : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
   const size_t f = sizeof(float);
@@ -463,15 +469,10 @@ QLayout quantize_layout(int64_t m, int64_t n) {
   L.wt = take(f * L.Mp * L.Np);
   L.ehi = take(f * L.Mp * L.Np);
   L.elo = take(f * L.Mp * L.Np);
-  // the near products' Y^T pair (critical stream only)
-  L.ynhi = take(f * L.Np * L.Mp);
-  L.ynlo = take(f * L.Np * L.Mp);
-  // one Y^T pair per recursion depth: a propagation's deferred chunks may
-  // still be reading its Y^T while deeper propagations write theirs
-  for (int d = 0; d < L.ndepth; ++d) {
-    L.yhi[d] = take(f * L.Np * L.Mp);
-    L.ylo[d] = take(f * L.Np * L.Mp);
-  }
+  // the row accumulators R^T (Np x Mp): fp32 running sums, and split
+  L.racc = take(f * L.Np * L.Mp);
+  L.rhi = take(f * L.Np * L.Mp);
+  L.rlo = take(f * L.Np * L.Mp);
   L.lathi = take(f * L.Np * L.Np);
   L.latlo = take(f * L.Np * L.Np);
   L.lbthi = take(f * L.Mp * L.Mp);
@@ -748,8 +749,8 @@ bool sizes_ok(int64_t m, int64_t n) {
 }
 
 // The one-sided solve (U_B = I): see RowsSchedule.  Arguments validated by
-// bakron_quantize; the workspace layout is the two-sided one (its Y^T and
-// U_B^T regions stay unused).
+// bakron_quantize; the workspace layout is the two-sided one (its row
+// accumulator and U_B^T regions stay unused).
 // One problem of a batch: the stream set it runs on (locked by the caller),
 // that set's event pool position, and what the call leaves for the caller:
 // the event recorded at its end on the critical stream and its status block.
@@ -825,7 +826,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
   PendingChunks pending;
   for (const RowsOp& op : sch.ops) {
     if (op.kind == 0) {
-      TRY_SOLVE(pending.order_before(cs, op.J, op.J + 1));
+      TRY_SOLVE(pending.order_before(cs, op.J, op.J + 1, true));
       la.D = op.J;
       la.I0 = 0;
       la.pdl = op.J > 0;   // the first leaf reads the factor the kernel before it wrote
@@ -842,7 +843,7 @@ bakron_status quantize_rows(const float* W, int64_t m, int64_t n, const float* U
     p2.st = st;
     if (op.nchunks > 0)
       TRY_SOLVE(pending.order_before(cs, sch.chunks[op.chunk0].dlo,
-                                    sch.chunks[op.chunk0 + op.nchunks - 1].dhi));
+                                    sch.chunks[op.chunk0 + op.nchunks - 1].dhi, true));
     for (int c = 0; c < op.nchunks; ++c) {
       const Chunk& ch = sch.chunks[op.chunk0 + c];
       if (o.times) o.times->prop_flops += ch.flops;
@@ -1259,57 +1260,77 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
   la.V = V; la.codes = codes; la.preround = preround;
   la.m = m; la.n = n; la.qmin = qmin; la.qmax = qmax;
   la.st = st;
-  // stage 1: Y^T = U_A^T E^T into the given buffer; stage 2: W~ -= U_B^T Y
-  auto stage1 = [&](float* yh, float* yl) {
-    PropArgs p{};
-    p.A_hi = lathi; p.A_lo = latlo; p.lda = L.Np; p.a_rows = L.Np;
-    p.B_hi = ehi; p.B_lo = elo; p.ldb = L.Np; p.b_rows = L.Mp;
-    p.out_hi = yh; p.out_lo = yl; p.ldo = L.Mp;
-    p.stage = 1;
-    p.st = st;
-    return p;
-  };
-  auto stage2 = [&](float* yh, float* yl) {
-    PropArgs p{};
-    p.A_hi = lbthi; p.A_lo = lbtlo; p.lda = L.Mp; p.a_rows = L.Mp;
-    p.B_hi = yh; p.B_lo = yl; p.ldb = L.Mp; p.b_rows = L.Np;
-    p.wt = wt; p.ldw = L.Np;
-    p.stage = 2;
-    p.st = st;
-    return p;
-  };
+  float* racc = (float*)(base + L.racc);
+  float* rhi = (float*)(base + L.rhi);
+  float* rlo = (float*)(base + L.rlo);
+  // stage 1: R^T += U_A^T E^T (fp32 running sums, written back and split);
+  // stage 2: W~ -= U_B^T R
+  PropArgs p1{};
+  p1.A_hi = lathi; p1.A_lo = latlo; p1.lda = L.Np; p1.a_rows = L.Np;
+  p1.B_hi = ehi; p1.B_lo = elo; p1.ldb = L.Np; p1.b_rows = L.Mp;
+  p1.out_hi = rhi; p1.out_lo = rlo; p1.acc = racc; p1.ldo = L.Mp;
+  p1.stage = 1;
+  p1.st = st;
+  PropArgs p2{};
+  p2.A_hi = lbthi; p2.A_lo = lbtlo; p2.lda = L.Mp; p2.a_rows = L.Mp;
+  p2.B_hi = rhi; p2.B_lo = rlo; p2.ldb = L.Mp; p2.b_rows = L.Np;
+  p2.wt = wt; p2.ldw = L.Np;
+  p2.stage = 2;
+  p2.st = st;
   auto launch = [&](PropArgs pa, int off, int nit, int maxk, cudaStream_t str) {
     pa.items = items + off; pa.n_items = nit; pa.max_k = maxk;
     pa.pdl = str == cs;
     return o.use_3xtf32 ? launch_prop_tc(pa, str) : launch_prop_simt(pa, str);
   };
-  PendingChunks pending;
-  cudaEvent_t ev_leaf = nullptr;   // recorded after the leaf a propagation follows
+  // R starts at zero: its fp32 sums are cleared on a lane stream beside the
+  // first leaf; the critical stream waits before the first near products,
+  // which every later writer of R follows
+  cudaEvent_t ev_rzero = nullptr;
+  {
+    cudaEvent_t ev;
+    TRY_SOLVE(next_event(&ev));
+    TRY_SOLVE(cudaEventRecord(ev, cs));
+    TRY_SOLVE(cudaStreamWaitEvent(ss->side[0], ev, 0));
+    TRY_SOLVE(cudaMemsetAsync(racc, 0, sizeof(float) * (size_t)L.Np * (size_t)L.Mp, ss->side[0]));
+    TRY_SOLVE(next_event(&ev_rzero));
+    TRY_SOLVE(cudaEventRecord(ev_rzero, ss->side[0]));
+  }
+  // Writers of W~ tiles (pending) and of R tiles (rpending), each keyed by
+  // the tile anti-diagonals they write; every later writer or reader of the
+  // same diagonals waits for them (a fixed order of the updates).
+  PendingChunks pending, rpending;
+  cudaEvent_t ev_near1 = nullptr;   // after the last near products' stage 1
+  bool first_near = true;
   auto enqueue = [&]() -> cudaError_t {
     cudaError_t e;
     for (const Op& op : sch.ops) {
       if (op.kind == 2) {
-        // near products into diagonal op.D, after every deferred chunk that
-        // updates its tiles (a fixed order of the W~ updates)
+        // near products into diagonal op.D, after every chunk that writes
+        // its R tiles (stage 1) or its W~ tiles
         const Chunk& ch = sch.chunks[op.chunk0];
-        if ((e = pending.order_before(cs, op.D, op.D + 1)) != cudaSuccess) return e;
+        if (first_near) {
+          if ((e = cudaStreamWaitEvent(cs, ev_rzero, 0)) != cudaSuccess) return e;
+          first_near = false;
+        }
+        if ((e = rpending.order_before(cs, op.D, op.D + 1, true)) != cudaSuccess) return e;
+        if ((e = pending.order_before(cs, op.D, op.D + 1, true)) != cudaSuccess) return e;
         if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
-        float* ynh = (float*)(base + L.ynhi);
-        float* ynl = (float*)(base + L.ynlo);
         if (ch.n1 > 0) {
           cudaEvent_t ev = pt.begin();
-          if ((e = launch(stage1(ynh, ynl), ch.off1, ch.n1, ch.maxk1, cs)) != cudaSuccess) return e;
+          if ((e = launch(p1, ch.off1, ch.n1, ch.maxk1, cs)) != cudaSuccess) return e;
           pt.end(4, ev);
         }
+        if ((e = next_event(&ev_near1)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(ev_near1, cs)) != cudaSuccess) return e;
         if (ch.n > 0) {
           cudaEvent_t ev = pt.begin();
-          if ((e = launch(stage2(ynh, ynl), ch.off, ch.n, ch.maxk, cs)) != cudaSuccess) return e;
+          if ((e = launch(p2, ch.off, ch.n, ch.maxk, cs)) != cudaSuccess) return e;
           pt.end(4, ev);
         }
         continue;
       }
       if (op.kind == 0) {
-        if ((e = pending.order_before(cs, op.D, op.D + 1)) != cudaSuccess) return e;
+        if ((e = pending.order_before(cs, op.D, op.D + 1, true)) != cudaSuccess) return e;
         la.D = op.D;
         la.I0 = op.I0;
         // the first leaf reads the factors the kernel directly before it
@@ -1320,58 +1341,58 @@ bakron_status quantize_impl(const float* W, int64_t m, int64_t n, const float* U
         cudaEvent_t ev = pt.begin();
         if ((e = launch_leaf(la, op.ntiles, cs)) != cudaSuccess) return e;
         pt.end(0, ev);
-        if ((e = next_event(&ev_leaf)) != cudaSuccess) return e;
-        if ((e = cudaEventRecord(ev_leaf, cs)) != cudaSuccess) return e;
         continue;
       }
-      // propagation: starts after the leaf of its last source diagonal (the
-      // op directly before it); its first chunk on the depth's urgent
-      // stream, the others on the depth's side stream after the first
-      // chunk's stage 1 (they read its Y^T tiles too)
-      float* yhi = (float*)(base + L.yhi[op.depth]);
-      float* ylo = (float*)(base + L.ylo[op.depth]);
-      // Each chunk goes to a stream of the propagation's lane chosen by its
-      // slack, the leaves between the propagation's start (after leaf op.D)
-      // and its first target: the next leaf's chunk to the urgent stream, the
-      // chunks due within kMidSlack leaves to a middle-priority stream, the
-      // rest to the lowest; so far-off chunks of a large propagation cannot
-      // hold the SMs that a near deadline needs.  A chunk's stage 2 reads the
-      // Y^T tiles of every earlier chunk's stage 1: it waits for those on
-      // other streams.
+      // propagation: starts after the near products' stage 1 right before it
+      // (its sources' leaves have run and its source band's R tiles are
+      // complete).  Each chunk goes to a stream of the propagation's lane
+      // chosen by its slack, the leaves between the propagation's start
+      // (after leaf op.D) and its first target: the next leaf's chunk to the
+      // urgent stream, the chunks due within kMidSlack leaves to a
+      // middle-priority stream, the rest to the lowest; so far-off chunks of
+      // a large propagation cannot hold the SMs that a near deadline needs.
+      // The row updates (stage 1) and the pushes (stage 2) of a chunk write
+      // different tiles and read nothing the other writes; they share the
+      // class's stream (measured: separate streams were slower).
       cudaStream_t lane_str[3] = {ss->urg[op.depth], ss->mid[op.depth], ss->side[op.depth]};
       bool started[3] = {false, false, false};
-      cudaEvent_t s1_ev[3] = {nullptr, nullptr, nullptr};   // latest stage 1 per stream
+      auto stream_for = [&](int k, cudaStream_t* out) -> cudaError_t {
+        *out = lane_str[k];
+        if (started[k]) return cudaSuccess;
+        started[k] = true;
+        return cudaStreamWaitEvent(*out, ev_near1, 0);
+      };
       for (int c = 0; c < op.nchunks; ++c) {
         const Chunk& ch = sch.chunks[op.chunk0 + c];
         if (o.times) o.times->prop_flops += ch.flops1 + ch.flops;
         const int slack = ch.dlo - op.D - 1;
         const int k = slack <= 1 ? 0 : (slack <= kMidSlack ? 1 : 2);
-        cudaStream_t cstr = lane_str[k];
-        if (!started[k]) {
-          if ((e = cudaStreamWaitEvent(cstr, ev_leaf, 0)) != cudaSuccess) return e;
-          started[k] = true;
-        }
         if (ch.n1 > 0) {
+          cudaStream_t cstr;
+          if ((e = stream_for(k, &cstr)) != cudaSuccess) return e;
+          // after the earlier writers of the same R tiles (fixed order)
+          if ((e = rpending.order_before(cstr, ch.dlo, ch.dhi)) != cudaSuccess) return e;
           cudaEvent_t ev = pt.begin(cstr);
-          if ((e = launch(stage1(yhi, ylo), ch.off1, ch.n1, ch.maxk1, cstr)) != cudaSuccess) return e;
+          if ((e = launch(p1, ch.off1, ch.n1, ch.maxk1, cstr)) != cudaSuccess) return e;
           pt.end(1, ev, cstr);
-          if ((e = next_event(&s1_ev[k])) != cudaSuccess) return e;
-          if ((e = cudaEventRecord(s1_ev[k], cstr)) != cudaSuccess) return e;
+          cudaEvent_t done;
+          if ((e = next_event(&done)) != cudaSuccess) return e;
+          if ((e = cudaEventRecord(done, cstr)) != cudaSuccess) return e;
+          rpending.add(done, ch.dlo, ch.dhi);
         }
         if (ch.n > 0) {
-          for (int k2 = 0; k2 < 3; ++k2)
-            if (k2 != k && s1_ev[k2] && (e = cudaStreamWaitEvent(cstr, s1_ev[k2], 0)) != cudaSuccess)
-              return e;
+          cudaStream_t cstr;
+          if ((e = stream_for(k, &cstr)) != cudaSuccess) return e;
           // after the earlier updates of the same W~ tiles (fixed order)
           if ((e = pending.order_before(cstr, ch.dlo, ch.dhi)) != cudaSuccess) return e;
           cudaEvent_t ev = pt.begin(cstr);
-          if ((e = launch(stage2(yhi, ylo), ch.off, ch.n, ch.maxk, cstr)) != cudaSuccess) return e;
+          if ((e = launch(p2, ch.off, ch.n, ch.maxk, cstr)) != cudaSuccess) return e;
           pt.end(2, ev, cstr);
+          cudaEvent_t done;
+          if ((e = next_event(&done)) != cudaSuccess) return e;
+          if ((e = cudaEventRecord(done, cstr)) != cudaSuccess) return e;
+          pending.add(done, ch.dlo, ch.dhi);
         }
-        cudaEvent_t done;
-        if ((e = next_event(&done)) != cudaSuccess) return e;
-        if ((e = cudaEventRecord(done, cstr)) != cudaSuccess) return e;
-        pending.add(done, ch.dlo, ch.dhi);
       }
     }
     return cudaSuccess;

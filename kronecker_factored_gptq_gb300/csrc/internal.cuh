@@ -13,14 +13,6 @@ namespace bakron {
 
 constexpr int kTile = 128;          // tile edge T of the solver
 
-// Tile anti-diagonals the near products of the solve reach back: the errors of
-// diagonals D - BAKRON_NEAR_DIAGONALS .. D - 1 reach diagonal D on the
-// critical stream right before its leaf, every older diagonal's through a
-// propagation that runs beside the leaves in between.
-#ifndef BAKRON_NEAR_DIAGONALS
-#define BAKRON_NEAR_DIAGONALS 1
-#endif
-
 // Largest problems the entry points accept: at most kMaxTiles 128-tiles of W
 // (m n <= 2^34 elements, 64 GiB in fp32) and factor orders up to kMaxOrder.
 // The host work lists then stay below a few hundred MB, and no single GPU
@@ -86,10 +78,14 @@ struct PropArgs {
   const float* A_hi; const float* A_lo; int64_t lda;
   const float* B_hi; const float* B_lo; int64_t ldb;
   int64_t a_rows, b_rows;                      // rows of A and B (tensor maps)
-  float* out_hi; float* out_lo; int64_t ldo;   // stage 1: Y^T split
+  float* out_hi; float* out_lo; int64_t ldo;   // stage 1: output, split
+  float* acc;                                  // stage 1, nullable: fp32 accumulator
+                                               // (layout of out): C += acc, written
+                                               // back and split into out
   float* wt; int64_t ldw;                      // stage 2: W~ -= C
   const WorkItem* items; int n_items;
-  int stage;  // 1: out = split(alpha C) [and tr = split(alpha C)^T]; 2: wt -= C;
+  int stage;  // 1: out = split(alpha C) [and tr = split(alpha C)^T], or with acc:
+              //    acc += C, out = split(acc); 2: wt -= C;
               // 3: wt = alpha C (tensor cores only)
   int max_k;  // longest K range of the items, in tiles
   float alpha;                       // stage 1 scale (0 means 1)

@@ -3,8 +3,9 @@
 //
 // One CTA per work item: a 128 x 128 output tile C[r][c] = sum_k A[r][k] B[c][k]
 // over the item's K tiles, A and B read as (hi + lo) pairs, which restores
-// their exact fp32 values.  Stage 1 stores C split into (hi, lo) (that is Y^T
-// for stage 2); stage 2 subtracts C from the working matrix W~.
+// their exact fp32 values.  Stage 1 stores C split into (hi, lo), after
+// adding it to the fp32 accumulator when one is given (the row accumulators
+// of the solve); stage 2 subtracts C from the working matrix W~.
 #include "internal.cuh"
 
 namespace bakron {
@@ -79,6 +80,13 @@ __global__ void __launch_bounds__(256) prop_simt_kernel(PropArgs p) {
     for (int jh = 0; jh < 2; ++jh) {
       const int64_t c = c0 + jh * 64 + tx * 4;
       if (p.stage == 1) {
+        if (p.acc) {   // running sum: acc += C, then split
+          float4* ap = reinterpret_cast<float4*>(p.acc + r * p.ldo + c);
+          const float4 a0 = *ap;
+          acc[i][jh * 4 + 0] += a0.x; acc[i][jh * 4 + 1] += a0.y;
+          acc[i][jh * 4 + 2] += a0.z; acc[i][jh * 4 + 3] += a0.w;
+          *ap = make_float4(acc[i][jh * 4 + 0], acc[i][jh * 4 + 1], acc[i][jh * 4 + 2], acc[i][jh * 4 + 3]);
+        }
         float4 h, l;
         h.x = tf32_round(acc[i][jh * 4 + 0]); l.x = acc[i][jh * 4 + 0] - h.x;
         h.y = tf32_round(acc[i][jh * 4 + 1]); l.y = acc[i][jh * 4 + 1] - h.y;

@@ -31,8 +31,9 @@
 //     accumulators, two of each);
 //   warps 4-7: epilogue, TMEM -> registers (warp 4 + q owns TMEM lanes
 //     32q..32q+31, i.e. output rows) -> running fp32 sums -> global: stage 1
-//     writes C split into (hi, lo), stage 2 subtracts C from W~, stage 3
-//     writes alpha C plainly (the factor accumulation).
+//     writes C split into (hi, lo) (or, with an fp32 accumulator, adds C to
+//     it and writes the sum back and split), stage 2 subtracts C from W~,
+//     stage 3 writes alpha C plainly (the factor accumulation).
 // Every mbarrier wait is bounded (clock64 budget); on expiry the CTA records
 // BAKRON_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs (with a
 // bound again), frees TMEM and returns.
@@ -185,6 +186,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---------------- epilogue: running fp32 sums of the K-tile chunks
     const int q = warp - 4;                 // TMEM lane quarter (warp % 4)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    if (p.stage == 1 && p.acc) {
+      // the running sums this warp adds in at the end: into L2 now, while
+      // the tensor core works (32 rows x 512 bytes, four 128-byte lines each)
+      const float* ar = p.acc + ((int64_t)it.r * BM + q * 32 + lane) * p.ldo + (int64_t)it.c * BN;
+#pragma unroll
+      for (int l = 0; l < 4; ++l) asm volatile("prefetch.global.L2 [%0];" ::"l"(ar + 32 * l));
+    }
     float acc[BN];
 #pragma unroll
     for (int t = 0; t < BN; ++t) acc[t] = 0.f;
@@ -247,7 +255,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       const int64_t grow0 = (int64_t)it.r * BM + q * 32;
       const int64_t gcol = (int64_t)it.c * BN + 4 * lane;
-      if (p.stage == 1) {
+      if (p.stage == 1 && p.acc) {
+        // running sums: acc += C (the fp32 tile), written back, then split;
+        // all of the warp's loads in flight at once
+        float4 a0[32];
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          a0[rr] = *reinterpret_cast<const float4*>(p.acc + (grow0 + rr) * p.ldo + gcol);
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+          float4 v = *reinterpret_cast<const float4*>(stg + rr * SPITCH + 4 * lane);
+          v.x += a0[rr].x; v.y += a0[rr].y; v.z += a0[rr].z; v.w += a0[rr].w;
+          *reinterpret_cast<float4*>(p.acc + (grow0 + rr) * p.ldo + gcol) = v;
+          float4 h, l;
+          h.x = tf32_round(v.x); l.x = tf32_round(v.x - h.x);
+          h.y = tf32_round(v.y); l.y = tf32_round(v.y - h.y);
+          h.z = tf32_round(v.z); l.z = tf32_round(v.z - h.z);
+          h.w = tf32_round(v.w); l.w = tf32_round(v.w - h.w);
+          *reinterpret_cast<float4*>(p.out_hi + (grow0 + rr) * p.ldo + gcol) = h;
+          *reinterpret_cast<float4*>(p.out_lo + (grow0 + rr) * p.ldo + gcol) = l;
+        }
+      } else if (p.stage == 1) {
 #pragma unroll 4
         for (int rr = 0; rr < 32; ++rr) {
           const float4 v = *reinterpret_cast<const float4*>(stg + rr * SPITCH + 4 * lane);

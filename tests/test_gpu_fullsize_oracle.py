@@ -16,7 +16,7 @@ certificate of ``test_gpu_workloads.py``:
   codes only at its own near ties (within 1e-4 grid units of a rounding
   boundary), must reproduce every code, with at most 0.1% guided decisions;
   V = s c exactly; the proxy loss ||L(B)(V-W)L(A)^T||_F^2 of the GPU output
-  within 1e-3 relative of the unguided oracle's;
+  within FULL_LOSS_RTOL relative of the unguided oracle's (see below);
 * the GPU's own factor preparation against the oracle's fp64 factors, within
   10 n eps cond (the forward error bound of the Cholesky and triangular
   inverse), cond from Lanczos estimates of the extreme eigenvalues.
@@ -31,9 +31,19 @@ import pytest
 import oracle as O
 from kronecker_factored_gptq_gb300 import workloads as WL
 
-from _gpu_helpers import TOL, MAX_FRAC, LOSS_RTOL, to_dev
+from _gpu_helpers import TOL, MAX_FRAC, to_dev
 
 pytestmark = pytest.mark.gpu
+
+# Once one near-tie decision goes the other way (both are correct roundings),
+# every later entry sees a different error history: the GPU's trajectory and
+# the unguided oracle's are two valid GPTQ runs, and at these sizes their
+# losses drift apart by more than 1e-3.  Measured with the oracle alone on the
+# 14336 x 4096 workload (seed 0): perturbing W by 1e-7 and 1e-6 relative
+# moved the loss by 1.7e-3 and 2.4e-3 (29% and 36% of the codes changed).
+# The bound is twice the larger drift; the codes themselves are checked
+# exactly against the guided oracle.
+FULL_LOSS_RTOL = 5e-3
 
 FULL = ["c4096", "mlp4096x14336", "mlp14336x4096", "c8192"]
 RB = 8   # rows per block of the oracle's row-blocked traversal
@@ -82,7 +92,7 @@ def test_whole_solve_matches_oracle(case):
         ref = O.rowacc(w.W, UA, UB, s, w.qmin, w.qmax, rows_per_block=RB)
         V_ref = (s[:, None] * ref.codes.astype(np.float32)).astype(np.float32)
         l_ref = O.proxy_loss(w.W, V_ref, LA, LB)
-    assert abs(l_gpu - l_ref) <= LOSS_RTOL * abs(l_ref), (w.name, l_gpu, l_ref)
+    assert abs(l_gpu - l_ref) <= FULL_LOSS_RTOL * abs(l_ref), (w.name, l_gpu, l_ref)
 
 
 def _cond_estimate(Ad, U):

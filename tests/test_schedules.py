@@ -3,26 +3,30 @@ from the C ABI (bakron_schedule_export), the checks from the method.
 
 Two-sided solve (summary page "FastKron: Efficient Quantization with
 Kronecker-Factored Hessians", the derivation of BaKron-antidiagonal and of the
-divide and conquer over anti-diagonals): the error of tile (I, J) reaches every tile
-(I', J') with I' >= I, J' >= J, through Y[I][J'] = sum_J E[I][J] U_A[J][J']
-(stage 1) and W~[I'][J'] -= sum_I U_B[I][I']^T Y[I][J'] (stage 2).  The
-schedule must apply each (source, target) contribution exactly once, from a
-source whose leaf has run, before the leaf of the target: pairs on
-neighbouring tile diagonals through the near products issued between the two
-leaves, every other pair through a propagation that starts after the leaf of
-its last source.  One-sided solve (B = I): the same over column tiles.
+divide and conquer over anti-diagonals): the error of tile (I, J) reaches every
+tile (I', J') with I' >= I, J' >= J through the row accumulator
+R[I][J'] = sum_J E[I][J] U_A[J][J'] (stage 1 adds row updates into R, which
+lives for the whole solve) and W~[I'][J'] -= U_B[I][I']^T R[I][J'] (stage 2,
+R complete for I < I', R over J < J' for I = I').  The schedule must apply
+each (source, target) contribution exactly once, from a source whose leaf has
+run, before the leaf of the target: pairs on neighbouring tile diagonals
+through the near products issued between the two leaves, every other pair
+through a propagation that starts after the leaf of its last source.
+One-sided solve (B = I): the same over column tiles.
 Preparation: the blocked Cholesky's trailing updates and the
 recursive-doubling inverse.
 
 The stream model mirrors the executor's rules in csrc/api.cu: leaves and near
 products on the critical stream; a propagation's chunks on its lane's urgent,
 middle or lowest-priority stream by their slack, each stream starting after
-the leaf before the propagation; every chunk's stage 2 after the earlier
-chunks' stage 1 on the other streams and after the chunks enqueued earlier
-that update any of the same diagonals, and every near product and leaf after
-the chunks that update its diagonal.  The checks then require every update of a W~ tile (so
-their fp32 order is fixed), every Y tile's writer and readers, and every E
-tile's producer and readers to be ordered by stream order and events.
+the near products' stage 1 before the propagation; every chunk's stage 1
+after the chunks enqueued earlier that write R tiles of the same diagonals,
+its stage 2 after those that update W~ tiles of the same diagonals, and every
+near product after both kinds for its diagonal, every leaf after the W~
+updates of its diagonal.  The checks then require every update of a W~ or an
+R tile (so their fp32 order is fixed) to form one chain, every R tile's
+readers to sit between the writers enqueued before and after them, and every
+E tile's producer and readers to be ordered by stream order and events.
 """
 
 import numpy as np
@@ -94,36 +98,41 @@ MID_SLACK = 15   # the executor's middle-priority bound (csrc/api.cu, kMidSlack)
 
 def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
     """Builds the stream model and returns (S, accesses) where accesses maps
-    ('W', tile) / ('Y', buffer, tile) / ('E', tile) to [(node, 'r'|'w')].
-    With wait_at_propagation False, propagation chunks skip the waits for
-    earlier chunks of the same diagonals (the sensitivity check)."""
+    ('W', tile) / ('R', tile) / ('E', tile) to [(node, 'r'|'w')].  With
+    wait_at_propagation False, propagation chunks skip the waits for earlier
+    chunks of the same diagonals (the sensitivity check)."""
     S = Streams()
     acc = {}
 
     def touch(key, node, mode):
         acc.setdefault(key, []).append((node, mode))
 
-    pending = []   # (event node, dlo, dhi)
+    pending = []    # W~ writers: (event node, dlo, dhi)
+    rpending = []   # R writers
 
-    def order_before(stream, lo, hi):
+    crit_waited = set()   # events the critical stream already waited for
+
+    def order_before(lst, stream, lo, hi):
         keep = []
-        for ev, dlo, dhi in pending:
+        for ev, dlo, dhi in lst:
             overlap = dlo < hi and dhi > lo
-            if overlap:
+            if overlap and not (stream == "cs" and ev in crit_waited):
                 S.wait(stream, ev)
+                if stream == "cs":
+                    crit_waited.add(ev)
             if not (overlap and lo <= dlo and dhi <= hi):
                 keep.append((ev, dlo, dhi))
-        pending[:] = keep
+        lst[:] = keep
 
-    def stage1(stream, buf, its):
+    def stage1(stream, its):
         n = S.node(stream)
         for Jp, I, k0, k1 in its:
-            touch(("Y", buf, (I, Jp)), n, "w")
+            touch(("R", (I, Jp)), n, "w")   # read-modify-write of the fp32 sums
             for J in range(k0, k1):
                 touch(("E", (I, J)), n, "r")
         return n
 
-    def stage2(stream, buf, its):
+    def stage2(stream, its):
         n = S.node(stream)
         for Ip, Jp, k0, k1 in its:
             touch(("W", (Ip, Jp)), n, "w")
@@ -131,13 +140,14 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
                 if one_sided:
                     touch(("E", (Ip, I)), n, "r")
                 else:
-                    touch(("Y", buf, (I, Jp)), n, "r")
+                    touch(("R", (I, Jp)), n, "r")
         return n
 
     ev_leaf = None
+    ev_near1 = None
     for kind, D, I0, ntiles, depth, chunk0, nchunks in ops.tolist():
         if kind == 0:
-            order_before("cs", D, D + 1)
+            order_before(pending, "cs", D, D + 1)
             n = S.node("cs")
             if one_sided:
                 tiles = [(I, D) for I in range(ntiles)]
@@ -150,51 +160,56 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
             continue
         if kind == 2:
             dlo, dhi, off1, n1, off, nn = chunks[chunk0].tolist()
-            order_before("cs", D, D + 1)
+            order_before(rpending, "cs", D, D + 1)
+            order_before(pending, "cs", D, D + 1)
             if n1 > 0:
-                stage1("cs", "near", items[off1:off1 + n1].tolist())
+                stage1("cs", items[off1:off1 + n1].tolist())
+            ev_near1 = S.record("cs")
             if nn > 0:
-                stage2("cs", "near", items[off:off + nn].tolist())
+                stage2("cs", items[off:off + nn].tolist())
             continue
         if one_sided:
             # one-sided path: first chunk on the critical stream, waits for the
             # deferred chunks of the same columns before it
             if wait_at_propagation and nchunks > 0:
-                order_before("cs", chunks[chunk0][0], chunks[chunk0 + nchunks - 1][1])
+                order_before(pending, "cs", chunks[chunk0][0], chunks[chunk0 + nchunks - 1][1])
             for c in range(nchunks):
                 dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
                 stream = "cs" if c == 0 else "side%d" % depth
                 if c == 1:
                     S.wait(stream, S.record("cs"))
                 if nn > 0:
-                    stage2(stream, depth, items[off:off + nn].tolist())
+                    stage2(stream, items[off:off + nn].tolist())
                 if c > 0:
                     pending.append((S.record(stream), dlo, dhi))
             continue
         # the chunk's stream by its slack (leaves between the propagation's
         # start, after leaf D, and its first target), as the executor does
-        streams = ["urg%d" % depth, "mid%d" % depth, "side%d" % depth]
-        started = [False, False, False]
-        s1ev = [None, None, None]
+        started = set()
+
+        def stream_for(h, k):
+            name = ["urg", "mid", "side"][k] + "%d" % depth
+            if name not in started:
+                S.wait(name, ev_near1)
+                started.add(name)
+            return name
+
         for c in range(nchunks):
             dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
             slack = dlo - D - 1
             k = 0 if slack <= 1 else (1 if slack <= MID_SLACK else 2)
-            stream = streams[k]
-            if not started[k]:
-                S.wait(stream, ev_leaf)
-                started[k] = True
             if n1 > 0:
-                stage1(stream, depth, items[off1:off1 + n1].tolist())
-                s1ev[k] = S.record(stream)
-            if nn > 0:
-                for k2 in range(3):
-                    if k2 != k and s1ev[k2] is not None:
-                        S.wait(stream, s1ev[k2])
+                stream = stream_for(0, k)
                 if wait_at_propagation:
-                    order_before(stream, dlo, dhi)
-                stage2(stream, depth, items[off:off + nn].tolist())
-            pending.append((S.record(stream), dlo, dhi))
+                    order_before(rpending, stream, dlo, dhi)
+                stage1(stream, items[off1:off1 + n1].tolist())
+                rpending.append((S.record(stream), dlo, dhi))
+            if nn > 0:
+                stream = stream_for(1, k)
+                if wait_at_propagation:
+                    order_before(pending, stream, dlo, dhi)
+                stage2(stream, items[off:off + nn].tolist())
+                pending.append((S.record(stream), dlo, dhi))
     return S, acc
 
 
@@ -203,16 +218,15 @@ def ordering_violations(S, acc):
     for key, lst in acc.items():
         lst = sorted(set(lst))
         writers = [n for n, m in lst if m == "w"]
-        if key[0] == "W":
-            # every read-modify-write of a W~ tile (updates and the leaf) in
-            # one chain
+        if key[0] in ("W", "R"):
+            # every read-modify-write of a W~ tile (updates and the leaf) or
+            # of an R tile (row updates) in one chain
             for a_, b_ in zip(writers, writers[1:]):
                 if not S.before(a_, b_):
                     bad.append((key, a_, b_))
-        else:
+        if key[0] != "W":
             # each reader after the latest writer enqueued before it, and
-            # before the next writer (Y buffers are reused across
-            # propagations of the same depth)
+            # before the next writer
             for n, m in lst:
                 if m != "r":
                     continue
@@ -226,10 +240,13 @@ def ordering_violations(S, acc):
 
 
 def contributions_solve(ops, chunks, items, M, N):
-    """count[Ip, Jp, I, J]: times the error of tile (I, J) reaches (Ip, Jp);
-    also checks each contribution's source leaf precedes the products that
-    read it and its target lies in the chunk's target range and after them."""
+    """count[Ip, Jp, I, J]: times the error of tile (I, J) reaches (Ip, Jp),
+    following the row accumulators in the order the schedule lists their
+    updates and reads (the stream model checks that execution keeps that
+    order); also checks each product's sources are finished, its outputs lie
+    in its chunk's range and its targets are not."""
     count = np.zeros((M, N, M, N), dtype=np.int32)
+    rsum = {}        # R tile (I, J') -> source columns J added so far
     last_leaf = -1   # leaves run in diagonal order
     for kind, D, a2, a3, depth, chunk0, nchunks in ops.tolist():
         if kind == 0:
@@ -243,26 +260,31 @@ def contributions_solve(ops, chunks, items, M, N):
             assert D == last_leaf, "a propagation starts right after its last source's leaf"
             s0, s1 = a2, a3
             assert s1 == D + 1
-        yset = {}
         for c in range(nchunks):
             dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
             if kind == 2:
                 assert (dlo, dhi) == (D, D + 1)
+            seen = set()
             for Jp, I, k0, k1 in items[off1:off1 + n1].tolist():
-                assert (I, Jp) not in yset, "Y tile computed twice in one propagation"
+                assert (I, Jp) not in seen, "R tile updated twice in one launch"
+                seen.add((I, Jp))
                 assert 0 <= k0 < k1 <= Jp + 1
                 assert I + k1 - 1 <= last_leaf, "stage 1 reads an unfinished source"
                 if kind == 1:
+                    assert dlo <= I + Jp < dhi, "R tile outside its chunk's range"
                     assert s0 <= I + k0 and I + k1 - 1 < s1, "source outside the band"
-                yset[(I, Jp)] = (c, k0, k1)
+                else:
+                    assert I + Jp in (D - 1, D)
+                rsum.setdefault((I, Jp), []).extend(range(k0, k1))
             for Ip, Jp, k0, k1 in items[off:off + nn].tolist():
                 assert dlo <= Ip + Jp < dhi, "stage-2 target outside its chunk's range"
                 assert Ip + Jp > last_leaf, "stage 2 updates a finished tile"
                 assert 0 <= k0 < k1 <= Ip + 1
                 for I in range(k0, k1):
-                    cy, j0, j1 = yset[(I, Jp)]
-                    assert cy <= c, "stage 2 reads a Y tile of a later chunk"
-                    count[Ip, Jp, I, j0:j1] += 1
+                    if kind == 1:
+                        assert s0 <= I + Jp < s1, "pushed R tile outside the band"
+                    for J in rsum.get((I, Jp), []):
+                        count[Ip, Jp, I, J] += 1
     return count
 
 
@@ -309,21 +331,23 @@ def test_solve_streams_order_every_tile_access(M, N):
 def test_solve_streams_without_the_propagation_wait_overlap():
     """The checker is sensitive: without the waits of a propagation chunk for
     the earlier chunks of the same diagonals, two propagations can update the
-    same W~ tiles concurrently.  The stage-2 updates are atomic adds, so that
-    was correct, but the order of the adds, and with it the fp32 rounding of
-    W~, could change from run to run; ordered updates make the solve
-    bit-reproducible."""
-    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, 4, 4))
+    same W~ tiles, or the same row accumulator tiles, concurrently.  The
+    stage-2 updates are atomic adds, so for W~ that was correct but the order
+    of the adds, and with it the fp32 rounding, could change from run to run;
+    the row accumulators are read-modify-written and need the order outright.
+    Ordered updates make the solve bit-reproducible."""
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, 8, 8))
     S, acc = model_solve(ops, chunks, items, wait_at_propagation=False)
     bad = ordering_violations(S, acc)
-    assert bad and all(b[0][0] == "W" for b in bad)
+    assert bad and {b[0][0] for b in bad} <= {"W", "R"}
 
 
 @pytest.mark.parametrize("M,N", [(9, 7), (4, 4), (16, 13)])
 def test_solve_near_products_reach_a_fixed_depth(M, N):
     """The near products issued between leaf D - 1 and leaf D read the
-    diagonals D - h .. D - 1 (h the same for every D) and write only diagonal
-    D; every propagation's sources are at least h + 1 diagonals before its
+    diagonals D - h .. D - 1 (h the same for every D) and update the W~ tiles
+    of diagonal D only; every propagation's sources are at least h + 1
+    diagonals before its
     first target, so it can start h leaves early; no propagation sits
     between two leaves on the critical stream."""
     ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
