@@ -548,7 +548,7 @@ def run_ours(args, world, rank, local):
                                                           else "bakron_fma_probe"),
                 "algorithmic_flops_per_launch": per_launch, "avg_launch_ms": per_launch_ms,
                 "traffic": (traffic_per_launch("kronecker_factored_gptq_gb300/csrc/prop_tc.cu",
-                                               "profiles/prop_tc_kernel_c4096_traffic.md")
+                                               "profiles/prop_tc_kernel_c8192_traffic.md")
                             if kernel != "leaf_kernel" and use_tc else None),
                 "traffic_unit": "bytes per launch (ncu dram read + write, see profiles/)",
                 "launches_per_step": launches_per_step,
