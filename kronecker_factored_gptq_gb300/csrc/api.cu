@@ -219,14 +219,17 @@ Op build_near(Schedule& s, int D) {
 }
 
 // The propagations of the recursion, each filed under its last source
-// diagonal.  A wide source band is split into parts of about kSplitWidth
-// diagonals, propagated separately: the pairs are partitioned by source, so
-// each still reaches every target once, and each part starts right after the
-// leaf of its own last source.  The first part of the top-level band can
-// then run beside dozens of leaves instead of one; the price is the
-// stage-2 work repeated per part.
+// diagonal.  A wide source band is split into up to four parts of about
+// kSplitWidth diagonals, propagated separately: both kinds of pairs are
+// partitioned by their source diagonal (a row update by its error tile, a
+// push by its accumulator tile), so each pair is still handled once and no
+// work repeats, and each part starts right after the near products that
+// follow its own last source.  The early parts of a wide band then run
+// beside many leaves, and the part due at the band's first target has at
+// most kSplitWidth-deep products (measured at 8192^2: width 16 17.8 ms,
+// 8 and 32 17.9 ms, no split 18.0 ms).
 #ifndef BAKRON_SPLIT_WIDTH
-#define BAKRON_SPLIT_WIDTH 0
+#define BAKRON_SPLIT_WIDTH 16
 #endif
 constexpr int kSplitWidth = BAKRON_SPLIT_WIDTH;   // 0: no split
 
