@@ -188,6 +188,9 @@ cudaError_t launch_leaf(const LeafArgs& a, int n_tiles, cudaStream_t s);
 cudaError_t launch_rows_leaf(const LeafArgs& a, int n_row_tiles, cudaStream_t s);
 cudaError_t launch_prop_simt(const PropArgs& p, cudaStream_t s);
 cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s);
+// Two item lists (for instance a chunk's row updates and its pushes, which
+// touch different tiles) in one launch: a's CTAs first, then b's.
+cudaError_t launch_prop_tc2(const PropArgs& a, const PropArgs& b, cudaStream_t s);
 bool prop_tc_supported();
 
 // antidiag

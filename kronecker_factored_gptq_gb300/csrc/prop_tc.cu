@@ -59,10 +59,23 @@ constexpr uint32_t kIdesc = tc::idesc_tf32(BM, BN);
 
 }  // namespace
 
+// Two item lists in one launch: CTAs [0, n_first) take list 0 (maps m0,
+// arguments p0), the rest list 1 (m1, p1); a single list passes n_first =
+// its length.
 __global__ void __launch_bounds__(NTHREADS, 1)
-    prop_tc_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
-                   const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
-                   PropArgs p, DevStatus* st) {
+    prop_tc_kernel(const __grid_constant__ CUtensorMap m0_ahi, const __grid_constant__ CUtensorMap m0_alo,
+                   const __grid_constant__ CUtensorMap m0_bhi, const __grid_constant__ CUtensorMap m0_blo,
+                   const __grid_constant__ CUtensorMap m1_ahi, const __grid_constant__ CUtensorMap m1_alo,
+                   const __grid_constant__ CUtensorMap m1_bhi, const __grid_constant__ CUtensorMap m1_blo,
+                   const __grid_constant__ PropArgs p0, const __grid_constant__ PropArgs p1, int n_first,
+                   DevStatus* st) {
+  const bool second = (int)blockIdx.x >= n_first;
+  const PropArgs& p = second ? p1 : p0;
+  const CUtensorMap& tm_ahi = second ? m1_ahi : m0_ahi;
+  const CUtensorMap& tm_alo = second ? m1_alo : m0_alo;
+  const CUtensorMap& tm_bhi = second ? m1_bhi : m0_bhi;
+  const CUtensorMap& tm_blo = second ? m1_blo : m0_blo;
+  const int item = second ? (int)blockIdx.x - n_first : (int)blockIdx.x;
   extern __shared__ __align__(1024) unsigned char dsm[];
   __shared__ __align__(8) unsigned long long bar_full[STAGES], bar_empty[STAGES];
   __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2], bar_done;
@@ -70,7 +83,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WorkItem it = p.items[blockIdx.x];
+  const WorkItem it = p.items[item];
   if (!item_in_bounds(it, p)) {   // uniform over the CTA: nothing set up yet
     if (threadIdx.x == 0) set_status(st, BAKRON_ERR_INVALID_ARG);
     return;
@@ -377,18 +390,36 @@ bool prop_tc_supported() {
   return ok;
 }
 
-cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s) {
-  if (p.n_items == 0) return cudaSuccess;
+namespace {
+bool make_maps(CUtensorMap* m, const PropArgs& p) {
+  return make_map(&m[0], p.A_hi, p.a_rows, p.lda) && make_map(&m[1], p.A_lo, p.a_rows, p.lda) &&
+         make_map(&m[2], p.B_hi, p.b_rows, p.ldb) && make_map(&m[3], p.B_lo, p.b_rows, p.ldb);
+}
+}  // namespace
+
+cudaError_t launch_prop_tc2(const PropArgs& a, const PropArgs& b, cudaStream_t s) {
+  if (a.n_items + b.n_items == 0) return cudaSuccess;
   static std::atomic<unsigned long long> done;
   cudaError_t e = ensure_smem_limit((const void*)prop_tc_kernel, kSmem, done);
   if (e != cudaSuccess) return e;
-  CUtensorMap ahi, alo, bhi, blo;
-  if (!make_map(&ahi, p.A_hi, p.a_rows, p.lda) || !make_map(&alo, p.A_lo, p.a_rows, p.lda) ||
-      !make_map(&bhi, p.B_hi, p.b_rows, p.ldb) || !make_map(&blo, p.B_lo, p.b_rows, p.ldb))
-    return cudaErrorInvalidValue;
+  CUtensorMap ma[4], mb[4];
+  if (!make_maps(ma, a)) return cudaErrorInvalidValue;
+  if (b.n_items > 0) {
+    if (!make_maps(mb, b)) return cudaErrorInvalidValue;
+  } else {
+    for (int i = 0; i < 4; ++i) mb[i] = ma[i];
+  }
   count_launch();
-  return launch_kernel(prop_tc_kernel, dim3(p.n_items), dim3(NTHREADS), kSmem, s, p.pdl != 0, ahi, alo,
-                       bhi, blo, p, p.st);
+  return launch_kernel(prop_tc_kernel, dim3((unsigned)(a.n_items + b.n_items)), dim3(NTHREADS), kSmem, s,
+                       a.pdl != 0, ma[0], ma[1], ma[2], ma[3], mb[0], mb[1], mb[2], mb[3], a,
+                       b.n_items > 0 ? b : a, a.n_items, a.st);
+}
+
+cudaError_t launch_prop_tc(const PropArgs& p, cudaStream_t s) {
+  if (p.n_items == 0) return cudaSuccess;
+  PropArgs none = p;
+  none.n_items = 0;
+  return launch_prop_tc2(p, none, s);
 }
 
 }  // namespace bakron

@@ -21,7 +21,8 @@ products on the critical stream; a propagation's chunks on its lane's urgent,
 middle or lowest-priority stream by their slack, each stream starting after
 the near products' stage 1 before the propagation; every chunk's stage 1
 after the chunks enqueued earlier that write R tiles of the same diagonals,
-its stage 2 after those that update W~ tiles of the same diagonals, and every
+its stage 2 after those that update W~ tiles of the same diagonals (a chunk
+with both stages launches them together, after both kinds), and every
 near product after both kinds for its diagonal, every leaf after the W~
 updates of its diagonal.  The checks then require every update of a W~ or an
 R tile (so their fp32 order is fixed) to form one chain, every R tile's
@@ -94,6 +95,7 @@ class Streams:
 
 
 MID_SLACK = 15   # the executor's middle-priority bound (csrc/api.cu, kMidSlack)
+FUSE_CLASS = 2   # classes whose chunks launch both stages together (kFuseClass)
 
 
 def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
@@ -124,16 +126,16 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
                 keep.append((ev, dlo, dhi))
         lst[:] = keep
 
-    def stage1(stream, its):
-        n = S.node(stream)
+    def stage1(stream, its, n=None):
+        n = S.node(stream) if n is None else n
         for Jp, I, k0, k1 in its:
             touch(("R", (I, Jp)), n, "w")   # read-modify-write of the fp32 sums
             for J in range(k0, k1):
                 touch(("E", (I, J)), n, "r")
         return n
 
-    def stage2(stream, its):
-        n = S.node(stream)
+    def stage2(stream, its, n=None):
+        n = S.node(stream) if n is None else n
         for Ip, Jp, k0, k1 in its:
             touch(("W", (Ip, Jp)), n, "w")
             for I in range(k0, k1):
@@ -198,6 +200,19 @@ def model_solve(ops, chunks, items, one_sided=False, wait_at_propagation=True):
             dlo, dhi, off1, n1, off, nn = chunks[chunk0 + c].tolist()
             slack = dlo - D - 1
             k = 0 if slack <= 1 else (1 if slack <= MID_SLACK else 2)
+            if k <= FUSE_CLASS and n1 > 0 and nn > 0:
+                # one launch holds both stages: one node touching both lists
+                stream = stream_for(0, k)
+                if wait_at_propagation:
+                    order_before(rpending, stream, dlo, dhi)
+                    order_before(pending, stream, dlo, dhi)
+                node = S.node(stream)
+                stage1(stream, items[off1:off1 + n1].tolist(), node)
+                stage2(stream, items[off:off + nn].tolist(), node)
+                ev = S.record(stream)
+                rpending.append((ev, dlo, dhi))
+                pending.append((ev, dlo, dhi))
+                continue
             if n1 > 0:
                 stream = stream_for(0, k)
                 if wait_at_propagation:
