@@ -295,13 +295,28 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   __syncthreads();
   for (int idx = tid; idx < NB * (NB - 1) * S * PP; idx += NTHR) Pt[idx] = 0.f;
   grid_dep_wait();
-#pragma unroll 4
-  for (int idx = tid; idx < T * T / 4; idx += NTHR) {
-    const int r = idx >> 5, c = (idx & 31) * 4;
+  // W~: block (0, 0) now, the rest by the warps that do not sweep level 0
+  // (they are idle until its barrier, and nothing else reads the tile before)
+  if (tid < S * S / 4) {
+    const int r = tid / (S / 4), c = (tid % (S / 4)) * 4;
     *reinterpret_cast<float4*>(X + r * PX + c) =
         *reinterpret_cast<const float4*>(a.wt + (i0 + r) * a.ldw + j0 + c);
   }
   __syncthreads();
+  // E of one 16-byte group q of block (I, J), split, to the error arrays
+  auto write_e = [&](int I, int J, int q) {
+    const int r = S * I + q / (S / 4), cc = S * J + (q % (S / 4)) * 4;
+    const float4 e = *reinterpret_cast<const float4*>(X + r * PX + cc);
+    float4 h, l;
+    h.x = tf32_round(e.x); h.y = tf32_round(e.y); h.z = tf32_round(e.z); h.w = tf32_round(e.w);
+    l.x = e.x - h.x; l.y = e.y - h.y; l.z = e.z - h.z; l.w = e.w - h.w;
+    if (a.round_lo) {
+      l.x = tf32_round(l.x); l.y = tf32_round(l.y); l.z = tf32_round(l.z); l.w = tf32_round(l.w);
+    }
+    const int64_t g = (i0 + r) * a.ldw + j0 + cc;
+    *reinterpret_cast<float4*>(a.e_hi + g) = h;
+    *reinterpret_cast<float4*>(a.e_lo + g) = l;
+  };
 
   const float fqmin = (float)a.qmin, fqmax = (float)a.qmax;
   bool nonfinite = false, out_of_range = false;
@@ -499,6 +514,23 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
           }
         }
       }
+    } else if (k == 0) {
+      // the rest of the W~ tile (everything but block (0, 0))
+      for (int idx = tid - 32 * nsw; idx < T * T / 4; idx += NTHR - 32 * nsw) {
+        const int r = idx >> 5, c = (idx & 31) * 4;
+        if (r < S && c < S) continue;
+        *reinterpret_cast<float4*>(X + r * PX + c) =
+            *reinterpret_cast<const float4*>(a.wt + (i0 + r) * a.ldw + j0 + c);
+      }
+    } else if (warp >= nsw + NDEF) {
+      // the errors of level k-1's blocks are final (later steps only read
+      // them): out to the error arrays while this level sweeps
+      const int kp = k - 1, Ipmin = level_imin(kp, NB), npb = level_imax(kp, NB) - Ipmin + 1;
+      const int nthr = NTHR - 32 * (nsw + NDEF);
+      for (int t = tid - 32 * (nsw + NDEF); t < npb * (S * S / 4); t += nthr) {
+        const int I = Ipmin + t / (S * S / 4);
+        write_e(I, kp - I, t % (S * S / 4));
+      }
     } else if (k >= 1 && warp < nsw + NDEF) {
       // ---- deferred pushes of level k-1 into levels >= k+1, on NDEF of the
       // other warps (more would take issue and shared-memory bandwidth from
@@ -533,20 +565,9 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   if (nonfinite) set_status(a.st, BAKRON_ERR_NONFINITE);
   if (out_of_range) set_status(a.st, BAKRON_ERR_CODE_RANGE);
 
-  // write-out: scaled errors (split) for the propagation
-  for (int idx = tid; idx < T * T / 4; idx += NTHR) {
-    const int r = idx >> 5, cc = (idx & 31) * 4;
-    const float4 e = *reinterpret_cast<const float4*>(X + r * PX + cc);
-    float4 h, l;
-    h.x = tf32_round(e.x); h.y = tf32_round(e.y); h.z = tf32_round(e.z); h.w = tf32_round(e.w);
-    l.x = e.x - h.x; l.y = e.y - h.y; l.z = e.z - h.z; l.w = e.w - h.w;
-    if (a.round_lo) {
-      l.x = tf32_round(l.x); l.y = tf32_round(l.y); l.z = tf32_round(l.z); l.w = tf32_round(l.w);
-    }
-    const int64_t g = (i0 + r) * a.ldw + j0 + cc;
-    *reinterpret_cast<float4*>(a.e_hi + g) = h;
-    *reinterpret_cast<float4*>(a.e_lo + g) = l;
-  }
+  // write-out: the errors of the last level's block (the earlier levels'
+  // went out while the next level swept)
+  if (tid < S * S / 4) write_e(NB - 1, NB - 1, tid);
 }
 
 namespace {
