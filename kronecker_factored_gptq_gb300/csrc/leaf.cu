@@ -303,10 +303,14 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         *reinterpret_cast<const float4*>(a.wt + (i0 + r) * a.ldw + j0 + c);
   }
   __syncthreads();
-  // E of one 16-byte group q of block (I, J), split, to the error arrays
+  bool nonfinite = false, out_of_range = false;
+  // E of one 16-byte group q of block (I, J), split, to the error arrays.  A
+  // non-finite pre-rounding value gives a non-finite error (and so does an
+  // error that overflows), so the check runs here, off the sweep's steps.
   auto write_e = [&](int I, int J, int q) {
     const int r = S * I + q / (S / 4), cc = S * J + (q % (S / 4)) * 4;
     const float4 e = *reinterpret_cast<const float4*>(X + r * PX + cc);
+    nonfinite |= !isfinite(e.x) || !isfinite(e.y) || !isfinite(e.z) || !isfinite(e.w);
     float4 h, l;
     h.x = tf32_round(e.x); h.y = tf32_round(e.y); h.z = tf32_round(e.z); h.w = tf32_round(e.w);
     l.x = e.x - h.x; l.y = e.y - h.y; l.z = e.z - h.z; l.w = e.w - h.w;
@@ -319,7 +323,6 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
   };
 
   const float fqmin = (float)a.qmin, fqmax = (float)a.qmax;
-  bool nonfinite = false, out_of_range = false;
 
   // Grid scale and zero point of the row and block this thread sweeps at
   // level kk (lane = (sub, row) of block slot BPW warp + sub; a slot past
@@ -450,7 +453,6 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         c = fminf(fmaxf(c, clo), chi);
         const float e = act ? (x - sc * c) * lBa * la : 0.f;
         const float code = c + zc;
-        nonfinite |= act && !isfinite(x);
         if (CHK) out_of_range |= act && ((code < -128.f) || (code > 127.f));
         if (d + 1 < NSTEP) FR[d + 1] += pnext;
         FR[d] = fmaf(e, dv[0].x, FR[d]);
