@@ -459,7 +459,8 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         rlast = FR[d];
         if (act) {
           Xrow[b] = e;
-          csr[b] = (signed char)(int)fminf(fmaxf(code, -128.f), 127.f);
+          // without CHK the grid keeps every code inside the int8 range
+          csr[b] = (signed char)(int)(CHK ? fminf(fmaxf(code, -128.f), 127.f) : code);
           rs[b * PR + row] = FR[d];
         }
         if (PRE && act && row_real && jb0 + b < a.n) a.preround[gi * a.n + jb0 + b] = x;
