@@ -423,8 +423,11 @@ __global__ void __launch_bounds__(NTHR, 1) leaf_kernel(LeafArgs a) {
         // rows a' < a - 1, all completed by the previous step; it is off this
         // step's dependency chain.  A lane active next step has a <= d + 1,
         // so only the rows a' <= d - 1 can count (ub is zero past a - 2).
+        // A lane inactive next step (bn outside 0 .. S-1) reads other shared
+        // data here (at most 13 rows before the slot, 14 past it: still
+        // inside the P, rT and Dg areas) and never uses the sum.
         const int bn = b + 1;
-        const float* rc = rs + ((unsigned)bn < (unsigned)S ? bn : S) * PR;
+        const float* rc = rs + bn * PR;
         float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
         for (int c = 0; c < S / 4; ++c) {
