@@ -64,9 +64,12 @@ typedef enum {
  * split. */
 typedef struct {
   double leaf_ms;         /* leaf sweeps (anti-diagonal steps inside tiles) */
-  double prop1_ms;        /* propagation stage 1: row accumulators
-                             R^T += U_A^T E^T (off the critical stream) */
-  double prop2_ms;        /* propagation stage 2: W~ -= U_B^T R */
+  double prop1_ms;        /* propagation launches with row updates of the
+                             accumulators R^T += U_A^T E^T (off the critical
+                             stream), including the pushes launched together
+                             with them */
+  double prop2_ms;        /* propagation launches of pushes alone,
+                             W~ -= U_B^T R */
   double other_ms;        /* padding, factor transposition/split */
   double prop_flops;      /* executed propagation flops (both stages) */
   int64_t leaf_launches;
