@@ -42,7 +42,8 @@
 // split by the tile anti-diagonal of the R tile (stage 1) or target (stage
 // 2) into chunks [Dm, Dm+1), [Dm+1, Dm+2), [Dm+2, Dm+4), ...: every chunk is
 // due at the near products of its first diagonal, which wait for it; the
-// chunk due next runs on a high-priority stream, the later ones lower.
+// chunk due next runs on a high-priority stream, the later ones lower.  A
+// chunk's two stages touch different tiles and go out as one launch.
 #include <algorithm>
 #include <climits>
 #include <cstring>
