@@ -336,6 +336,24 @@ def test_solve_schedule_full_size_shapes(M, N):
     np.testing.assert_array_equal(count, expected_counts(M, N))
 
 
+@pytest.mark.parametrize("M,N", SHAPES + [(64, 64), (32, 112), (112, 32)])
+def test_solve_schedule_executes_each_product_once(M, N):
+    """No redundant tile products: with the row accumulators kept for the
+    whole solve, each row update E[I,J] U_A[J,J'] (J <= J', the own term
+    J = J' only where a row below reads it) and each push U_B[I,I']^T R[I,J']
+    (I <= I', the diagonal-block term I = I' only for J' >= 1) is one 128^3
+    product, so the K tiles of all items add up to
+    M N (N + 1) / 2 - N + N M (M + 1) / 2 - M = M N (M + N) / 2 + M N - M - N,
+    the method's m n (m + n) count at tile granularity plus the diagonal
+    blocks."""
+    ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
+    total = 0
+    for dlo, dhi, off1, n1, off, nn in chunks.tolist():
+        total += int(np.sum(items[off1:off1 + n1, 3] - items[off1:off1 + n1, 2]))
+        total += int(np.sum(items[off:off + nn, 3] - items[off:off + nn, 2]))
+    assert total == M * N * (M + N) // 2 + M * N - M - N
+
+
 @pytest.mark.parametrize("M,N", SHAPES + [(64, 64), (32, 112)])
 def test_solve_streams_order_every_tile_access(M, N):
     ops, chunks, items = parse_solve(kb.schedule_export(kb.SCHEDULE_SOLVE, M, N))
